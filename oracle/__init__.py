@@ -1,0 +1,38 @@
+"""CPU oracle for top-k sparse attention prefill -- TEST INFRASTRUCTURE ONLY.
+
+Plain, slow, obviously correct numpy (float64) restatements of what the sparse
+prefill path computes.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+``bench.py``'s CPU-baseline / reference arm may import or run anything in this
+package.  The product path (the CUDA library and its Python binding) never
+imports it, and this package imports nothing from the product path: the two
+share only the seeded input generators, which hold none of the method's
+arithmetic and are passed in here as plain arrays.
+
+Functions and the passages they follow:
+
+* ``attention.sparse_prefill`` -- per-token sparse attention: for every query
+  row, the query heads sharing one KV head attend over the gathered K/V rows
+  of that row's selected slots (-1 = padding), scaled dot product, softmax,
+  O and the per-head log-sum-exp.  Pages: "[QSA] Tune sm120 sparse prefill
+  geometry" (Motivation: one program per query row, the [BLOCK_M, 256] fp32
+  accumulator over up to 2051 gathered slots; Tests: the FP32 torch sparse
+  attention reference, negative and out-of-range indices) and "DSA prefill
+  ... triton_sparse_mla" (Motivation: online softmax in registers; Robustness:
+  -1 marks an invalid slot, topk_length from metadata).
+* ``union.sorted_rows`` / ``union.union_build`` -- the G-token union with its
+  ownership bitmask ("DSA prefill ... triton_sparse_mla", Modifications: rows
+  sorted on their own, a token emits a row if no earlier token of the group
+  selected it and ORs in the bit of every token that did; Accuracy Tests: the
+  dedup contract -- each row once, bits = OR of owners, -1 dropped).
+* ``union.union_attention`` -- attention of each token of a group over the
+  union list restricted to its own ownership bit (same page: the bitmask
+  restores each token's own softmax support, identical to per-token).
+
+Every function is pinned by ``tests/test_oracle_pins.py`` against facts that
+do not come from this package: dense causal attention from a library routine
+(sparse must equal dense when the selection is the whole causal prefix), a
+library log-sum-exp, closed forms, invariances, and brute-force set
+arithmetic for the union.
+"""
+from .attention import sparse_prefill, sparse_prefill_rows, valid_slots  # noqa: F401
+from .union import sorted_rows, union_build, union_attention  # noqa: F401
