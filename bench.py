@@ -1,0 +1,425 @@
+"""Benchmark: top-k sparse attention prefill on GB300 through the C ABI.
+
+Default workload: the group-6 prefill chunk -- 8192 query rows at the end of a 32768-token
+context, 6 query heads over 1 KV head, head_dim 256, topk 2051 uniformly drawn causal slots,
+bf16 q/k/v ~ N(0, 1), seeded synthetic data.  One step = one qsa_sparse_prefill call over the
+whole chunk (all stages of the hot path).
+
+Timing: W untimed warm-up steps, then K steps each bracketed by CUDA events on the launching
+stream; L2 is flushed (a 512 MiB memset) before every timed step, outside the events; the K
+steps are bracketed by a barrier + synchronize; the max over ranks is reported.  SM clocks and
+throttle reasons are sampled with nvidia-smi during the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--union G]
+  python bench.py --impl reference ...     (the CPU oracle, timed on the host cores)
+
+Under torchrun (N > 1) every rank runs its own full workload on its own GPU (weak scaling,
+no collective on the data path); value = rows of all ranks / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sparse prefill query-rows/s (topk 2051, d=256, bf16) and % of gather/MMA roofline"
+UNIT = "query-rows/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["top_sparse_attention_row_gb300/csrc/prefill.cu",
+                  "top_sparse_attention_row_gb300/csrc/ptx.cuh",
+                  "top_sparse_attention_row_gb300/csrc/internal.h"]
+
+DESCRIPTIONS = {
+    "group6_32k": "group-6 prefill chunk: 8192 rows at the end of a 32768 context, 6 Q / 1 KV, "
+                  "head_dim 256, topk 2051 uniform causal slots",
+    "group12_128k": "group-12 long context: 8192 rows at the end of a 131072 context, 24 Q / 2 KV, "
+                    "head_dim 256, topk 2051 uniform causal slots",
+    "group12_128k_12q1kv": "group-12 long context, 12 Q / 1 KV rank shape",
+    "union_8k": "8192-token prefill from position 0, 8 Q / 1 KV, topk 2048, random-walk indices",
+    "mixed_paged": "mixed batch 512/2048/4096/8192 new tokens over prefixes 0/16k/32k/64k, "
+                   "6 Q / 1 KV, topk 2051, per-row topk_len, paged cache (64), shuffled pages",
+    "tiny": "tiny: 256 rows at positions 256..511, 6 Q / 1 KV, topk 128",
+}
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_stats(w):
+    """Algorithmic FLOPs / bytes of one call (unpadded heads, valid slots only)."""
+    v = w.valid_counts().astype(np.int64)
+    D, Hq, Hkv = w.head_dim, w.n_qheads, w.n_kvheads
+    flops = int(4 * Hq * D * v.sum())                       # QK^T + PV, 2 flops per MAC
+    idx = w.indices
+    mask = idx >= 0
+    if w.topk_len is not None:
+        mask &= np.arange(idx.shape[1])[None, :] < np.clip(w.topk_len, 0, idx.shape[1])[:, None]
+    unique_slots = int(np.unique(idx[mask]).size)
+    kv_unique = unique_slots * Hkv * D * 2 * 2               # K and V rows, bf16
+    io = (2 * w.n_rows * Hq * D * 2 + idx.size * 4 + w.n_rows * Hq * 4
+          + (0 if w.topk_len is None else w.n_rows * 4))
+    gathered = int(v.sum()) * Hkv * D * 2 * 2                 # every (row, slot) K+V read
+    return dict(flops=flops, bytes=kv_unique + io, unique_slots=unique_slots, gathered=gathered,
+                valid_slots=int(v.sum()))
+
+
+# ------------------------------------------------------------------------- CPU oracle leg
+
+_W = None
+
+
+def _oracle_init(name, seed_kw):
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    global _W
+    from top_sparse_attention_row_gb300 import workloads as W
+    _W = W.make(name, **seed_kw)
+
+
+def _oracle_rows(rows):
+    import oracle
+    w = _W
+    oracle.sparse_prefill_rows(w.q, w.k, w.v, w.indices, w.topk_len, w.scale, rows)
+    return len(rows)
+
+
+def oracle_pool(name, seed_kw, cores):
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    ctx = mp.get_context("spawn")
+    return ctx.Pool(cores, initializer=_oracle_init, initargs=(name, seed_kw))
+
+
+def time_oracle(pool, n_rows, sample_rows, cores):
+    rows = np.linspace(0, n_rows - 1, num=min(sample_rows, n_rows)).astype(np.int64)
+    chunks = [c for c in np.array_split(rows, cores * 4) if len(c)]
+    t0 = time.perf_counter()
+    done = sum(pool.map(_oracle_rows, chunks))
+    dt = time.perf_counter() - t0
+    return done / dt, done, dt
+
+
+# ------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------------- GPU leg
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from top_sparse_attention_row_gb300 import binding, build as _build, workloads as W
+
+    _build.build()
+    binding.load_library()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    seed_kw = {} if world == 1 else {"seed": 1000 + rank}
+    w = W.make(args.config, **seed_kw)
+    stats = workload_stats(w)
+
+    # CPU baseline pool (spawned before any GPU work of this process matters; spawn is safe).
+    cpu = None
+    pool = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cores = os.cpu_count() or 1
+        pool = oracle_pool(args.config, seed_kw, cores)
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+    h_q, h_k, h_v = bf(w.q).pin_memory(), bf(w.k).pin_memory(), bf(w.v).pin_memory()
+    h_idx = torch.from_numpy(w.indices).pin_memory()
+    h_tl = None if w.topk_len is None else torch.from_numpy(w.topk_len).pin_memory()
+    q, k, v = h_q.to(dev), h_k.to(dev), h_v.to(dev)
+    idx = h_idx.to(dev)
+    tl = None if h_tl is None else h_tl.to(dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((w.n_rows, w.n_qheads), dtype=torch.float32, device=dev)
+    ws = None
+    if args.union > 1:
+        nb = binding.workspace_bytes(w.n_rows, w.topk, args.union)
+        ws = torch.empty(max(nb, 256), dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        binding.sparse_prefill(q, k, v, idx, tl, w.scale, out=out, lse=lse, union_g=args.union,
+                               workspace=ws, stream=stream)
+
+    geo = binding.select_geometry(w.n_qheads, w.n_kvheads, args.union, w.topk, w.head_dim, w.n_rows)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    if binding.device_status(stream) != 0:
+        raise RuntimeError("device wait timed out during warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    c0 = binding.counters()["kernel_launches"]
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        call()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - t_wall
+    clocks = sampler.stop() if sampler else None
+    launches = binding.counters()["kernel_launches"] - c0
+    times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(times) / len(times)
+    if binding.device_status(stream) != 0:
+        raise RuntimeError("device wait timed out during the timed region")
+
+    # end to end: pinned host inputs -> device, call, result -> host, every step
+    e_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    e_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_idx) + ((h_tl,) if h_tl is not None else ()))
+    d2h = e_out.numel() * e_out.element_size() + e_lse.numel() * e_lse.element_size()
+
+    def e2e_step():
+        q.copy_(h_q, non_blocking=True)
+        k.copy_(h_k, non_blocking=True)
+        v.copy_(h_v, non_blocking=True)
+        idx.copy_(h_idx, non_blocking=True)
+        if tl is not None:
+            tl.copy_(h_tl, non_blocking=True)
+        call()
+        e_out.copy_(out, non_blocking=True)
+        e_lse.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_times = []
+    for _ in range(args.steps):
+        flush.zero_()
+        s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s_ev.record(stream)
+        e2e_step()
+        e_ev.record(stream)
+        torch.cuda.synchronize()
+        e_times.append(s_ev.elapsed_time(e_ev))
+    e_ms = sum(e_times) / len(e_times)
+
+    # max over ranks
+    if world > 1:
+        t = torch.tensor([ms, e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e_ms = float(t[0]), float(t[1])
+
+    if rank != 0:
+        return None
+
+    if pool is not None:
+        cores = os.cpu_count() or 1
+        rps, done, dt = time_oracle(pool, w.n_rows, args.cpu_rows, cores)
+        pool.close()
+        pool.join()
+        cpu = {"value": rps, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{done} of {w.n_rows} rows of the same workload (evenly spaced), "
+                         f"numpy float64 oracle in {cores} spawned single-threaded processes, "
+                         f"{dt:.2f} s wall"}
+
+    peaks, peak_src = load_peaks()
+    kernel_s = ms / 1e3
+    t_tc = stats["flops"] / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = stats["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    bound = "tensor" if t_tc >= t_hbm else "hbm"
+    if bound == "tensor":
+        achieved = stats["flops"] / kernel_s / 1e12
+        peak, unit = peaks["bf16_tflops"], "TFLOP/s"
+    else:
+        achieved = stats["bytes"] / kernel_s / 1e9
+        peak, unit = peaks["hbm_gbs"], "GB/s"
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            tj = json.load(f)
+        key = f"{args.config}:union{args.union}"
+        ent = tj.get(key)
+        if ent and ent.get("kernel_sha") == kernel_sha():
+            traffic = ent.get("dram_bytes_per_launch")
+    roofline = {
+        "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+        "frac": achieved / peak, "traffic": traffic,
+        "peak_source": f"{peak_src} (MEASURED_PEAKS.json bf16 burst / hbm copy)",
+        "algorithmic_flops": stats["flops"], "algorithmic_bytes": stats["bytes"],
+        "roofline_us": max(t_tc, t_hbm) * 1e6,
+        "gathered_bytes": stats["gathered"],
+        "gather_gbs": stats["gathered"] / kernel_s / 1e9,
+        "kernel_ms": ms,
+    }
+    rows_total = w.n_rows * world
+    line = {
+        "metric": METRIC, "value": rows_total / kernel_s, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; no dataset or weights)",
+        "config": {"workload": DESCRIPTIONS.get(args.config, args.config), "name": args.config,
+                   "rows": w.n_rows, "n_qheads": w.n_qheads, "n_kvheads": w.n_kvheads,
+                   "head_dim": w.head_dim, "topk": w.topk, "union_g": args.union,
+                   "valid_slots": stats["valid_slots"], "geometry": geo,
+                   "l2": "flushed before every timed step (512 MiB memset outside the events)",
+                   "parallelism": f"{world} independent shard(s), no collective"},
+        "roofline": roofline,
+        "e2e": {"value": rows_total / (e_ms / 1e3), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "wall_s_timed_region": wall,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    return line
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm, timed on this host's cores."""
+    if rank != 0:
+        return None
+    from top_sparse_attention_row_gb300 import workloads as W
+    w = W.make(args.config)
+    cores = os.cpu_count() or 1
+    pool = oracle_pool(args.config, {}, cores)
+    sample = min(w.n_rows, args.cpu_rows)
+    for _ in range(args.warmup):
+        time_oracle(pool, w.n_rows, max(cores, sample // 8), cores)
+    vals, secs = [], []
+    for _ in range(args.steps):
+        rps, done, dt = time_oracle(pool, w.n_rows, sample, cores)
+        vals.append(rps)
+        secs.append(dt)
+    pool.close()
+    pool.join()
+    value = statistics.median(vals)
+    ms = 1e3 * w.n_rows / value
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; no dataset or weights)",
+        "impl": "reference",
+        "config": {"workload": DESCRIPTIONS.get(args.config, args.config), "name": args.config,
+                   "rows": w.n_rows, "n_qheads": w.n_qheads, "n_kvheads": w.n_kvheads,
+                   "head_dim": w.head_dim, "topk": w.topk, "union_g": args.union},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{sample} of {w.n_rows} rows per step (evenly spaced), numpy "
+                                   f"float64 oracle in {cores} spawned single-threaded processes"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="group6_32k")
+    ap.add_argument("--union", type=int, default=0)
+    ap.add_argument("--cpu-rows", type=int, default=8192)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    line = run_gpu(args, rank, world, local_rank)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,149 @@
+/*
+ * qsa.h -- C ABI of the top-k sparse attention prefill library (libqsa.so), GB300 / sm_103a.
+ *
+ * The operation ("[QSA] Tune sm120 sparse prefill geometry", Motivation; "DSA prefill ...
+ * triton_sparse_mla", Motivation and Modifications): an indexer has chosen, for every query
+ * row, up to `topk` KV token slots (int32, negative = padding).  For each row, the query
+ * heads that share one KV head attend only over the K/V rows gathered at those slots --
+ * scaled dot product, numerically stable softmax -- and the library writes O and the
+ * per-head natural-log log-sum-exp of the scaled logits.  Optionally G adjacent rows share
+ * one gathered union of their slots, with a per-slot ownership bitmask that keeps every
+ * row's own softmax support (same page, Modifications: union mode).
+ *
+ * Conventions for every entry point:
+ *  - Layouts are contiguous, row-major:
+ *      q        [n_rows, n_qheads, head_dim]   bf16
+ *      k_cache  [n_slots, n_kvheads, head_dim] bf16   (physical slots)
+ *      v_cache  [n_slots, n_kvheads, head_dim] bf16
+ *      indices  [n_rows, topk]                 int32  physical slots; < 0 = padding
+ *      topk_len [n_rows]                       int32  leading slots considered (clamped to
+ *                                                     [0, topk]); NULL = all topk
+ *      out      [n_rows, n_qheads, head_dim]   bf16   (the [tokens, heads, d_v] contract)
+ *      lse      [n_rows, n_qheads]             fp32   NULL = not written
+ *    One index row serves every KV head; query head h reads KV head h / (n_qheads/n_kvheads).
+ *  - Every pointer argument except the ones marked host-side is a DEVICE pointer of the
+ *    current CUDA device.  The caller owns all memory; the library never frees or keeps a
+ *    pointer past the call.  q, k_cache, v_cache and out must be 16-byte aligned.
+ *  - Work is enqueued on `stream` (a cudaStream_t passed as void*; NULL = legacy default
+ *    stream).  Calls return before the GPU finishes and make no host synchronisation.
+ *  - No exception crosses the ABI.  Argument errors are detected on the host before any
+ *    GPU work and return a status; nothing is enqueued then.
+ *  - A row with no valid slot gets O = 0 and LSE = -inf.  A slot listed twice in one row is
+ *    weighted twice (per-token path).
+ *  - Results are deterministic: no atomics take part in any reduction.
+ */
+#ifndef QSA_H_
+#define QSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum qsa_status {
+  QSA_OK = 0,
+  QSA_ERR_INVALID_ARG = 1,   /* null required pointer, bad size, misaligned pointer */
+  QSA_ERR_UNSUPPORTED = 2,   /* head_dim != 256, device is not sm_103, shape beyond limits */
+  QSA_ERR_WORKSPACE = 3,     /* caller workspace smaller than qsa_workspace_bytes() */
+  QSA_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
+  QSA_ERR_TIMEOUT = 5        /* a kernel wait ran past its limit (see qsa_get_device_status) */
+} qsa_status;
+
+/* Launch geometry chosen by the selector ("[QSA] Tune sm120 sparse prefill geometry",
+ * Modifications: a measured launch table per group size, top-k and head dimension). */
+typedef struct qsa_geometry {
+  int32_t tile_tokens;      /* gathered slots per MMA tile (128) */
+  int32_t stages;           /* shared-memory pipeline stages, each 128 slots x 128 dims bf16 */
+  int32_t n_pad;            /* MMA N: query columns of a tile, padded to a multiple of 16 */
+  int32_t cols;             /* real query columns of a tile (heads x rows of the group) */
+  int32_t head_chunks;      /* tiles of query heads per KV head (1 unless the group > 64) */
+  int32_t union_g;          /* effective union group size (1 = per-token) */
+  int32_t grid;             /* CTAs launched (persistent, <= SM count) */
+  int32_t threads;          /* threads per CTA */
+  int32_t smem_bytes;       /* dynamic shared memory per CTA */
+  int32_t tmem_cols;        /* tensor-memory columns allocated per CTA */
+  int64_t n_items;          /* work items: row groups x KV heads x head chunks */
+} qsa_geometry;
+
+/* Per-path call counters (host side, process wide), in the spirit of the pages' invocation
+ * counts ("DSA prefill ... triton_sparse_mla", Speed Tests: every run counts invocations of
+ * the kernel so a silent no-op cannot pass for a win). */
+typedef struct qsa_counters {
+  uint64_t calls_per_token;    /* calls served by the per-token path */
+  uint64_t calls_union;        /* calls served by the union path */
+  uint64_t union_fallbacks;    /* union requested but illegal for the shape -> per-token */
+  uint64_t step_downs;         /* forced geometry stepped down to fit shared memory */
+  uint64_t kernel_launches;    /* kernels enqueued by this library */
+} qsa_counters;
+
+/* Main entry: sparse prefill attention for all rows.
+ *   union_g: 0 or 1 = per-token path; 2..8 = union of union_g consecutive rows with ownership
+ *            bits.  A union shape the kernel cannot tile (union_g * group > 64) runs the
+ *            per-token path instead and counts a fallback; the result is the same.  Union mode
+ *            requires each row's valid slots to be distinct (a repeated slot is used once).
+ *   Slots must be < n_slots of the caches (not checked: the signature carries no slot
+ *   count; use qsa_sparse_prefill_ex with n_kv_slots to have them treated as padding).
+ *   Union mode allocates its workspace on `stream` (cudaMallocAsync / cudaFreeAsync). */
+qsa_status qsa_sparse_prefill(const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* indices, const int32_t* topk_len,
+                              void* out, float* lse,
+                              int64_t n_rows, int32_t n_qheads, int32_t n_kvheads,
+                              int32_t head_dim, int32_t topk, float scale,
+                              int32_t union_g, void* stream);
+
+/* Extended entry.
+ *   n_kv_slots: 0 = unchecked; > 0 = slots >= n_kv_slots are padding (and gathers are
+ *               bounds-checked against it).
+ *   workspace / workspace_bytes: caller scratch for union mode (NULL = allocate on stream);
+ *               must hold qsa_workspace_bytes(n_rows, topk, effective union_g) bytes and be
+ *               256-byte aligned.  Unused by the per-token path.
+ *   forced:     host pointer, NULL = selector; fields > 0 override stages and grid (an
+ *               oversized stage count is stepped down to fit and counted). */
+qsa_status qsa_sparse_prefill_ex(const void* q, const void* k_cache, const void* v_cache,
+                                 const int32_t* indices, const int32_t* topk_len,
+                                 void* out, float* lse,
+                                 int64_t n_rows, int32_t n_qheads, int32_t n_kvheads,
+                                 int32_t head_dim, int32_t topk, float scale,
+                                 int32_t union_g, int64_t n_kv_slots,
+                                 void* workspace, size_t workspace_bytes,
+                                 const qsa_geometry* forced, void* stream);
+
+/* Bytes of union-mode workspace for a call (0 when union_g <= 1). */
+size_t qsa_workspace_bytes(int64_t n_rows, int32_t topk, int32_t union_g);
+
+/* Union build on its own ("DSA prefill ... triton_sparse_mla", Modifications and Accuracy
+ * Tests: each row sorted on its own; a row emits a slot no earlier row of its group
+ * selected and ORs in the bit of every row that did; each slot once, -1 dropped).
+ *   sorted_out [n_rows, topk] (nullable): each row's valid slots ascending, then -1.
+ *   union_idx  [n_groups, union_g*topk]: group list, canonical order (row 0's emitted slots
+ *              ascending, then row 1's, ...), -1 padded.
+ *   union_bits [n_groups, union_g*topk] uint8: bit u = row u of the group owns the slot; 0 pad.
+ *   union_len  [n_groups]: emitted count.  n_groups = ceil(n_rows / union_g); the last group
+ *              may hold fewer rows.  union_g in [1, 8]. */
+qsa_status qsa_union_build(const int32_t* indices, const int32_t* topk_len,
+                           int64_t n_rows, int32_t topk, int32_t union_g, int64_t n_kv_slots,
+                           int32_t* sorted_out, int32_t* union_idx, uint8_t* union_bits,
+                           int32_t* union_len, void* stream);
+
+/* Host-only geometry selection (no GPU needed).  num_sms <= 0 queries the current device.
+ * Returns QSA_ERR_UNSUPPORTED for shapes the kernel cannot run. */
+qsa_status qsa_select_geometry(int32_t n_qheads, int32_t n_kvheads, int32_t union_g,
+                               int32_t topk, int32_t head_dim, int64_t n_rows,
+                               int32_t num_sms, qsa_geometry* out);
+
+void qsa_get_counters(qsa_counters* out);   /* host pointer */
+void qsa_reset_counters(void);
+const char* qsa_status_string(qsa_status s);
+const char* qsa_version(void);
+
+/* Reads and clears the device status word that kernels set when a bounded wait gives up
+ * (0 = no error).  Synchronises `stream`.  Returns QSA_ERR_TIMEOUT if the word was set. */
+qsa_status qsa_get_device_status(void* stream, int32_t* status_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QSA_H_ */

@@ -1,0 +1,112 @@
+"""The C-ABI library builds, loads on a CPU-only machine and exports every declared symbol;
+host-side validation and geometry selection (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from top_sparse_attention_row_gb300 import build, binding
+    build.build()
+    return binding.load_library()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "qsa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(qsa_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from top_sparse_attention_row_gb300 import binding
+    names = declared_functions()
+    assert set(names) == set(binding.EXPORTED), names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version_and_status_strings(lib):
+    from top_sparse_attention_row_gb300 import binding
+    assert "sm_103a" in binding.version()
+    for s in range(6):
+        assert lib.qsa_status_string(s)
+
+
+def test_selector_configs(lib):
+    from top_sparse_attention_row_gb300 import binding as B
+    g = B.select_geometry(6, 1, 0, 2051, 256, 8192, 152)
+    assert g["n_pad"] == 16 and g["cols"] == 6 and g["union_g"] == 1 and g["grid"] == 152
+    assert g["stages"] >= 4 and g["smem_bytes"] <= 232448 and g["n_items"] == 8192
+    g = B.select_geometry(24, 2, 0, 2051, 256, 8192, 152)
+    assert g["n_pad"] == 16 and g["cols"] == 12 and g["n_items"] == 16384
+    g = B.select_geometry(8, 1, 4, 2048, 256, 8192, 152)
+    assert g["union_g"] == 4 and g["n_pad"] == 32 and g["n_items"] == 2048
+    g = B.select_geometry(8, 1, 2, 2048, 256, 8192, 152)
+    assert g["union_g"] == 2 and g["n_pad"] == 16
+    g = B.select_geometry(6, 1, 0, 128, 256, 256, 152)
+    assert g["grid"] == 152 and g["n_items"] == 256
+    g = B.select_geometry(6, 1, 0, 128, 256, 10, 152)
+    assert g["grid"] == 10
+    assert g["tmem_cols"] in (32, 64, 128, 256, 512) and g["tmem_cols"] >= 4 * g["n_pad"]
+
+
+def test_selector_union_fallback_and_head_chunks(lib):
+    from top_sparse_attention_row_gb300 import binding as B
+    # 32 heads per KV group x G=4 = 128 columns > 64: falls back to per-token
+    g = B.select_geometry(32, 1, 4, 2048, 256, 100, 152)
+    assert g["union_g"] == 1 and g["n_pad"] == 32
+    # 96 heads per group: two chunks of 48 columns
+    g = B.select_geometry(96, 1, 0, 2048, 256, 100, 152)
+    assert g["head_chunks"] == 2 and g["cols"] == 48 and g["n_pad"] == 48 and g["n_items"] == 200
+    # odd union sizes are legal shapes in this kernel
+    g = B.select_geometry(6, 1, 3, 2048, 256, 100, 152)
+    assert g["union_g"] == 3 and g["n_pad"] == 32 and g["n_items"] == 34
+
+
+@pytest.mark.parametrize("args,status", [
+    ((6, 1, 0, 2051, 128, 10, 152), 2),     # head_dim != 256
+    ((6, 4, 0, 2051, 256, 10, 152), 1),     # Hq % Hkv != 0
+    ((6, 1, 9, 2051, 256, 10, 152), 1),     # union_g > 8
+    ((6, 1, 0, 0, 256, 10, 152), 1),        # topk <= 0
+    ((6, 1, 0, 2051, 256, -1, 152), 1),     # n_rows < 0
+    ((6, 1, 0, 1 << 20, 256, 10, 152), 2),  # per-token slot list cannot fit shared memory
+])
+def test_selector_rejections(lib, args, status):
+    from top_sparse_attention_row_gb300 import binding as B
+    assert B.select_geometry_status(*args) == status
+
+
+def test_entry_validation_before_any_cuda_call(lib):
+    """Argument errors come back as statuses without touching the (absent) GPU."""
+    f = lib.qsa_sparse_prefill
+    fake = 1 << 20                     # 16-byte aligned non-null stand-in, never dereferenced
+    assert f(None, fake, fake, fake, None, fake, None, 10, 6, 1, 256, 2051, 0.0625, 0, None) == 1
+    assert f(fake + 2, fake, fake, fake, None, fake, None, 10, 6, 1, 256, 2051, 0.0625, 0, None) == 1
+    assert f(fake, fake, fake, fake, None, fake, None, 10, 6, 1, 128, 2051, 0.0625, 0, None) == 2
+    assert f(fake, fake, fake, fake, None, fake, None, 10, 6, 4, 256, 2051, 0.0625, 0, None) == 1
+    assert f(fake, fake, fake, fake, None, fake, None, 10, 6, 1, 256, 2051, float("nan"), 0, None) == 1
+    assert f(fake, fake, fake, fake, None, fake, None, 0, 6, 1, 256, 2051, 0.0625, 0, None) == 0
+    ub = lib.qsa_union_build
+    assert ub(None, None, 10, 16, 2, 0, None, fake, fake, fake, None) == 1
+    assert ub(fake, None, 10, 16, 0, 0, None, fake, fake, fake, None) == 1
+    assert ub(fake, None, 10, 1 << 16, 8, 0, None, fake, fake, fake, None) == 2
+
+
+def test_workspace_bytes(lib):
+    from top_sparse_attention_row_gb300 import binding as B
+    assert B.workspace_bytes(8192, 2048, 1) == 0
+    n = B.workspace_bytes(8192, 2048, 4)
+    groups = 2048
+    assert n >= groups * 4 * 2048 * 5 + groups * 4 and n % 256 == 0
+    assert B.workspace_bytes(1023, 16, 4) >= 256 * 64 * 5
+
+
+def test_counters_reset(lib):
+    from top_sparse_attention_row_gb300 import binding as B
+    B.reset_counters()
+    assert all(v == 0 for v in B.counters().values())

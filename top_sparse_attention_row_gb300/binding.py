@@ -1,0 +1,222 @@
+"""Thin ctypes binding over libqsa.so (argument marshalling only).
+
+Every step of the sparse prefill runs in the library's CUDA kernels; this module only
+checks tensor dtypes / shapes / devices and passes raw pointers and sizes through the C ABI
+declared in ``include/qsa.h``.  It raises ``RuntimeError`` on any non-OK status and refuses
+to run when the library has not been built -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libqsa.so")
+
+QSA_OK = 0
+STATUS_NAMES = {0: "QSA_OK", 1: "QSA_ERR_INVALID_ARG", 2: "QSA_ERR_UNSUPPORTED",
+                3: "QSA_ERR_WORKSPACE", 4: "QSA_ERR_CUDA", 5: "QSA_ERR_TIMEOUT"}
+
+# Every symbol include/qsa.h declares (checked by the CPU test suite).
+EXPORTED = ["qsa_sparse_prefill", "qsa_sparse_prefill_ex", "qsa_workspace_bytes",
+            "qsa_union_build", "qsa_select_geometry", "qsa_get_counters", "qsa_reset_counters",
+            "qsa_status_string", "qsa_version", "qsa_get_device_status"]
+
+
+class Geometry(ctypes.Structure):
+    _fields_ = [("tile_tokens", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("n_pad", ctypes.c_int32), ("cols", ctypes.c_int32),
+                ("head_chunks", ctypes.c_int32), ("union_g", ctypes.c_int32),
+                ("grid", ctypes.c_int32), ("threads", ctypes.c_int32),
+                ("smem_bytes", ctypes.c_int32), ("tmem_cols", ctypes.c_int32),
+                ("n_items", ctypes.c_int64)]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class Counters(ctypes.Structure):
+    _fields_ = [("calls_per_token", ctypes.c_uint64), ("calls_union", ctypes.c_uint64),
+                ("union_fallbacks", ctypes.c_uint64), ("step_downs", ctypes.c_uint64),
+                ("kernel_launches", ctypes.c_uint64)]
+
+    def as_dict(self):
+        return {name: int(getattr(self, name)) for name, _ in self._fields_}
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libqsa.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libqsa.so not built at {path}; run __graft_entry__.build() "
+                           "or python -m top_sparse_attention_row_gb300.build")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    lib.qsa_sparse_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, f32, i32, vp]
+    lib.qsa_sparse_prefill.restype = ctypes.c_int
+    lib.qsa_sparse_prefill_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, f32, i32,
+                                          i64, vp, sz, ctypes.POINTER(Geometry), vp]
+    lib.qsa_sparse_prefill_ex.restype = ctypes.c_int
+    lib.qsa_workspace_bytes.argtypes = [i64, i32, i32]
+    lib.qsa_workspace_bytes.restype = sz
+    lib.qsa_union_build.argtypes = [vp, vp, i64, i32, i32, i64, vp, vp, vp, vp, vp]
+    lib.qsa_union_build.restype = ctypes.c_int
+    lib.qsa_select_geometry.argtypes = [i32, i32, i32, i32, i32, i64, i32, ctypes.POINTER(Geometry)]
+    lib.qsa_select_geometry.restype = ctypes.c_int
+    lib.qsa_get_counters.argtypes = [ctypes.POINTER(Counters)]
+    lib.qsa_get_counters.restype = None
+    lib.qsa_reset_counters.argtypes = []
+    lib.qsa_reset_counters.restype = None
+    lib.qsa_status_string.argtypes = [ctypes.c_int]
+    lib.qsa_status_string.restype = ctypes.c_char_p
+    lib.qsa_version.argtypes = []
+    lib.qsa_version.restype = ctypes.c_char_p
+    lib.qsa_get_device_status.argtypes = [vp, ctypes.POINTER(i32)]
+    lib.qsa_get_device_status.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _check(status: int, what: str):
+    if status != QSA_OK:
+        msg = load_library().qsa_status_string(status).decode()
+        raise RuntimeError(f"{what} failed: {STATUS_NAMES.get(status, status)} ({msg})")
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _require(t, dtype, name, ndim=None):
+    import torch
+    if t is None:
+        return
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims")
+
+
+def sparse_prefill(q, k_cache, v_cache, indices, topk_len, scale: float, *, out=None, lse=None,
+                   union_g: int = 0, n_kv_slots: int = 0, workspace=None, forced: Optional[dict] = None,
+                   want_lse: bool = True, stream=None):
+    """O (bf16 [R, Hq, D]) and LSE (fp32 [R, Hq]) of top-k sparse attention prefill.
+
+    q [R, Hq, D] bf16, k_cache / v_cache [S, Hkv, D] bf16, indices [R, topk] int32 (physical
+    slots, negative = padding), topk_len [R] int32 or None.  Calls qsa_sparse_prefill (or the
+    _ex entry when n_kv_slots / workspace / forced are given) on the current stream.
+    """
+    import torch
+    lib = load_library()
+    _require(q, torch.bfloat16, "q", 3)
+    _require(k_cache, torch.bfloat16, "k_cache", 3)
+    _require(v_cache, torch.bfloat16, "v_cache", 3)
+    _require(indices, torch.int32, "indices", 2)
+    _require(topk_len, torch.int32, "topk_len", 1)
+    R, Hq, D = q.shape
+    Hkv = k_cache.shape[1]
+    topk = indices.shape[1]
+    if indices.shape[0] != R or (topk_len is not None and topk_len.shape[0] != R):
+        raise ValueError("indices / topk_len rows must match q")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((R, Hq), dtype=torch.float32, device=q.device)
+    _require(out, torch.bfloat16, "out", 3)
+    _require(lse, torch.float32, "lse", 2)
+    s = _stream_ptr(stream)
+    if n_kv_slots or workspace is not None or forced:
+        g = None
+        if forced:
+            g = Geometry()
+            for k, v in forced.items():
+                setattr(g, k, v)
+        ws_ptr = None if workspace is None else workspace.data_ptr()
+        ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        st = lib.qsa_sparse_prefill_ex(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(indices),
+                                       _ptr(topk_len), _ptr(out), _ptr(lse), R, Hq, Hkv, D, topk,
+                                       float(scale), int(union_g), int(n_kv_slots), ws_ptr, ws_bytes,
+                                       None if g is None else ctypes.byref(g), s)
+    else:
+        st = lib.qsa_sparse_prefill(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(indices),
+                                    _ptr(topk_len), _ptr(out), _ptr(lse), R, Hq, Hkv, D, topk,
+                                    float(scale), int(union_g), s)
+    _check(st, "qsa_sparse_prefill")
+    return out, lse
+
+
+def union_build(indices, topk_len, union_g: int, n_kv_slots: int = 0, want_sorted: bool = True,
+                stream=None):
+    """Runs qsa_union_build; returns (sorted [R, K] or None, union_idx, union_bits, union_len)."""
+    import torch
+    lib = load_library()
+    _require(indices, torch.int32, "indices", 2)
+    _require(topk_len, torch.int32, "topk_len", 1)
+    R, K = indices.shape
+    n_groups = -(-R // union_g)
+    dev = indices.device
+    srt = torch.empty((R, K), dtype=torch.int32, device=dev) if want_sorted else None
+    uidx = torch.empty((n_groups, union_g * K), dtype=torch.int32, device=dev)
+    ubits = torch.empty((n_groups, union_g * K), dtype=torch.uint8, device=dev)
+    ulen = torch.empty((n_groups,), dtype=torch.int32, device=dev)
+    st = lib.qsa_union_build(_ptr(indices), _ptr(topk_len), R, K, int(union_g), int(n_kv_slots),
+                             _ptr(srt), _ptr(uidx), _ptr(ubits), _ptr(ulen), _stream_ptr(stream))
+    _check(st, "qsa_union_build")
+    return srt, uidx, ubits, ulen
+
+
+def workspace_bytes(n_rows: int, topk: int, union_g: int) -> int:
+    return int(load_library().qsa_workspace_bytes(n_rows, topk, union_g))
+
+
+def select_geometry(n_qheads, n_kvheads, union_g, topk, head_dim, n_rows, num_sms=0) -> dict:
+    g = Geometry()
+    st = load_library().qsa_select_geometry(n_qheads, n_kvheads, union_g, topk, head_dim, n_rows,
+                                            num_sms, ctypes.byref(g))
+    _check(st, "qsa_select_geometry")
+    return g.as_dict()
+
+
+def select_geometry_status(n_qheads, n_kvheads, union_g, topk, head_dim, n_rows, num_sms) -> int:
+    g = Geometry()
+    return int(load_library().qsa_select_geometry(n_qheads, n_kvheads, union_g, topk, head_dim,
+                                                  n_rows, num_sms, ctypes.byref(g)))
+
+
+def counters() -> dict:
+    c = Counters()
+    load_library().qsa_get_counters(ctypes.byref(c))
+    return c.as_dict()
+
+
+def reset_counters():
+    load_library().qsa_reset_counters()
+
+
+def device_status(stream=None) -> int:
+    v = ctypes.c_int32(0)
+    st = load_library().qsa_get_device_status(_stream_ptr(stream), ctypes.byref(v))
+    if st not in (0, 5):
+        _check(st, "qsa_get_device_status")
+    return int(v.value)
+
+
+def version() -> str:
+    return load_library().qsa_version().decode()

@@ -1,0 +1,346 @@
+// C-ABI entry points of libqsa: argument validation, the launch-geometry selector, union-mode
+// workspace handling, counters and status reporting.  Every argument error is caught here,
+// before any CUDA call, so a bad call enqueues nothing.
+#include <atomic>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+
+#include "internal.h"
+
+namespace {
+
+using qsa::Geometry;
+
+std::atomic<uint64_t> g_calls_per_token{0}, g_calls_union{0}, g_union_fallbacks{0},
+    g_step_downs{0}, g_launches{0};
+
+constexpr size_t kWsAlign = 256;
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+int pow2_at_least(int v) {
+  int p = 32;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+struct WsLayout {
+  size_t idx, bits, len, total;
+};
+WsLayout ws_layout(int64_t n_rows, int32_t topk, int32_t G) {
+  WsLayout w{};
+  if (G <= 1 || n_rows <= 0) return w;
+  const int64_t n_groups = ceil_div(n_rows, G);
+  const size_t cap = static_cast<size_t>(n_groups) * G * topk;
+  w.idx = 0;
+  w.bits = round_up(static_cast<int64_t>(cap * 4), kWsAlign);
+  w.len = w.bits + round_up(static_cast<int64_t>(cap), kWsAlign);
+  w.total = w.len + round_up(n_groups * 4, kWsAlign);
+  return w;
+}
+
+// Pure host selection.  `forced` may override stages / grid; an oversized stage count steps
+// down to the largest that fits ("DSA prefill ... triton_sparse_mla", Robustness: the launcher
+// steps the shared-memory tile down instead of failing).
+qsa_status select(int32_t Hq, int32_t Hkv, int32_t union_g, int32_t topk, int32_t head_dim,
+                  int64_t n_rows, int32_t num_sms, const qsa_geometry* forced, Geometry* g,
+                  bool* fell_back, bool* stepped) {
+  *fell_back = false;
+  *stepped = false;
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || topk <= 0 || n_rows < 0 || head_dim <= 0 ||
+      union_g < 0 || union_g > 8 || num_sms <= 0)
+    return QSA_ERR_INVALID_ARG;
+  if (head_dim != qsa::kHeadDim) return QSA_ERR_UNSUPPORTED;
+  if (n_rows > INT32_MAX) return QSA_ERR_UNSUPPORTED;
+  const int group = Hq / Hkv;
+  int G = union_g <= 1 ? 1 : union_g;
+  if (G > 1) {
+    const bool legal = G * group <= qsa::kMaxNPad &&
+                       qsa::union_build_smem_bytes(topk, G) <= static_cast<size_t>(qsa::kUnionMaxSmem) &&
+                       static_cast<int64_t>(G) * topk <= INT32_MAX / 2;
+    if (!legal) {
+      G = 1;
+      *fell_back = true;
+    }
+  }
+  int chunks, chunk_cols, np, slot_cap;
+  if (G == 1) {
+    chunks = static_cast<int>(ceil_div(group, qsa::kMaxNPad));
+    chunk_cols = static_cast<int>(ceil_div(group, chunks));
+    np = static_cast<int>(round_up(chunk_cols, 16));
+    slot_cap = static_cast<int>(round_up(topk, qsa::kTileTokens));
+  } else {
+    chunks = 1;
+    chunk_cols = G * group;
+    np = static_cast<int>(round_up(chunk_cols, 16));
+    slot_cap = 0;
+  }
+  int stages = 0;
+  for (int s = qsa::kMaxStages; s >= qsa::kMinStages; --s) {
+    if (qsa::smem_layout(np, s, slot_cap).total <= qsa::kSmemLimit) {
+      stages = s;
+      break;
+    }
+  }
+  if (stages == 0) return QSA_ERR_UNSUPPORTED;   // per-token slot list too large for topk
+  if (forced && forced->stages > 0) {
+    int want = forced->stages < qsa::kMinStages ? qsa::kMinStages : forced->stages;
+    if (want > stages) {
+      *stepped = true;
+      want = stages;
+    }
+    stages = want;
+  }
+  const int64_t n_groups = ceil_div(n_rows, G);
+  const int64_t n_items = n_groups * Hkv * chunks;
+  int64_t grid = n_items < num_sms ? n_items : num_sms;
+  if (forced && forced->grid > 0 && forced->grid < grid) grid = forced->grid;
+  g->np = np;
+  g->cols = chunk_cols;
+  g->head_chunks = chunks;
+  g->chunk_cols = chunk_cols;
+  g->union_g = G;
+  g->stages = stages;
+  g->grid = static_cast<int>(grid);
+  g->smem_bytes = qsa::smem_layout(np, stages, slot_cap).total;
+  g->tmem_cols = pow2_at_least(4 * np);
+  g->slot_cap = slot_cap;
+  g->n_items = n_items;
+  g->n_groups = static_cast<int>(n_groups);
+  return QSA_OK;
+}
+
+void to_public(const Geometry& g, qsa_geometry* out) {
+  out->tile_tokens = qsa::kTileTokens;
+  out->stages = g.stages;
+  out->n_pad = g.np;
+  out->cols = g.cols;
+  out->head_chunks = g.head_chunks;
+  out->union_g = g.union_g;
+  out->grid = g.grid;
+  out->threads = qsa::kThreads;
+  out->smem_bytes = g.smem_bytes;
+  out->tmem_cols = g.tmem_cols;
+  out->n_items = g.n_items;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Device checks: compute capability 10.3 and the SM count (cached per device).
+qsa_status device_sms(int32_t* sms) {
+  static std::atomic<int32_t> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return QSA_ERR_CUDA;
+  if (dev >= 0 && dev < 64) {
+    const int32_t c = cache[dev].load();
+    if (c > 0) {
+      *sms = c;
+      return QSA_OK;
+    }
+  }
+  int major = 0, minor = 0, n = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return QSA_ERR_CUDA;
+  if (major != 10 || minor != 3) return QSA_ERR_UNSUPPORTED;
+  if (dev >= 0 && dev < 64) cache[dev].store(n);
+  *sms = n;
+  return QSA_OK;
+}
+
+qsa_status run(const void* q, const void* k_cache, const void* v_cache, const int32_t* indices,
+               const int32_t* topk_len, void* out, float* lse, int64_t n_rows, int32_t n_qheads,
+               int32_t n_kvheads, int32_t head_dim, int32_t topk, float scale, int32_t union_g,
+               int64_t n_kv_slots, void* workspace, size_t workspace_bytes,
+               const qsa_geometry* forced, void* stream_v) {
+  if (!q || !k_cache || !v_cache || !indices || !out) return QSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return QSA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || n_kv_slots < 0) return QSA_ERR_INVALID_ARG;
+  if (n_kvheads > 0 && n_kv_slots > 0 && n_kv_slots * n_kvheads >= INT32_MAX)
+    return QSA_ERR_UNSUPPORTED;
+  Geometry g{};
+  bool fell_back = false, stepped = false;
+  // Validate the shape on the host first (num_sms = 1 stands in until the device is known).
+  qsa_status st = select(n_qheads, n_kvheads, union_g, topk, head_dim, n_rows, 1, forced, &g,
+                         &fell_back, &stepped);
+  if (st != QSA_OK) return st;
+  if (n_rows == 0) return QSA_OK;
+  int32_t sms = 0;
+  st = device_sms(&sms);
+  if (st != QSA_OK) return st;
+  st = select(n_qheads, n_kvheads, union_g, topk, head_dim, n_rows, sms, forced, &g, &fell_back,
+              &stepped);
+  if (st != QSA_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+
+  qsa::PrefillParams p{};
+  p.q = static_cast<const uint16_t*>(q);
+  p.indices = indices;
+  p.topk_len = topk_len;
+  p.out = static_cast<uint16_t*>(out);
+  p.lse = lse;
+  p.n_rows = n_rows;
+  p.n_items = g.n_items;
+  p.n_kv_slots = n_kv_slots;
+  p.n_qheads = n_qheads;
+  p.n_kvheads = n_kvheads;
+  p.group = n_qheads / n_kvheads;
+  p.topk = topk;
+  p.union_g = g.union_g;
+  p.n_groups = g.n_groups;
+  p.head_chunks = g.head_chunks;
+  p.chunk_cols = g.chunk_cols;
+  p.stages = g.stages;
+  p.slot_cap = g.slot_cap;
+  p.tmem_cols = g.tmem_cols;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  const int64_t tmap_rows = n_kv_slots > 0 ? n_kv_slots * n_kvheads : static_cast<int64_t>(INT32_MAX);
+  p.pad_row = static_cast<int32_t>(tmap_rows);
+
+  void* ws = nullptr;
+  bool own_ws = false;
+  if (g.union_g > 1) {
+    const WsLayout w = ws_layout(n_rows, topk, g.union_g);
+    if (workspace) {
+      if (workspace_bytes < w.total || (reinterpret_cast<uintptr_t>(workspace) % kWsAlign) != 0)
+        return QSA_ERR_WORKSPACE;
+      ws = workspace;
+    } else {
+      if (cudaMallocAsync(&ws, w.total, stream) != cudaSuccess) return QSA_ERR_CUDA;
+      own_ws = true;
+    }
+    uint8_t* b = static_cast<uint8_t*>(ws);
+    p.union_idx = reinterpret_cast<int32_t*>(b + w.idx);
+    p.union_bits = b + w.bits;
+    p.union_len = reinterpret_cast<int32_t*>(b + w.len);
+    cudaError_t e = qsa::launch_union_build(indices, topk_len, n_rows, topk, g.union_g, n_kv_slots,
+                                            nullptr, const_cast<int32_t*>(p.union_idx),
+                                            const_cast<uint8_t*>(p.union_bits),
+                                            const_cast<int32_t*>(p.union_len), false, stream);
+    if (e != cudaSuccess) {
+      if (own_ws) cudaFreeAsync(ws, stream);
+      return QSA_ERR_CUDA;
+    }
+    g_launches.fetch_add(1);
+  }
+  cudaError_t e = qsa::launch_prefill(p, g, k_cache, v_cache, tmap_rows, stream);
+  if (own_ws) cudaFreeAsync(ws, stream);
+  if (e != cudaSuccess) return QSA_ERR_CUDA;
+  g_launches.fetch_add(1);
+  if (g.union_g > 1) g_calls_union.fetch_add(1); else g_calls_per_token.fetch_add(1);
+  if (fell_back) g_union_fallbacks.fetch_add(1);
+  if (stepped) g_step_downs.fetch_add(1);
+  return QSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+qsa_status qsa_sparse_prefill(const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* indices, const int32_t* topk_len, void* out, float* lse,
+                              int64_t n_rows, int32_t n_qheads, int32_t n_kvheads, int32_t head_dim,
+                              int32_t topk, float scale, int32_t union_g, void* stream) {
+  return run(q, k_cache, v_cache, indices, topk_len, out, lse, n_rows, n_qheads, n_kvheads,
+             head_dim, topk, scale, union_g, 0, nullptr, 0, nullptr, stream);
+}
+
+qsa_status qsa_sparse_prefill_ex(const void* q, const void* k_cache, const void* v_cache,
+                                 const int32_t* indices, const int32_t* topk_len, void* out,
+                                 float* lse, int64_t n_rows, int32_t n_qheads, int32_t n_kvheads,
+                                 int32_t head_dim, int32_t topk, float scale, int32_t union_g,
+                                 int64_t n_kv_slots, void* workspace, size_t workspace_bytes,
+                                 const qsa_geometry* forced, void* stream) {
+  return run(q, k_cache, v_cache, indices, topk_len, out, lse, n_rows, n_qheads, n_kvheads,
+             head_dim, topk, scale, union_g, n_kv_slots, workspace, workspace_bytes, forced, stream);
+}
+
+size_t qsa_workspace_bytes(int64_t n_rows, int32_t topk, int32_t union_g) {
+  if (topk <= 0 || n_rows <= 0 || union_g <= 1 || union_g > 8) return 0;
+  return ws_layout(n_rows, topk, union_g).total;
+}
+
+qsa_status qsa_union_build(const int32_t* indices, const int32_t* topk_len, int64_t n_rows,
+                           int32_t topk, int32_t union_g, int64_t n_kv_slots, int32_t* sorted_out,
+                           int32_t* union_idx, uint8_t* union_bits, int32_t* union_len,
+                           void* stream) {
+  if (!indices || !union_idx || !union_bits || !union_len) return QSA_ERR_INVALID_ARG;
+  if (n_rows < 0 || topk <= 0 || union_g < 1 || union_g > 8 || n_kv_slots < 0)
+    return QSA_ERR_INVALID_ARG;
+  if (n_rows > INT32_MAX ||
+      qsa::union_build_smem_bytes(topk, union_g) > static_cast<size_t>(qsa::kUnionMaxSmem))
+    return QSA_ERR_UNSUPPORTED;
+  if (n_rows == 0) return QSA_OK;
+  int32_t sms = 0;
+  qsa_status st = device_sms(&sms);
+  if (st != QSA_OK) return st;
+  cudaError_t e = qsa::launch_union_build(indices, topk_len, n_rows, topk, union_g, n_kv_slots,
+                                          sorted_out, union_idx, union_bits, union_len, true,
+                                          static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return QSA_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return QSA_OK;
+}
+
+qsa_status qsa_select_geometry(int32_t n_qheads, int32_t n_kvheads, int32_t union_g, int32_t topk,
+                               int32_t head_dim, int64_t n_rows, int32_t num_sms,
+                               qsa_geometry* out) {
+  if (!out) return QSA_ERR_INVALID_ARG;
+  if (num_sms <= 0) {
+    qsa_status st = device_sms(&num_sms);
+    if (st != QSA_OK) return st;
+  }
+  Geometry g{};
+  bool fb = false, sd = false;
+  qsa_status st = select(n_qheads, n_kvheads, union_g, topk, head_dim, n_rows, num_sms, nullptr, &g,
+                         &fb, &sd);
+  if (st != QSA_OK) return st;
+  to_public(g, out);
+  return QSA_OK;
+}
+
+void qsa_get_counters(qsa_counters* out) {
+  if (!out) return;
+  out->calls_per_token = g_calls_per_token.load();
+  out->calls_union = g_calls_union.load();
+  out->union_fallbacks = g_union_fallbacks.load();
+  out->step_downs = g_step_downs.load();
+  out->kernel_launches = g_launches.load();
+}
+
+void qsa_reset_counters(void) {
+  g_calls_per_token = 0;
+  g_calls_union = 0;
+  g_union_fallbacks = 0;
+  g_step_downs = 0;
+  g_launches = 0;
+}
+
+const char* qsa_status_string(qsa_status s) {
+  switch (s) {
+    case QSA_OK: return "ok";
+    case QSA_ERR_INVALID_ARG: return "invalid argument";
+    case QSA_ERR_UNSUPPORTED: return "unsupported shape or device";
+    case QSA_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case QSA_ERR_CUDA: return "CUDA error";
+    case QSA_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+const char* qsa_version(void) { return "qsa 0.1.0 (sm_103a, tcgen05 + TMA gather4)"; }
+
+qsa_status qsa_get_device_status(void* stream, int32_t* status_out) {
+  if (!status_out) return QSA_ERR_INVALID_ARG;
+  int32_t s = 0;
+  if (qsa::read_and_clear_device_status(static_cast<cudaStream_t>(stream), &s) != cudaSuccess)
+    return QSA_ERR_CUDA;
+  *status_out = s;
+  return s == 0 ? QSA_OK : QSA_ERR_TIMEOUT;
+}
+
+}  // extern "C"

@@ -1,0 +1,95 @@
+// Declarations shared by the host API (api.cpp) and the CUDA translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/qsa.h"
+
+namespace qsa {
+
+constexpr int kHeadDim = 256;
+constexpr int kTileTokens = 128;             // gathered slots per MMA tile (MMA M)
+constexpr int kStageBytes = kTileTokens * 128 * 2;  // 128 slots x 128 dims bf16 = 32 KiB
+constexpr int kMaxNPad = 64;                 // largest MMA N per tile
+constexpr int kThreads = 224;                // 4 softmax warps, MMA, TMA and index warps
+constexpr int kMinStages = 4;                // ring must hold V(j) and K(j+1) together
+constexpr int kMaxStages = 8;
+constexpr int kSmemLimit = 232448;           // 227 KiB opt-in dynamic shared memory
+constexpr int kUnionMaxSmem = 200 * 1024;    // union-build kernel shared-memory cap
+
+// Everything the attention kernel needs besides the two tensor maps.
+struct PrefillParams {
+  const uint16_t* q;            // bf16 bits [n_rows, n_qheads, 256]
+  const int32_t* indices;       // per-token mode
+  const int32_t* topk_len;      // nullable
+  uint16_t* out;
+  float* lse;                   // nullable
+  const int32_t* union_idx;     // union mode: [n_groups, union_g * topk]
+  const uint8_t* union_bits;
+  const int32_t* union_len;
+  int64_t n_rows;
+  int64_t n_items;
+  int64_t n_kv_slots;           // 0 = unchecked
+  int32_t n_qheads, n_kvheads, group;   // group = n_qheads / n_kvheads
+  int32_t topk;
+  int32_t union_g;              // 1 = per-token
+  int32_t n_groups;             // row groups
+  int32_t head_chunks, chunk_cols;
+  int32_t stages;
+  int32_t slot_cap;             // per-token slot-list capacity (multiple of 128)
+  int32_t pad_row;              // tensor-map row used for padding gathers (out of bounds)
+  int32_t tmem_cols;
+  float scale_log2;             // scale * log2(e)
+};
+
+struct Geometry {
+  int np;             // MMA N (padded query columns)
+  int cols;           // real columns per item (max)
+  int head_chunks;
+  int chunk_cols;
+  int union_g;        // effective
+  int stages;
+  int grid;
+  int smem_bytes;
+  int tmem_cols;
+  int slot_cap;
+  int64_t n_items;
+  int n_groups;
+};
+
+// Shared-memory layout of the attention kernel (offsets from a 1024-aligned base).
+struct SmemLayout {
+  int ring, qbuf, pbuf, slots, bars, misc, total;
+  int q_bytes, p_bytes;
+};
+__host__ __device__ inline SmemLayout smem_layout(int np, int stages, int slot_cap) {
+  SmemLayout L;
+  L.q_bytes = np * 512;
+  L.p_bytes = np * 256;
+  L.ring = 0;
+  L.qbuf = stages * kStageBytes;
+  L.pbuf = L.qbuf + 2 * L.q_bytes;
+  L.slots = L.pbuf + 2 * L.p_bytes;
+  L.bars = L.slots + 2 * slot_cap * 4;
+  // full[st], empty[st], s_full[2], s_free[2], p_full[2], pv_done[2], item_full[2],
+  // item_empty[2], q_empty[2], final
+  L.misc = L.bars + (2 * stages + 15) * 8;
+  // info[2][8] int32, red[2][4][np] float, tmem base, abort flag, vote[3]
+  int misc_bytes = 2 * 8 * 4 + 2 * 4 * np * 4 + 32;
+  L.total = L.misc + misc_bytes + 1024;   // + alignment slack for the 1024-aligned base
+  return L;
+}
+
+// Host launchers (prefill.cu / union.cu).  Return cudaSuccess or the launch error.
+cudaError_t launch_prefill(const PrefillParams& p, const Geometry& g, const void* k_cache,
+                           const void* v_cache, int64_t tmap_rows, cudaStream_t stream);
+cudaError_t launch_union_build(const int32_t* indices, const int32_t* topk_len, int64_t n_rows,
+                               int32_t topk, int32_t union_g, int64_t n_kv_slots,
+                               int32_t* sorted_out, int32_t* union_idx, uint8_t* union_bits,
+                               int32_t* union_len, bool pad_outputs, cudaStream_t stream);
+size_t union_build_smem_bytes(int32_t topk, int32_t union_g);
+cudaError_t read_and_clear_device_status(cudaStream_t stream, int32_t* status);
+
+}  // namespace qsa

@@ -1,0 +1,747 @@
+// Top-k sparse attention prefill kernel for sm_103a (tcgen05 + TMA gather4).
+//
+// What it computes ("[QSA] Tune sm120 sparse prefill geometry", Motivation; "DSA prefill ...
+// triton_sparse_mla", Motivation and Modifications): for every query row, the query heads
+// that share one KV head attend over the K/V rows gathered at the row's selected slots
+// (negative = padding, topk_len leading slots), scaled dot product, online softmax, and the
+// kernel writes O (bf16) and the natural-log LSE (fp32) with no split-K partials.  In union
+// mode a work item is G adjacent rows sharing the union of their slots; an ownership bit per
+// (slot, row) masks every row's logits to its own support.
+//
+// Design (GB300-first, not the pages' Triton tiling):
+//  * One persistent CTA per SM walks work items (row group x KV head x head chunk), KV-head
+//    major so all CTAs stream one KV head's cache at a time (L2 locality).
+//  * The MMA is "swap-AB": the gathered slots are the MMA M dimension (128 per tile) and the
+//    query columns of the item (heads, or G x heads in union mode) are N, padded to 16 --
+//    instead of padding the head dimension up to the MMA M.
+//      S^T[128 x N]  = K_tile[128 x 256] . Q^T            (A: K-major SW128, B: K-major SW128)
+//      O^T[256 x N] += V_tile^T[256 x 128] . P^T[128 x N]  (A: MN-major SW128, B: K-major SW128)
+//    Accumulators live in tensor memory: two S buffers and the two 128-row halves of O^T.
+//  * K/V rows are gathered by TMA tile::gather4 (4 slots x 128 B per instruction) into a ring
+//    of 32 KiB stages (128 slots x 128 dims): K_lo, K_hi, V_lo, V_hi per tile.  Padding slots
+//    read out-of-bounds rows, which TMA fills with zeros.
+//  * Online softmax in registers, one thread per slot (tensor-memory lane).  The running max
+//    is only raised when a tile's logits exceed it by more than 2^8 (log2 domain), so the
+//    O^T rescale through tensor memory is rare; the result is exact either way because O and
+//    the row sum use the same stale max.
+//  * Warp roles: 0-3 softmax + epilogue, 4 MMA issue + tensor-memory owner, 5 TMA producer,
+//    6 index/Q loader (per-token: compacts the row's valid slots into shared memory).
+//  * Every mbarrier wait is bounded (~2 s); a timeout records a code in a device status word,
+//    all roles leave their loops, in-flight copies and MMAs are drained, tensor memory is
+//    freed and the kernel returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace qsa {
+
+__device__ int32_t g_device_status = 0;
+
+namespace {
+
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s per wait
+constexpr unsigned long long kDrainLimitNs = 200000000ull;   // 0.2 s per drain wait
+constexpr float kRescaleThreshold = 8.0f;                    // log2 units (factor 256)
+constexpr float kLn2 = 0.6931471805599453f;
+
+enum WaitSite : int32_t {
+  kSiteItemEmpty = 1, kSiteQEmpty, kSiteItemFull, kSiteStageEmpty, kSiteStageFull,
+  kSiteSFree, kSiteSFull, kSitePFull, kSitePvDone, kSiteDrain
+};
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                       int32_t site, unsigned long long limit) {
+  const unsigned long long t0 = global_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > limit) {
+      *abort_flag = 1;
+      atomicCAS(&g_device_status, 0, 0x100 | site);
+      return false;
+    }
+  }
+}
+
+// Bounded wait for phase `parity` of mbarrier `bar`.  False on timeout or abort.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         int32_t site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_slow(bar, parity, abort_flag, site, kWaitLimitNs);
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ void sts_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+struct ItemInfo {   // written by the index warp, read by every role
+  int32_t n_valid, group, kvh, chunk, cols, row0, rows_in_group, pad;
+};
+
+__device__ __forceinline__ void decode_item(const PrefillParams& p, int64_t item, int32_t& group,
+                                            int32_t& kvh, int32_t& chunk) {
+  const int64_t per_kv = static_cast<int64_t>(p.head_chunks) * p.n_groups;
+  kvh = static_cast<int32_t>(item / per_kv);
+  const int64_t rem = item - static_cast<int64_t>(kvh) * per_kv;
+  chunk = static_cast<int32_t>(rem / p.n_groups);
+  group = static_cast<int32_t>(rem - static_cast<int64_t>(chunk) * p.n_groups);
+}
+
+}  // namespace
+
+template <int NP, bool UNION>
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_prefill_kernel(const __grid_constant__ CUtensorMap tmK,
+                          const __grid_constant__ CUtensorMap tmV,
+                          const __grid_constant__ PrefillParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  const uint32_t base = (raw_u32 + 1023u) & ~1023u;
+  uint8_t* const gbase = smem_raw + (base - raw_u32);
+
+  const int slot_cap = UNION ? 0 : p.slot_cap;
+  const SmemLayout L = smem_layout(NP, p.stages, slot_cap);
+  const int R = p.stages;
+
+  // barrier addresses
+  const uint32_t b_full = base + L.bars;
+  const uint32_t b_empty = b_full + 8 * R;
+  const uint32_t b_sfull = b_empty + 8 * R;
+  const uint32_t b_sfree = b_sfull + 16;
+  const uint32_t b_pfull = b_sfree + 16;
+  const uint32_t b_pvdone = b_pfull + 16;
+  const uint32_t b_itemfull = b_pvdone + 16;
+  const uint32_t b_itemempty = b_itemfull + 16;
+  const uint32_t b_qempty = b_itemempty + 16;
+  const uint32_t b_fin = b_qempty + 16;
+
+  ItemInfo* const info = reinterpret_cast<ItemInfo*>(gbase + L.misc);
+  float* const red = reinterpret_cast<float*>(gbase + L.misc + 2 * sizeof(ItemInfo));  // [2][4][NP]
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + L.misc + 2 * sizeof(ItemInfo) +
+                                                          2 * 4 * NP * sizeof(float));
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* const vote = reinterpret_cast<int*>(tmem_slot + 2);   // [3]
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < R; ++s) {
+      mbar_init(b_full + 8 * s, 1);
+      mbar_init(b_empty + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(b_sfull + 8 * b, 1);
+      mbar_init(b_sfree + 8 * b, 128);
+      mbar_init(b_pfull + 8 * b, 128);
+      mbar_init(b_pvdone + 8 * b, 1);
+      mbar_init(b_itemfull + 8 * b, 1);
+      mbar_init(b_itemempty + 8 * b, 130);
+      mbar_init(b_qempty + 8 * b, 1);
+    }
+    mbar_init(b_fin, 1);
+    *abort_flag = 0;
+    vote[0] = 0;
+    vote[1] = 0;
+    vote[2] = 0;
+    fence_mbar_init();
+  }
+  if (warp == 4) {
+    tmem_alloc(smem_u32(tmem_slot), static_cast<uint32_t>(p.tmem_cols));
+    tmem_relinquish();
+  }
+  if (warp == 5 && lane == 0) {
+    prefetch_tmap(&tmK);
+    prefetch_tmap(&tmV);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t tm_s0 = tmem_base;              // S buffers: columns [0, NP), [NP, 2NP)
+  const uint32_t tm_o = tmem_base + 2 * NP;      // O^T halves: [2NP, 3NP), [3NP, 4NP)
+
+  const int64_t n_items = p.n_items;
+  const int64_t stride = gridDim.x;
+
+  if (warp == 6) {
+    // ------------------------------------------------------------ index / Q loader
+    uint32_t it = 0;
+    for (int64_t item = blockIdx.x; item < n_items; item += stride, ++it) {
+      const uint32_t b = it & 1, ph = (it >> 1) & 1;
+      bool ok = wait_bar(b_itemempty + 8 * b, ph ^ 1, abort_flag, kSiteItemEmpty);
+      ok = ok && wait_bar(b_qempty + 8 * b, ph ^ 1, abort_flag, kSiteQEmpty);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      int32_t group, kvh, chunk;
+      decode_item(p, item, group, kvh, chunk);
+      int32_t cols, row0, rows_in_group;
+      if (UNION) {
+        row0 = group * p.union_g;
+        rows_in_group = static_cast<int32_t>(p.n_rows - row0 < p.union_g ? p.n_rows - row0 : p.union_g);
+        cols = rows_in_group * p.group;
+      } else {
+        row0 = group;
+        rows_in_group = 1;
+        cols = min(p.chunk_cols, p.group - chunk * p.chunk_cols);
+      }
+      // Q tile: rows = query columns c (NP, zero beyond cols), 4 regions of 64 dims, SW128.
+      const uint32_t qb = base + L.qbuf + b * L.q_bytes;
+      const int rg = lane >> 3, jc = lane & 7;
+#pragma unroll
+      for (int c0 = 0; c0 < NP; c0 += 8) {
+        uint4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int c = c0 + i;
+          v[i] = make_uint4(0u, 0u, 0u, 0u);
+          if (c < cols) {
+            int64_t row, head;
+            if (UNION) {
+              row = row0 + c / p.group;
+              head = static_cast<int64_t>(kvh) * p.group + c % p.group;
+            } else {
+              row = row0;
+              head = static_cast<int64_t>(kvh) * p.group + chunk * p.chunk_cols + c;
+            }
+            v[i] = ldg_nc_v4(p.q + (row * p.n_qheads + head) * kHeadDim + lane * 8);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int c = c0 + i;
+          sts_v4(qb + rg * (NP * 128) + (c >> 3) * 1024 + (c & 7) * 128 + ((jc ^ (c & 7)) << 4), v[i]);
+        }
+      }
+      int32_t nv;
+      if (!UNION) {
+        // Compact the row's valid slots (in order) into the slot list, as tensor-map rows.
+        int32_t Lr = p.topk;
+        if (p.topk_len) Lr = min(max(p.topk_len[row0], 0), p.topk);
+        int32_t* const sl = reinterpret_cast<int32_t*>(gbase + L.slots) + b * slot_cap;
+        const uint32_t sl_u32 = base + L.slots + b * slot_cap * 4;
+        const int32_t* src = p.indices + static_cast<int64_t>(row0) * p.topk;
+        for (int j = lane; j < Lr; j += 32) cp_async_4(sl_u32 + 4 * j, src + j);
+        cp_async_commit_wait_all();
+        __syncwarp();
+        int32_t n = 0;
+        for (int j0 = 0; j0 < Lr; j0 += 32) {
+          const int j = j0 + lane;
+          const int32_t x = j < Lr ? sl[j] : -1;
+          bool valid = x >= 0 && (p.n_kv_slots == 0 || x < p.n_kv_slots);
+          const int64_t y = static_cast<int64_t>(x) * p.n_kvheads + kvh;
+          valid = valid && y < static_cast<int64_t>(p.pad_row);
+          const uint32_t m = __ballot_sync(0xffffffffu, valid);
+          if (valid) sl[n + __popc(m & ((1u << lane) - 1u))] = static_cast<int32_t>(y);
+          n += __popc(m);
+          __syncwarp();
+        }
+        nv = n;
+      } else {
+        nv = p.union_len[group];
+      }
+      if (lane == 0) {
+        ItemInfo& I = info[b];
+        I.n_valid = nv;
+        I.group = group;
+        I.kvh = kvh;
+        I.chunk = chunk;
+        I.cols = cols;
+        I.row0 = row0;
+        I.rows_in_group = rows_in_group;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_itemfull + 8 * b);
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ TMA gather producer
+    uint32_t seq = 0, it = 0, issued = 0;
+    bool aborted = false;
+    for (int64_t item = blockIdx.x; item < n_items && !aborted; item += stride, ++it) {
+      const uint32_t b = it & 1, ph = (it >> 1) & 1;
+      if (!__all_sync(0xffffffffu, wait_bar(b_itemfull + 8 * b, ph, abort_flag, kSiteItemFull))) {
+        aborted = true;
+        break;
+      }
+      const ItemInfo I = info[b];
+      const int nv = I.n_valid;
+      const int nt = (nv + kTileTokens - 1) / kTileTokens;
+      const int32_t* sl = reinterpret_cast<const int32_t*>(gbase + L.slots) + b * slot_cap;
+      const int32_t* ul =
+          UNION ? p.union_idx + static_cast<int64_t>(I.group) * p.union_g * p.topk : nullptr;
+      int y[4];
+      auto fetch = [&](int j, int* yy) {
+        const int t0 = j * kTileTokens + 4 * lane;
+        if (!UNION) {
+          const int4 v = *reinterpret_cast<const int4*>(sl + t0);
+          yy[0] = t0 + 0 < nv ? v.x : p.pad_row;
+          yy[1] = t0 + 1 < nv ? v.y : p.pad_row;
+          yy[2] = t0 + 2 < nv ? v.z : p.pad_row;
+          yy[3] = t0 + 3 < nv ? v.w : p.pad_row;
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int t = t0 + k;
+            yy[k] = t < nv ? ul[t] * p.n_kvheads + I.kvh : p.pad_row;
+          }
+        }
+      };
+      if (nt > 0) fetch(0, y);
+      for (int j = 0; j < nt; ++j) {
+        int yn[4] = {p.pad_row, p.pad_row, p.pad_row, p.pad_row};
+        if (j + 1 < nt) fetch(j + 1, yn);
+#pragma unroll 1
+        for (int piece = 0; piece < 4; ++piece) {
+          const uint32_t s = seq + 4 * j + piece;
+          const uint32_t st = s % R;
+          if (!__all_sync(0xffffffffu, wait_bar(b_empty + 8 * st, ((s / R) & 1) ^ 1, abort_flag,
+                                                kSiteStageEmpty))) {
+            aborted = true;
+            break;
+          }
+          if (lane == 0) mbar_arrive_expect_tx(b_full + 8 * st, kStageBytes);
+          __syncwarp();
+          const CUtensorMap* tm = piece < 2 ? &tmK : &tmV;
+          const int x0 = (piece & 1) * 128;
+          const uint32_t dst = base + L.ring + st * kStageBytes + lane * 512;
+          tma_gather4(dst, tm, x0, y[0], y[1], y[2], y[3], b_full + 8 * st);
+          tma_gather4(dst + 16384, tm, x0 + 64, y[0], y[1], y[2], y[3], b_full + 8 * st);
+          issued = s + 1;
+        }
+        if (aborted) break;
+        y[0] = yn[0]; y[1] = yn[1]; y[2] = yn[2]; y[3] = yn[3];
+      }
+      if (aborted) break;
+      seq += 4 * nt;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_itemempty + 8 * b);
+    }
+    if (aborted && lane == 0) {
+      // Drain: wait (bounded) for the newest phase of every stage this warp filled.
+      for (uint32_t s = issued > static_cast<uint32_t>(R) ? issued - R : 0; s < issued; ++s)
+        wait_slow(b_full + 8 * (s % R), (s / R) & 1, abort_flag, kSiteDrain, kDrainLimitNs);
+    }
+  } else if (warp == 4) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t kIdescQK = idesc_bf16_f32(128, NP, false, false);
+    constexpr uint32_t kIdescPV = idesc_bf16_f32(128, NP, true, false);
+    uint32_t seq = 0, js = 0, it = 0;
+    bool aborted = false;
+    for (int64_t item = blockIdx.x; item < n_items && !aborted; item += stride, ++it) {
+      const uint32_t b = it & 1, ph = (it >> 1) & 1;
+      if (!__all_sync(0xffffffffu, wait_bar(b_itemfull + 8 * b, ph, abort_flag, kSiteItemFull))) {
+        aborted = true;
+        break;
+      }
+      const int nv = info[b].n_valid;
+      const int nt = (nv + kTileTokens - 1) / kTileTokens;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_itemempty + 8 * b);
+      const uint32_t qaddr = base + L.qbuf + b * L.q_bytes;
+      for (int j = 0; j <= nt; ++j) {
+        if (j < nt) {
+          // S^T(j) = K(j) . Q^T
+          const uint32_t s_lo = seq + 4 * j, s_hi = s_lo + 1;
+          const uint32_t jsj = js + j, sb = jsj & 1, sph = (jsj >> 1) & 1;
+          bool ok = wait_bar(b_full + 8 * (s_lo % R), (s_lo / R) & 1, abort_flag, kSiteStageFull);
+          ok = ok && wait_bar(b_full + 8 * (s_hi % R), (s_hi / R) & 1, abort_flag, kSiteStageFull);
+          ok = ok && wait_bar(b_sfree + 8 * sb, sph ^ 1, abort_flag, kSiteSFree);
+          if (!__all_sync(0xffffffffu, ok)) {
+            aborted = true;
+            break;
+          }
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t klo = base + L.ring + (s_lo % R) * kStageBytes;
+            const uint32_t khi = base + L.ring + (s_hi % R) * kStageBytes;
+#pragma unroll
+            for (int kk = 0; kk < 16; ++kk) {
+              const uint32_t kst = kk < 8 ? klo : khi;
+              const int kq = kk & 7;
+              const uint64_t a = sw128_desc(kst + (kq >> 2) * 16384 + (kq & 3) * 32, 16, 1024);
+              const uint64_t bq = sw128_desc(qaddr + (kk >> 2) * (NP * 128) + (kk & 3) * 32, 16, 1024);
+              tc_mma(tm_s0 + sb * NP, a, bq, kIdescQK, kk > 0 ? 1u : 0u);
+            }
+            tc_commit(b_empty + 8 * (s_lo % R));
+            tc_commit(b_empty + 8 * (s_hi % R));
+            tc_commit(b_sfull + 8 * sb);
+            if (j == nt - 1) tc_commit(b_qempty + 8 * b);
+          }
+          __syncwarp();
+        }
+        if (j > 0) {
+          // O^T += V(j-1)^T . P^T(j-1)
+          const int jp = j - 1;
+          const uint32_t jsp = js + jp, pb = jsp & 1, pph = (jsp >> 1) & 1;
+          const uint32_t s_vlo = seq + 4 * jp + 2, s_vhi = s_vlo + 1;
+          bool ok = wait_bar(b_pfull + 8 * pb, pph, abort_flag, kSitePFull);
+          ok = ok && wait_bar(b_full + 8 * (s_vlo % R), (s_vlo / R) & 1, abort_flag, kSiteStageFull);
+          ok = ok && wait_bar(b_full + 8 * (s_vhi % R), (s_vhi / R) & 1, abort_flag, kSiteStageFull);
+          if (!__all_sync(0xffffffffu, ok)) {
+            aborted = true;
+            break;
+          }
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t pbase = base + L.pbuf + pb * L.p_bytes;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const uint32_t vst = base + L.ring + ((hh ? s_vhi : s_vlo) % R) * kStageBytes;
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t a = sw128_desc(vst + kk * 2048, 16384, 1024);
+                const uint64_t bp = sw128_desc(pbase + (kk >> 2) * (NP * 128) + (kk & 3) * 32, 16, 1024);
+                tc_mma(tm_o + hh * NP, a, bp, kIdescPV, (jp == 0 && kk == 0) ? 0u : 1u);
+              }
+            }
+            tc_commit(b_empty + 8 * (s_vlo % R));
+            tc_commit(b_empty + 8 * (s_vhi % R));
+            tc_commit(b_pvdone + 8 * pb);
+          }
+          __syncwarp();
+        }
+      }
+      if (aborted) break;
+      if (nt == 0 && lane == 0) tc_commit(b_qempty + 8 * b);
+      __syncwarp();
+      seq += 4 * nt;
+      js += nt;
+    }
+    // Every MMA this thread issued has completed once `fin` flips.
+    if (lane == 0) {
+      tc_commit(b_fin);
+      wait_slow(b_fin, 0, abort_flag, kSiteDrain, aborted ? kDrainLimitNs : kWaitLimitNs);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue (warps 0-3)
+    const int t = threadIdx.x;                       // tensor-memory lane = slot within tile
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    uint32_t js = 0, it = 0, rb = 0;
+    bool bad = false;
+    const float NEG_INF = -INFINITY;
+    for (int64_t item = blockIdx.x; item < n_items; item += stride, ++it) {
+      const uint32_t b = it & 1, ph = (it >> 1) & 1;
+      bad |= !wait_bar(b_itemfull + 8 * b, ph, abort_flag, kSiteItemFull);
+      const ItemInfo I = info[b];
+      mbar_arrive(b_itemempty + 8 * b);
+      const int nv = I.n_valid;
+      const int nt = (nv + kTileTokens - 1) / kTileTokens;
+      const int cols = I.cols;
+      // Column masks: bit c of colmask[u] set when query column c belongs to row u of the group.
+      uint64_t colmask[8];
+      uint64_t allcols = (cols >= 64) ? ~0ull : ((1ull << cols) - 1ull);
+      if (UNION) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int lo = u * p.group, hi = min((u + 1) * p.group, cols);
+          uint64_t m = 0;
+          if (lo < hi) {
+            const uint64_t upto = hi >= 64 ? ~0ull : ((1ull << hi) - 1ull);
+            const uint64_t below = lo >= 64 ? ~0ull : ((1ull << lo) - 1ull);
+            m = upto & ~below;
+          }
+          colmask[u] = m;
+        }
+      }
+      const uint8_t* ub =
+          UNION ? p.union_bits + static_cast<int64_t>(I.group) * p.union_g * p.topk : nullptr;
+      float m_used[NP], l_part[NP];
+#pragma unroll
+      for (int c = 0; c < NP; ++c) {
+        m_used[c] = NEG_INF;
+        l_part[c] = 0.f;
+      }
+      uint32_t bits_next = 0;
+      if (UNION && nt > 0) bits_next = t < nv ? ub[t] : 0u;
+      bool quit = false;
+      for (int j = 0; j < nt; ++j) {
+        const uint32_t jsj = js + j, sb = jsj & 1, sph = (jsj >> 1) & 1;
+        const int token = j * kTileTokens + t;
+        const bool valid = token < nv;
+        uint64_t vmask = valid ? allcols : 0ull;
+        if (UNION) {
+          const uint32_t bits = bits_next;
+          if (j + 1 < nt) bits_next = (token + kTileTokens) < nv ? ub[token + kTileTokens] : 0u;
+          uint64_t m = 0;
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            if ((bits >> u) & 1u) m |= colmask[u];
+          vmask &= m;
+        }
+        bad |= !wait_bar(b_sfull + 8 * sb, sph, abort_flag, kSiteSFull);
+        tc_fence_after();
+        float x[NP];
+#pragma unroll
+        for (int q = 0; q < NP / 16; ++q) tmem_ld16(tm_s0 + lane_off + sb * NP + 16 * q, x + 16 * q);
+        tc_wait_ld();
+        tc_fence_before();
+        mbar_arrive(b_sfree + 8 * sb);
+        bool need = false;
+#pragma unroll
+        for (int c = 0; c < NP; ++c) {
+          x[c] = ((vmask >> c) & 1ull) ? x[c] * p.scale_log2 : NEG_INF;
+          need |= x[c] > m_used[c] + kRescaleThreshold;
+        }
+        // One barrier per tile decides, uniformly for the 128 threads, whether the max moves
+        // and whether some role gave up.
+        const int myvote = (need ? 1 : 0) | ((bad || *abort_flag) ? 2 : 0);
+        // vote[] is used round robin over the CTA's tile sequence: the word for tile jsj+2
+        // is cleared here, after every thread has read it at tile jsj-1 and before any
+        // thread can pass the next barrier and write it.
+        if (myvote) atomicOr(&vote[jsj % 3], myvote);
+        named_bar_sync(2, 128);
+        const int f = vote[jsj % 3];
+        if (t == 0) vote[(jsj + 2) % 3] = 0;
+        if (f & 2) {
+          quit = true;
+          break;
+        }
+        if (f & 1) {
+          float* rbuf = red + rb * 4 * NP;
+#pragma unroll
+          for (int c = 0; c < NP; ++c) {
+            float v = x[c];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+            if (lane == 0) rbuf[warp * NP + c] = v;
+          }
+          named_bar_sync(1, 128);
+          float alpha[NP];
+          bool any_scale = false;
+#pragma unroll
+          for (int c = 0; c < NP; ++c) {
+            const float tmax = fmaxf(fmaxf(rbuf[c], rbuf[NP + c]), fmaxf(rbuf[2 * NP + c], rbuf[3 * NP + c]));
+            const float m_new = fmaxf(m_used[c], tmax);
+            alpha[c] = (m_new == NEG_INF) ? 1.f : fast_exp2(m_used[c] - m_new);
+            any_scale |= alpha[c] != 1.f;
+            m_used[c] = m_new;
+            l_part[c] *= alpha[c];
+          }
+          rb ^= 1;
+          if (j > 0 && any_scale) {
+            // O^T columns shrink by alpha once the previous tile's P.V has landed.
+            const uint32_t jprev = jsj - 1;
+            bad |= !wait_bar(b_pvdone + 8 * (jprev & 1), (jprev >> 1) & 1, abort_flag, kSitePvDone);
+            tc_fence_after();
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+              for (int q = 0; q < NP / 16; ++q) {
+                float o[16];
+                const uint32_t ta = tm_o + lane_off + hh * NP + 16 * q;
+                tmem_ld16(ta, o);
+                tc_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) o[i] *= alpha[16 * q + i];
+                tmem_st16(ta, o);
+              }
+            }
+            tc_wait_st();
+          }
+        }
+        // P buffer sb is free once the P.V of tile jsj-2 has completed.
+        bad |= !wait_bar(b_pvdone + 8 * sb, sph ^ 1, abort_flag, kSitePvDone);
+        uint8_t* pbuf = gbase + L.pbuf + sb * L.p_bytes;
+        uint8_t* prow = pbuf + (t >> 6) * (NP * 128) + ((t & 7) << 1);
+        const int tchunk = (t & 63) >> 3;
+#pragma unroll
+        for (int c = 0; c < NP; ++c) {
+          const float pv = x[c] == NEG_INF ? 0.f : fast_exp2(x[c] - m_used[c]);
+          l_part[c] += pv;
+          const __nv_bfloat16 pb16 = __float2bfloat16_rn(pv);
+          *reinterpret_cast<__nv_bfloat16*>(prow + (c >> 3) * 1024 + (c & 7) * 128 +
+                                            ((tchunk ^ (c & 7)) << 4)) = pb16;
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(b_pfull + 8 * sb);
+      }
+      if (quit) break;
+      // ---- epilogue: row sums, O / l, LSE
+      float* rbuf = red + rb * 4 * NP;
+#pragma unroll
+      for (int c = 0; c < NP; ++c) {
+        float v = l_part[c];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) rbuf[warp * NP + c] = v;
+      }
+      named_bar_sync(1, 128);
+      float inv_l[NP];
+      float my_l = 0.f, my_m = NEG_INF;
+#pragma unroll
+      for (int c = 0; c < NP; ++c) {
+        const float l = (rbuf[c] + rbuf[NP + c]) + (rbuf[2 * NP + c] + rbuf[3 * NP + c]);
+        inv_l[c] = l > 0.f ? 1.f / l : 0.f;
+        if (c == t) {
+          my_l = l;
+          my_m = m_used[c];
+        }
+      }
+      rb ^= 1;
+      if (nt > 0) {
+        const uint32_t jl = js + nt - 1;
+        bad |= !wait_bar(b_pvdone + 8 * (jl & 1), (jl >> 1) & 1, abort_flag, kSitePvDone);
+        tc_fence_after();
+      }
+      // Output base for column c: row(c) * Hq + head(c), times head_dim.
+      const int64_t Hq = p.n_qheads;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float o[NP];
+        if (nt > 0) {
+#pragma unroll
+          for (int q = 0; q < NP / 16; ++q) tmem_ld16(tm_o + lane_off + hh * NP + 16 * q, o + 16 * q);
+          tc_wait_ld();
+        } else {
+#pragma unroll
+          for (int c = 0; c < NP; ++c) o[c] = 0.f;
+        }
+        const int d = hh * 128 + t;
+#pragma unroll
+        for (int c = 0; c < NP; ++c) {
+          if (c < cols) {
+            int64_t row, head;
+            if (UNION) {
+              row = I.row0 + c / p.group;
+              head = static_cast<int64_t>(I.kvh) * p.group + c % p.group;
+            } else {
+              row = I.row0;
+              head = static_cast<int64_t>(I.kvh) * p.group + I.chunk * p.chunk_cols + c;
+            }
+            reinterpret_cast<__nv_bfloat16*>(p.out)[(row * Hq + head) * kHeadDim + d] =
+                __float2bfloat16_rn(o[c] * inv_l[c]);
+          }
+        }
+      }
+      if (p.lse != nullptr && t < cols) {
+        int64_t row, head;
+        if (UNION) {
+          row = I.row0 + t / p.group;
+          head = static_cast<int64_t>(I.kvh) * p.group + t % p.group;
+        } else {
+          row = I.row0;
+          head = static_cast<int64_t>(I.kvh) * p.group + I.chunk * p.chunk_cols + t;
+        }
+        p.lse[row * Hq + head] = my_l > 0.f ? (my_m + log2f(my_l)) * kLn2 : NEG_INF;
+      }
+      tc_fence_before();
+      js += nt;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, static_cast<uint32_t>(p.tmem_cols));
+  }
+}
+
+// ---------------------------------------------------------------------------- host side
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 2-D map over a KV cache viewed as [rows = slots x kv_heads, 256] bf16, box 64 x 1, SW128.
+cudaError_t make_cache_map(CUtensorMap* m, const void* cache, int64_t rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim * 2)};
+  const cuuint32_t box[2] = {64, 1};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int NP, bool UNION>
+cudaError_t launch_np(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
+                      const Geometry& g, cudaStream_t stream) {
+  auto kern = sparse_prefill_kernel<NP, UNION>;
+  // The shared-memory opt-in is set once per device and size, so calls made while a stream
+  // is being captured into a CUDA graph only enqueue the launch.
+  static std::atomic<int> opted_in[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || opted_in[dev].load() < g.smem_bytes) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_bytes);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) opted_in[dev].store(g.smem_bytes);
+  }
+  kern<<<g.grid, kThreads, g.smem_bytes, stream>>>(tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillParams& p, const Geometry& g, const void* k_cache,
+                           const void* v_cache, int64_t tmap_rows, cudaStream_t stream) {
+  if (g.n_items == 0) return cudaSuccess;
+  CUtensorMap tk, tv;
+  cudaError_t e = make_cache_map(&tk, k_cache, tmap_rows);
+  if (e != cudaSuccess) return e;
+  e = make_cache_map(&tv, v_cache, tmap_rows);
+  if (e != cudaSuccess) return e;
+  const bool u = p.union_g > 1;
+  switch (g.np) {
+    case 16: return u ? launch_np<16, true>(tk, tv, p, g, stream) : launch_np<16, false>(tk, tv, p, g, stream);
+    case 32: return u ? launch_np<32, true>(tk, tv, p, g, stream) : launch_np<32, false>(tk, tv, p, g, stream);
+    case 48: return u ? launch_np<48, true>(tk, tv, p, g, stream) : launch_np<48, false>(tk, tv, p, g, stream);
+    case 64: return u ? launch_np<64, true>(tk, tv, p, g, stream) : launch_np<64, false>(tk, tv, p, g, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t read_and_clear_device_status(cudaStream_t stream, int32_t* status) {
+  int32_t zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(status, g_device_status, sizeof(int32_t), 0,
+                                            cudaMemcpyDeviceToHost, stream);
+  if (e != cudaSuccess) return e;
+  e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyToSymbolAsync(g_device_status, &zero, sizeof(int32_t), 0, cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return e;
+  return cudaStreamSynchronize(stream);
+}
+
+}  // namespace qsa
