@@ -173,6 +173,15 @@ class ClockSampler:
 
 # ------------------------------------------------------------------------- GPU leg
 
+def max_over_ranks(values, device):
+    """Element-wise max of per-rank timings (any torch.distributed backend)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -280,9 +289,7 @@ def run_gpu(args, rank, world, local_rank):
 
     # max over ranks
     if world > 1:
-        t = torch.tensor([ms, e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e_ms = float(t[0]), float(t[1])
+        ms, e_ms = max_over_ranks([ms, e_ms], dev)
 
     if rank != 0:
         return None

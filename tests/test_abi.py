@@ -63,6 +63,9 @@ def test_selector_union_fallback_and_head_chunks(lib):
     # 96 heads per group: two chunks of 48 columns
     g = B.select_geometry(96, 1, 0, 2048, 256, 100, 152)
     assert g["head_chunks"] == 2 and g["cols"] == 48 and g["n_pad"] == 48 and g["n_items"] == 200
+    # 8 rows x 8 heads = 64 columns: the union tile leaves no room for 4 stages -> per-token
+    g = B.select_geometry(8, 1, 8, 2048, 256, 100, 152)
+    assert g["union_g"] == 1
     # odd union sizes are legal shapes in this kernel
     g = B.select_geometry(6, 1, 3, 2048, 256, 100, 152)
     assert g["union_g"] == 3 and g["n_pad"] == 32 and g["n_items"] == 34

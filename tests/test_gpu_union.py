@@ -70,7 +70,9 @@ def test_union_attention_matches_per_token_oracle(B, G):
     torch.cuda.synchronize()
     assert B.device_status() == 0
     c = B.counters()
-    assert (c["calls_union"] == 1) == (G > 1)
+    # 8 rows x 8 heads does not fit the union tile's shared memory: counted per-token fallback
+    assert (c["calls_union"] == 1) == (1 < G < 8)
+    assert c["union_fallbacks"] == (1 if G == 8 else 0)
     O, L = oracle.sparse_prefill(w.q, w.k, w.v, w.indices, None, w.scale)
     assert_parity(out, lse, O, L, what=f"union G={G}")
 

@@ -57,7 +57,9 @@ qsa_status select(int32_t Hq, int32_t Hkv, int32_t union_g, int32_t topk, int32_
   const int group = Hq / Hkv;
   int G = union_g <= 1 ? 1 : union_g;
   if (G > 1) {
+    const int np_u = static_cast<int>(round_up(G * group, 16));
     const bool legal = G * group <= qsa::kMaxNPad &&
+                       qsa::smem_layout(np_u, qsa::kMinStages, 0).total <= qsa::kSmemLimit &&
                        qsa::union_build_smem_bytes(topk, G) <= static_cast<size_t>(qsa::kUnionMaxSmem) &&
                        static_cast<int64_t>(G) * topk <= INT32_MAX / 2;
     if (!legal) {
@@ -124,6 +126,16 @@ void to_public(const Geometry& g, qsa_geometry* out) {
   out->smem_bytes = g.smem_bytes;
   out->tmem_cols = g.tmem_cols;
   out->n_items = g.n_items;
+}
+
+// Gather engine: cp.async 16-byte copies by default; QSA_GATHER=tma selects TMA tile::gather4
+// (both are exact; the switch exists to compare them).
+bool gather_engine_is_tma() {
+  static const bool tma = [] {
+    const char* e = std::getenv("QSA_GATHER");
+    return e != nullptr && std::strcmp(e, "tma") == 0;
+  }();
+  return tma;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -197,6 +209,9 @@ qsa_status run(const void* q, const void* k_cache, const void* v_cache, const in
   p.stages = g.stages;
   p.slot_cap = g.slot_cap;
   p.tmem_cols = g.tmem_cols;
+  p.gather_tma = gather_engine_is_tma() ? 1 : 0;
+  p.k_bytes = static_cast<const uint8_t*>(k_cache);
+  p.v_bytes = static_cast<const uint8_t*>(v_cache);
   p.scale_log2 = scale * 1.4426950408889634f;
   const int64_t tmap_rows = n_kv_slots > 0 ? n_kv_slots * n_kvheads : static_cast<int64_t>(INT32_MAX);
   p.pad_row = static_cast<int32_t>(tmap_rows);

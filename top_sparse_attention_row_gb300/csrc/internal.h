@@ -13,7 +13,12 @@ constexpr int kHeadDim = 256;
 constexpr int kTileTokens = 128;             // gathered slots per MMA tile (MMA M)
 constexpr int kStageBytes = kTileTokens * 128 * 2;  // 128 slots x 128 dims bf16 = 32 KiB
 constexpr int kMaxNPad = 64;                 // largest MMA N per tile
-constexpr int kThreads = 224;                // 4 softmax warps, MMA, TMA and index warps
+constexpr int kSoftmaxWarps = 4;             // warps 0-3: softmax + epilogue (TMEM lanes 0-127)
+constexpr int kMmaWarp = 4;                  // MMA issue + tensor-memory owner
+constexpr int kIndexWarp = 5;                // slot compaction, Q tile, item info
+constexpr int kProducerWarp0 = 6;            // first gather warp
+constexpr int kProducerWarps = 6;            // gather warps issuing every piece together
+constexpr int kThreads = 32 * (kProducerWarp0 + kProducerWarps);
 constexpr int kMinStages = 4;                // ring must hold V(j) and K(j+1) together
 constexpr int kMaxStages = 8;
 constexpr int kSmemLimit = 232448;           // 227 KiB opt-in dynamic shared memory
@@ -41,6 +46,9 @@ struct PrefillParams {
   int32_t slot_cap;             // per-token slot-list capacity (multiple of 128)
   int32_t pad_row;              // tensor-map row used for padding gathers (out of bounds)
   int32_t tmem_cols;
+  int32_t gather_tma;           // 1 = TMA tile::gather4, 0 = cp.async 16-byte row copies
+  const uint8_t* k_bytes;       // caches as bytes, for the cp.async gather
+  const uint8_t* v_bytes;
   float scale_log2;             // scale * log2(e)
 };
 

@@ -17,15 +17,19 @@
 //      S^T[128 x N]  = K_tile[128 x 256] . Q^T            (A: K-major SW128, B: K-major SW128)
 //      O^T[256 x N] += V_tile^T[256 x 128] . P^T[128 x N]  (A: MN-major SW128, B: K-major SW128)
 //    Accumulators live in tensor memory: two S buffers and the two 128-row halves of O^T.
-//  * K/V rows are gathered by TMA tile::gather4 (4 slots x 128 B per instruction) into a ring
-//    of 32 KiB stages (128 slots x 128 dims): K_lo, K_hi, V_lo, V_hi per tile.  Padding slots
-//    read out-of-bounds rows, which TMA fills with zeros.
+//  * K/V rows are gathered into a ring of 32 KiB stages (128 slots x 128 dims, 128-byte
+//    swizzled rows) in exactly the order the MMA consumes them -- K(0), K(1), V(0), K(2), V(1),
+//    ..., V(nt-1), two half-row pieces each -- so the ring drains FIFO.  Six producer warps issue
+//    every piece together: per-SM gather bandwidth grows with the number of issuing warps, not
+//    with the number of stages.  Two gather engines: cp.async 16-byte copies (default; each
+//    warp waits for its own copies, fences them into the async proxy and arrives) and TMA
+//    tile::gather4 (4 slots x 128 B per instruction, out-of-bounds rows zero-filled).
 //  * Online softmax in registers, one thread per slot (tensor-memory lane).  The running max
 //    is only raised when a tile's logits exceed it by more than 2^8 (log2 domain), so the
 //    O^T rescale through tensor memory is rare; the result is exact either way because O and
 //    the row sum use the same stale max.
-//  * Warp roles: 0-3 softmax + epilogue, 4 MMA issue + tensor-memory owner, 5 TMA producer,
-//    6 index/Q loader (per-token: compacts the row's valid slots into shared memory).
+//  * Warp roles: 0-3 softmax + epilogue, 4 MMA issue + tensor-memory owner, 5 index/Q loader
+//    (per-token: compacts the row's valid slots into shared memory), 6-11 gather producers.
 //  * Every mbarrier wait is bounded (~2 s); a timeout records a code in a device status word,
 //    all roles leave their loops, in-flight copies and MMAs are drained, tensor memory is
 //    freed and the kernel returns.
@@ -95,6 +99,31 @@ __device__ __forceinline__ void sts_v4(uint32_t addr, uint4 v) {
                : "memory");
 }
 
+// Pieces of an item in consumption order: K(0), K(1), V(0), K(2), V(1), ..., K(nt-1), V(nt-2),
+// V(nt-1); every entry is two pieces (dims 0-127, 128-255).
+__device__ __forceinline__ void piece_of(int q, int nt, int& tile, int& is_v, int& half) {
+  if (q < 2) {
+    tile = 0; is_v = 0; half = q;
+    return;
+  }
+  const int b = (q + 2) >> 2, r = (q + 2) & 3;
+  if (b < nt) {
+    if (r < 2) { tile = b; is_v = 0; half = r; } else { tile = b - 1; is_v = 1; half = r - 2; }
+  } else {
+    tile = nt - 1; is_v = 1; half = r;
+  }
+}
+__device__ __forceinline__ int k_piece(int j) { return j == 0 ? 0 : 4 * j - 2; }
+__device__ __forceinline__ int v_piece(int j, int nt) { return j + 1 < nt ? 4 * j + 4 : 4 * nt - 2; }
+
+__device__ __forceinline__ void cp_async_16_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 struct ItemInfo {   // written by the index warp, read by every role
   int32_t n_valid, group, kvh, chunk, cols, row0, rows_in_group, pad;
 };
@@ -148,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < R; ++s) {
-      mbar_init(b_full + 8 * s, 1);
+      mbar_init(b_full + 8 * s, p.gather_tma ? 1 : kProducerWarps);
       mbar_init(b_empty + 8 * s, 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -157,7 +186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(b_pfull + 8 * b, 128);
       mbar_init(b_pvdone + 8 * b, 1);
       mbar_init(b_itemfull + 8 * b, 1);
-      mbar_init(b_itemempty + 8 * b, 130);
+      mbar_init(b_itemempty + 8 * b, 1 + 128 + kProducerWarps);
       mbar_init(b_qempty + 8 * b, 1);
     }
     mbar_init(b_fin, 1);
@@ -167,11 +196,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     vote[2] = 0;
     fence_mbar_init();
   }
-  if (warp == 4) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), static_cast<uint32_t>(p.tmem_cols));
     tmem_relinquish();
   }
-  if (warp == 5 && lane == 0) {
+  if (warp == kProducerWarp0 && lane == 0 && p.gather_tma) {
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
   }
@@ -185,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t n_items = p.n_items;
   const int64_t stride = gridDim.x;
 
-  if (warp == 6) {
+  if (warp == kIndexWarp) {
     // ------------------------------------------------------------ index / Q loader
     uint32_t it = 0;
     for (int64_t item = blockIdx.x; item < n_items; item += stride, ++it) {
@@ -274,12 +303,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(b_itemfull + 8 * b);
     }
-  } else if (warp == 5) {
-    // ------------------------------------------------------------ TMA gather producer
+  } else if (warp >= kProducerWarp0) {
+    // ------------------------------------------------------------ gather producers
+    // All producer warps take part in every piece, in order, so they all wait on the same
+    // phase of a stage.  cp.async: instruction i of a piece (2 slots x 16 chunks of 16 B)
+    // belongs to warp i % W; TMA: gather4 op o (4 slots x 64 dims) to warp o % W, lane o / W.
+    const int pw = warp - kProducerWarp0;
+    constexpr int W = kProducerWarps;
+    const bool tma = p.gather_tma != 0;
     uint32_t seq = 0, it = 0, issued = 0;
+    int pend_st = -1;                  // cp.async: stage filled by this warp, not yet signalled
     bool aborted = false;
+    auto flush = [&]() {
+      if (pend_st >= 0) {
+        cp_async_wait_0();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_full + 8 * pend_st);
+        pend_st = -1;
+      }
+    };
+    // Union slots come from global memory: each lane caches its slots for three tiles
+    // (V(j-1), K(j), K(j+1) can be in flight around one another), in registers indexed
+    // statically.  Per-token slots are read from the shared-memory slot list directly.
+    constexpr int kPerLane = (64 + W - 1) / W;        // cp.async instructions per lane
+    int yc0[kPerLane], yc1[kPerLane], yc2[kPerLane];
     for (int64_t item = blockIdx.x; item < n_items && !aborted; item += stride, ++it) {
       const uint32_t b = it & 1, ph = (it >> 1) & 1;
+      if (!__all_sync(0xffffffffu, mbar_try_wait(b_itemfull + 8 * b, ph))) flush();
       if (!__all_sync(0xffffffffu, wait_bar(b_itemfull + 8 * b, ph, abort_flag, kSiteItemFull))) {
         aborted = true;
         break;
@@ -290,59 +341,105 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t* sl = reinterpret_cast<const int32_t*>(gbase + L.slots) + b * slot_cap;
       const int32_t* ul =
           UNION ? p.union_idx + static_cast<int64_t>(I.group) * p.union_g * p.topk : nullptr;
-      int y[4];
-      auto fetch = [&](int j, int* yy) {
-        const int t0 = j * kTileTokens + 4 * lane;
-        if (!UNION) {
-          const int4 v = *reinterpret_cast<const int4*>(sl + t0);
-          yy[0] = t0 + 0 < nv ? v.x : p.pad_row;
-          yy[1] = t0 + 1 < nv ? v.y : p.pad_row;
-          yy[2] = t0 + 2 < nv ? v.z : p.pad_row;
-          yy[3] = t0 + 3 < nv ? v.w : p.pad_row;
-        } else {
+      // tensor-map row of token t of the item, or the padding row
+      auto slot_of = [&](int t) -> int32_t {
+        if (t >= nv) return p.pad_row;
+        if (!UNION) return sl[t];
+        return ul[t] * p.n_kvheads + I.kvh;
+      };
+      // slot of the r-th token this lane gathers in a piece of `tile`
+      auto lane_token = [&](int tile, int r) -> int {
+        if (tma) return tile * kTileTokens + 4 * ((pw + W * lane) >> 1) + r;
+        return tile * kTileTokens + 2 * (pw + W * r) + (lane >> 4);
+      };
+      auto fill = [&](int* yc, int tile) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int t = t0 + k;
-            yy[k] = t < nv ? ul[t] * p.n_kvheads + I.kvh : p.pad_row;
-          }
+        for (int r = 0; r < kPerLane; ++r) {
+          const bool live = tma ? (r < 4 && pw + W * lane < 64) : (pw + W * r < 64);
+          yc[r] = live ? slot_of(lane_token(tile, r)) : p.pad_row;
         }
       };
-      if (nt > 0) fetch(0, y);
-      for (int j = 0; j < nt; ++j) {
-        int yn[4] = {p.pad_row, p.pad_row, p.pad_row, p.pad_row};
-        if (j + 1 < nt) fetch(j + 1, yn);
-#pragma unroll 1
-        for (int piece = 0; piece < 4; ++piece) {
-          const uint32_t s = seq + 4 * j + piece;
-          const uint32_t st = s % R;
-          if (!__all_sync(0xffffffffu, wait_bar(b_empty + 8 * st, ((s / R) & 1) ^ 1, abort_flag,
-                                                kSiteStageEmpty))) {
+      auto issue = [&](const int* yc, int tile, int is_v, int half, uint32_t st) {
+        const uint32_t stage = base + L.ring + st * kStageBytes;
+        int y[kPerLane];
+#pragma unroll
+        for (int r = 0; r < kPerLane; ++r) y[r] = UNION ? yc[r] : slot_of(lane_token(tile, r));
+        if (tma) {
+          if (pw == 0 && lane == 0) mbar_arrive_expect_tx(b_full + 8 * st, kStageBytes);
+          const int o = pw + W * lane;
+          if (o < 64) {
+            const int tg = o >> 1, c = o & 1;
+            tma_gather4(stage + c * 16384 + tg * 512, is_v ? &tmV : &tmK, half * 128 + c * 64,
+                        y[0], y[1], y[2], y[3], b_full + 8 * st);
+          }
+          __syncwarp();
+        } else {
+          const uint8_t* cache = is_v ? p.v_bytes : p.k_bytes;
+          const int ch = lane & 15;
+#pragma unroll
+          for (int r = 0; r < kPerLane; ++r) {
+            const int i = pw + W * r;
+            if (i < 64) {
+              const int t = 2 * i + (lane >> 4);
+              const bool pad = y[r] == p.pad_row;
+              const uint8_t* src = cache + (pad ? 0 : static_cast<int64_t>(y[r]) * (kHeadDim * 2)) +
+                                   half * 256 + ch * 16;
+              const uint32_t dst = stage + (ch >> 3) * 16384 + t * 128 + (((ch & 7) ^ (t & 7)) << 4);
+              cp_async_16_zfill(dst, src, pad ? 0u : 16u);
+            }
+          }
+          cp_async_commit();
+          if (pend_st >= 0) {
+            cp_async_wait_1();
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_full + 8 * pend_st);
+          }
+          pend_st = static_cast<int>(st);
+        }
+      };
+      if (UNION && nt > 0) fill(yc0, 0);
+      for (int q = 0; q < 4 * nt; ++q) {
+        int tile, is_v, half;
+        piece_of(q, nt, tile, is_v, half);
+        if (UNION && !is_v && half == 0 && tile + 1 < nt) {
+          switch ((tile + 1) % 3) {
+            case 0: fill(yc0, tile + 1); break;
+            case 1: fill(yc1, tile + 1); break;
+            default: fill(yc2, tile + 1); break;
+          }
+        }
+        const uint32_t s = seq + q;
+        const uint32_t st = s % R;
+        const uint32_t par = ((s / R) & 1) ^ 1;
+        if (!__all_sync(0xffffffffu, mbar_try_wait(b_empty + 8 * st, par))) {
+          flush();
+          if (!__all_sync(0xffffffffu, wait_bar(b_empty + 8 * st, par, abort_flag, kSiteStageEmpty))) {
             aborted = true;
             break;
           }
-          if (lane == 0) mbar_arrive_expect_tx(b_full + 8 * st, kStageBytes);
-          __syncwarp();
-          const CUtensorMap* tm = piece < 2 ? &tmK : &tmV;
-          const int x0 = (piece & 1) * 128;
-          const uint32_t dst = base + L.ring + st * kStageBytes + lane * 512;
-          tma_gather4(dst, tm, x0, y[0], y[1], y[2], y[3], b_full + 8 * st);
-          tma_gather4(dst + 16384, tm, x0 + 64, y[0], y[1], y[2], y[3], b_full + 8 * st);
-          issued = s + 1;
         }
-        if (aborted) break;
-        y[0] = yn[0]; y[1] = yn[1]; y[2] = yn[2]; y[3] = yn[3];
+        switch (tile % 3) {
+          case 0: issue(yc0, tile, is_v, half, st); break;
+          case 1: issue(yc1, tile, is_v, half, st); break;
+          default: issue(yc2, tile, is_v, half, st); break;
+        }
+        issued = s + 1;
       }
       if (aborted) break;
       seq += 4 * nt;
       __syncwarp();
       if (lane == 0) mbar_arrive(b_itemempty + 8 * b);
     }
-    if (aborted && lane == 0) {
-      // Drain: wait (bounded) for the newest phase of every stage this warp filled.
+    if (!tma) {
+      if (aborted) cp_async_wait_0();
+      else flush();
+    } else if (aborted && pw == 0 && lane == 0) {
+      // Drain: wait (bounded) for the newest phase of every stage that was filled.
       for (uint32_t s = issued > static_cast<uint32_t>(R) ? issued - R : 0; s < issued; ++s)
         wait_slow(b_full + 8 * (s % R), (s / R) & 1, abort_flag, kSiteDrain, kDrainLimitNs);
     }
-  } else if (warp == 4) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t kIdescQK = idesc_bf16_f32(128, NP, false, false);
     constexpr uint32_t kIdescPV = idesc_bf16_f32(128, NP, true, false);
@@ -362,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j <= nt; ++j) {
         if (j < nt) {
           // S^T(j) = K(j) . Q^T
-          const uint32_t s_lo = seq + 4 * j, s_hi = s_lo + 1;
+          const uint32_t s_lo = seq + k_piece(j), s_hi = s_lo + 1;
           const uint32_t jsj = js + j, sb = jsj & 1, sph = (jsj >> 1) & 1;
           bool ok = wait_bar(b_full + 8 * (s_lo % R), (s_lo / R) & 1, abort_flag, kSiteStageFull);
           ok = ok && wait_bar(b_full + 8 * (s_hi % R), (s_hi / R) & 1, abort_flag, kSiteStageFull);
@@ -394,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // O^T += V(j-1)^T . P^T(j-1)
           const int jp = j - 1;
           const uint32_t jsp = js + jp, pb = jsp & 1, pph = (jsp >> 1) & 1;
-          const uint32_t s_vlo = seq + 4 * jp + 2, s_vhi = s_vlo + 1;
+          const uint32_t s_vlo = seq + v_piece(jp, nt), s_vhi = s_vlo + 1;
           bool ok = wait_bar(b_pfull + 8 * pb, pph, abort_flag, kSitePFull);
           ok = ok && wait_bar(b_full + 8 * (s_vlo % R), (s_vlo / R) & 1, abort_flag, kSiteStageFull);
           ok = ok && wait_bar(b_full + 8 * (s_vhi % R), (s_vhi / R) & 1, abort_flag, kSiteStageFull);
@@ -654,7 +751,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem_base, static_cast<uint32_t>(p.tmem_cols));
   }
