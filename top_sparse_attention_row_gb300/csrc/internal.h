@@ -78,11 +78,11 @@ __host__ __device__ inline SmemLayout smem_layout(int np, int stages, int slot_c
   L.p_bytes = np * 256;
   L.ring = 0;
   L.qbuf = stages * kStageBytes;
-  L.pbuf = L.qbuf + 2 * L.q_bytes;
+  L.pbuf = L.qbuf + L.q_bytes;          // one Q tile buffer
   L.slots = L.pbuf + 2 * L.p_bytes;
   L.bars = L.slots + 2 * slot_cap * 4;
   // full[st], empty[st], s_full[2], s_free[2], p_full[2], pv_done[2], item_full[2],
-  // item_empty[2], q_empty[2], final
+  // item_empty[2], q_empty, q_full, final
   L.misc = L.bars + (2 * stages + 15) * 8;
   // info[2][8] int32, red[2][4][np] float, tmem base, abort flag, vote[3]
   int misc_bytes = 2 * 8 * 4 + 2 * 4 * np * 4 + 32;

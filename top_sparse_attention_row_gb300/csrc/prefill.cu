@@ -56,7 +56,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 enum WaitSite : int32_t {
   kSiteItemEmpty = 1, kSiteQEmpty, kSiteItemFull, kSiteStageEmpty, kSiteStageFull,
-  kSiteSFree, kSiteSFull, kSitePFull, kSitePvDone, kSiteDrain
+  kSiteSFree, kSiteSFull, kSitePFull, kSitePvDone, kSiteDrain, kSiteQFull
 };
 
 __device__ __forceinline__ unsigned long long global_ns() {
@@ -121,7 +121,11 @@ __device__ __forceinline__ void cp_async_16_zfill(uint32_t dst, const void* src,
                : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+// Arrive (without a pending-count increment) on `bar` once all earlier cp.async of this thread
+// have completed.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
 __device__ __forceinline__ void cp_async_wait_0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 struct ItemInfo {   // written by the index warp, read by every role
@@ -162,7 +166,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t b_pvdone = b_pfull + 16;
   const uint32_t b_itemfull = b_pvdone + 16;
   const uint32_t b_itemempty = b_itemfull + 16;
-  const uint32_t b_qempty = b_itemempty + 16;
+  const uint32_t b_qempty = b_itemempty + 16;     // Q buffer free (MMA commit, once per item)
+  const uint32_t b_qfull = b_qempty + 8;          // Q buffer written (index warp, once per item)
   const uint32_t b_fin = b_qempty + 16;
 
   ItemInfo* const info = reinterpret_cast<ItemInfo*>(gbase + L.misc);
@@ -177,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < R; ++s) {
-      mbar_init(b_full + 8 * s, p.gather_tma ? 1 : kProducerWarps);
+      mbar_init(b_full + 8 * s, p.gather_tma ? 1 : 32 * kProducerWarps);
       mbar_init(b_empty + 8 * s, 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -187,8 +192,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(b_pvdone + 8 * b, 1);
       mbar_init(b_itemfull + 8 * b, 1);
       mbar_init(b_itemempty + 8 * b, 1 + 128 + kProducerWarps);
-      mbar_init(b_qempty + 8 * b, 1);
     }
+    mbar_init(b_qempty, 1);
+    mbar_init(b_qfull, 1);
     mbar_init(b_fin, 1);
     *abort_flag = 0;
     vote[0] = 0;
@@ -220,7 +226,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t item = blockIdx.x; item < n_items; item += stride, ++it) {
       const uint32_t b = it & 1, ph = (it >> 1) & 1;
       bool ok = wait_bar(b_itemempty + 8 * b, ph ^ 1, abort_flag, kSiteItemEmpty);
-      ok = ok && wait_bar(b_qempty + 8 * b, ph ^ 1, abort_flag, kSiteQEmpty);
       if (!__all_sync(0xffffffffu, ok)) break;
       int32_t group, kvh, chunk;
       decode_item(p, item, group, kvh, chunk);
@@ -234,34 +239,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         rows_in_group = 1;
         cols = min(p.chunk_cols, p.group - chunk * p.chunk_cols);
       }
-      // Q tile: rows = query columns c (NP, zero beyond cols), 4 regions of 64 dims, SW128.
-      const uint32_t qb = base + L.qbuf + b * L.q_bytes;
-      const int rg = lane >> 3, jc = lane & 7;
-#pragma unroll
-      for (int c0 = 0; c0 < NP; c0 += 8) {
-        uint4 v[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int c = c0 + i;
-          v[i] = make_uint4(0u, 0u, 0u, 0u);
-          if (c < cols) {
-            int64_t row, head;
-            if (UNION) {
-              row = row0 + c / p.group;
-              head = static_cast<int64_t>(kvh) * p.group + c % p.group;
-            } else {
-              row = row0;
-              head = static_cast<int64_t>(kvh) * p.group + chunk * p.chunk_cols + c;
-            }
-            v[i] = ldg_nc_v4(p.q + (row * p.n_qheads + head) * kHeadDim + lane * 8);
-          }
+      // Q tile rows = query columns c (NP, zero beyond cols), 4 regions of 64 dims, SW128.
+      // One shared buffer: the first kQPre rows are fetched into registers now and stored once
+      // the previous item's last QK^T has read the buffer.
+      auto q_src = [&](int c) -> const uint16_t* {
+        int64_t row, head;
+        if (UNION) {
+          row = row0 + c / p.group;
+          head = static_cast<int64_t>(kvh) * p.group + c % p.group;
+        } else {
+          row = row0;
+          head = static_cast<int64_t>(kvh) * p.group + chunk * p.chunk_cols + c;
         }
+        return p.q + (row * p.n_qheads + head) * kHeadDim + lane * 8;
+      };
+      constexpr int kQPre = NP < 16 ? NP : 16;
+      uint4 qv[kQPre];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int c = c0 + i;
-          sts_v4(qb + rg * (NP * 128) + (c >> 3) * 1024 + (c & 7) * 128 + ((jc ^ (c & 7)) << 4), v[i]);
-        }
-      }
+      for (int c = 0; c < kQPre; ++c) qv[c] = c < cols ? ldg_nc_v4(q_src(c)) : make_uint4(0u, 0u, 0u, 0u);
       int32_t nv;
       if (!UNION) {
         // Compact the row's valid slots (in order) into the slot list, as tensor-map rows.
@@ -299,9 +294,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         I.row0 = row0;
         I.rows_in_group = rows_in_group;
       }
-      fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_itemfull + 8 * b);
+      // Q: wait until the previous item's QK^T MMAs are done with the buffer.
+      if (!__all_sync(0xffffffffu, wait_bar(b_qempty, (it & 1) ^ 1, abort_flag, kSiteQEmpty))) break;
+      const uint32_t qb = base + L.qbuf;
+      const int rg = lane >> 3, jc = lane & 7;
+      auto q_store = [&](int c, uint4 v) {
+        sts_v4(qb + rg * (NP * 128) + (c >> 3) * 1024 + (c & 7) * 128 + ((jc ^ (c & 7)) << 4), v);
+      };
+#pragma unroll
+      for (int c = 0; c < kQPre; ++c) q_store(c, qv[c]);
+#pragma unroll
+      for (int c = kQPre; c < NP; ++c) q_store(c, c < cols ? ldg_nc_v4(q_src(c)) : make_uint4(0u, 0u, 0u, 0u));
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_qfull);
     }
   } else if (warp >= kProducerWarp0) {
     // ------------------------------------------------------------ gather producers
@@ -312,17 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int W = kProducerWarps;
     const bool tma = p.gather_tma != 0;
     uint32_t seq = 0, it = 0, issued = 0;
-    int pend_st = -1;                  // cp.async: stage filled by this warp, not yet signalled
     bool aborted = false;
-    auto flush = [&]() {
-      if (pend_st >= 0) {
-        cp_async_wait_0();
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(b_full + 8 * pend_st);
-        pend_st = -1;
-      }
-    };
     // Union slots come from global memory: each lane caches its slots for three tiles
     // (V(j-1), K(j), K(j+1) can be in flight around one another), in registers indexed
     // statically.  Per-token slots are read from the shared-memory slot list directly.
@@ -330,7 +328,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     int yc0[kPerLane], yc1[kPerLane], yc2[kPerLane];
     for (int64_t item = blockIdx.x; item < n_items && !aborted; item += stride, ++it) {
       const uint32_t b = it & 1, ph = (it >> 1) & 1;
-      if (!__all_sync(0xffffffffu, mbar_try_wait(b_itemfull + 8 * b, ph))) flush();
       if (!__all_sync(0xffffffffu, wait_bar(b_itemfull + 8 * b, ph, abort_flag, kSiteItemFull))) {
         aborted = true;
         break;
@@ -388,14 +385,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               cp_async_16_zfill(dst, src, pad ? 0u : 16u);
             }
           }
-          cp_async_commit();
-          if (pend_st >= 0) {
-            cp_async_wait_1();
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(b_full + 8 * pend_st);
-          }
-          pend_st = static_cast<int>(st);
+          // Each lane's arrival fires once all its earlier copies have landed; the MMA thread
+          // orders them before its tensor-core reads with a proxy fence after the wait.
+          cp_async_arrive_noinc(b_full + 8 * st);
         }
       };
       if (UNION && nt > 0) fill(yc0, 0);
@@ -412,12 +404,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t s = seq + q;
         const uint32_t st = s % R;
         const uint32_t par = ((s / R) & 1) ^ 1;
-        if (!__all_sync(0xffffffffu, mbar_try_wait(b_empty + 8 * st, par))) {
-          flush();
-          if (!__all_sync(0xffffffffu, wait_bar(b_empty + 8 * st, par, abort_flag, kSiteStageEmpty))) {
-            aborted = true;
-            break;
-          }
+        if (!__all_sync(0xffffffffu, wait_bar(b_empty + 8 * st, par, abort_flag, kSiteStageEmpty))) {
+          aborted = true;
+          break;
         }
         switch (tile % 3) {
           case 0: issue(yc0, tile, is_v, half, st); break;
@@ -432,8 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(b_itemempty + 8 * b);
     }
     if (!tma) {
-      if (aborted) cp_async_wait_0();
-      else flush();
+      cp_async_wait_0();
     } else if (aborted && pw == 0 && lane == 0) {
       // Drain: wait (bounded) for the newest phase of every stage that was filled.
       for (uint32_t s = issued > static_cast<uint32_t>(R) ? issued - R : 0; s < issued; ++s)
@@ -455,7 +443,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nt = (nv + kTileTokens - 1) / kTileTokens;
       __syncwarp();
       if (lane == 0) mbar_arrive(b_itemempty + 8 * b);
-      const uint32_t qaddr = base + L.qbuf + b * L.q_bytes;
+      const uint32_t qaddr = base + L.qbuf;
+      if (!__all_sync(0xffffffffu, wait_bar(b_qfull, it & 1, abort_flag, kSiteQFull))) {
+        aborted = true;
+        break;
+      }
       for (int j = 0; j <= nt; ++j) {
         if (j < nt) {
           // S^T(j) = K(j) . Q^T
@@ -469,6 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
+          fence_proxy_async_smem();   // cp.async stage writes -> tensor-core (async proxy) reads
           if (lane == 0) {
             const uint32_t klo = base + L.ring + (s_lo % R) * kStageBytes;
             const uint32_t khi = base + L.ring + (s_hi % R) * kStageBytes;
@@ -483,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_commit(b_empty + 8 * (s_lo % R));
             tc_commit(b_empty + 8 * (s_hi % R));
             tc_commit(b_sfull + 8 * sb);
-            if (j == nt - 1) tc_commit(b_qempty + 8 * b);
+            if (j == nt - 1) tc_commit(b_qempty);
           }
           __syncwarp();
         }
@@ -500,6 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
+          fence_proxy_async_smem();   // cp.async stage writes -> tensor-core (async proxy) reads
           if (lane == 0) {
             const uint32_t pbase = base + L.pbuf + pb * L.p_bytes;
 #pragma unroll
@@ -520,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (aborted) break;
-      if (nt == 0 && lane == 0) tc_commit(b_qempty + 8 * b);
+      if (nt == 0 && lane == 0) tc_commit(b_qempty);
       __syncwarp();
       seq += 4 * nt;
       js += nt;
