@@ -110,6 +110,31 @@ qsa_status qsa_sparse_prefill_ex(const void* q, const void* k_cache, const void*
                                  void* workspace, size_t workspace_bytes,
                                  const qsa_geometry* forced, void* stream);
 
+/* Allocation-free variant of qsa_sparse_prefill (same arguments, same results).  The pages
+ * have no counterpart: it exists for callers that must not allocate device memory -- code
+ * whose GPU memory is owned entirely by a framework's pool, latency-critical loops where an
+ * allocator call (and the device synchronisation it may cause) is unacceptable, and plugin
+ * hosts that give kernels no allocator.  Union-mode scratch lives in a fixed array of
+ * QSA_NOALLOC_SCRATCH_BYTES in device global memory that the library owns; every GPU on which
+ * the library is loaded holds that array until the process exits.
+ *   - A call whose union workspace (qsa_workspace_bytes) exceeds QSA_NOALLOC_SCRATCH_BYTES is
+ *     rejected with QSA_ERR_WORKSPACE before anything is enqueued.  The per-token path needs
+ *     no scratch and has no such limit.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress,
+ *     with that device current); make that first call before any stream capture.
+ *   - Every call uses the same array, which keeps the previous call's contents; nothing in it
+ *     needs to start at zero (each call writes every entry it later reads).  Calls whose work
+ *     overlaps on the GPU (different streams, or different host threads) race on the array:
+ *     order them on one stream or with events.
+ *   - No cudaMalloc, cudaFree or other allocating routine is called. */
+#define QSA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+qsa_status qsa_sparse_prefill_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* indices, const int32_t* topk_len,
+                                      void* out, float* lse,
+                                      int64_t n_rows, int32_t n_qheads, int32_t n_kvheads,
+                                      int32_t head_dim, int32_t topk, float scale,
+                                      int32_t union_g, void* stream);
+
 /* Bytes of union-mode workspace for a call (0 when union_g <= 1). */
 size_t qsa_workspace_bytes(int64_t n_rows, int32_t topk, int32_t union_g);
 

@@ -21,7 +21,11 @@ STATUS_NAMES = {0: "QSA_OK", 1: "QSA_ERR_INVALID_ARG", 2: "QSA_ERR_UNSUPPORTED",
 # Every symbol include/qsa.h declares (checked by the CPU test suite).
 EXPORTED = ["qsa_sparse_prefill", "qsa_sparse_prefill_ex", "qsa_workspace_bytes",
             "qsa_union_build", "qsa_select_geometry", "qsa_get_counters", "qsa_reset_counters",
-            "qsa_status_string", "qsa_version", "qsa_get_device_status"]
+            "qsa_status_string", "qsa_version", "qsa_get_device_status",
+            "qsa_sparse_prefill_noalloc"]
+
+# Size of the library-owned scratch array used by qsa_sparse_prefill_noalloc (include/qsa.h).
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class Geometry(ctypes.Structure):
@@ -63,6 +67,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qsa_sparse_prefill_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, f32, i32,
                                           i64, vp, sz, ctypes.POINTER(Geometry), vp]
     lib.qsa_sparse_prefill_ex.restype = ctypes.c_int
+    lib.qsa_sparse_prefill_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, f32,
+                                               i32, vp]
+    lib.qsa_sparse_prefill_noalloc.restype = ctypes.c_int
     lib.qsa_workspace_bytes.argtypes = [i64, i32, i32]
     lib.qsa_workspace_bytes.restype = sz
     lib.qsa_union_build.argtypes = [vp, vp, i64, i32, i32, i64, vp, vp, vp, vp, vp]
@@ -159,6 +166,37 @@ def sparse_prefill(q, k_cache, v_cache, indices, topk_len, scale: float, *, out=
                                     _ptr(topk_len), _ptr(out), _ptr(lse), R, Hq, Hkv, D, topk,
                                     float(scale), int(union_g), s)
     _check(st, "qsa_sparse_prefill")
+    return out, lse
+
+
+def sparse_prefill_noalloc(q, k_cache, v_cache, indices, topk_len, scale: float, *, out=None,
+                           lse=None, union_g: int = 0, stream=None):
+    """Same as sparse_prefill, through qsa_sparse_prefill_noalloc: the library allocates
+    nothing; union-mode scratch comes from its fixed NOALLOC_SCRATCH_BYTES device array.
+    Calls needing more union scratch than that are refused (RuntimeError, QSA_ERR_WORKSPACE).
+    Calls that overlap on the GPU share the array and race: keep them on one stream."""
+    import torch
+    lib = load_library()
+    _require(q, torch.bfloat16, "q", 3)
+    _require(k_cache, torch.bfloat16, "k_cache", 3)
+    _require(v_cache, torch.bfloat16, "v_cache", 3)
+    _require(indices, torch.int32, "indices", 2)
+    _require(topk_len, torch.int32, "topk_len", 1)
+    R, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((R, Hq), dtype=torch.float32, device=q.device)
+    st = lib.qsa_sparse_prefill_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(indices),
+                                        _ptr(topk_len), _ptr(out), _ptr(lse), R, Hq,
+                                        k_cache.shape[1], D, indices.shape[1], float(scale),
+                                        int(union_g), _stream_ptr(stream))
+    if st == 3:
+        raise RuntimeError(
+            f"qsa_sparse_prefill_noalloc failed: QSA_ERR_WORKSPACE (union scratch of "
+            f"{workspace_bytes(R, indices.shape[1], union_g)} bytes exceeds the fixed "
+            f"{NOALLOC_SCRATCH_BYTES} bytes)")
+    _check(st, "qsa_sparse_prefill_noalloc")
     return out, lse
 
 
