@@ -226,6 +226,13 @@ def run_gpu(args, rank, world, local_rank):
                                workspace=ws, stream=stream)
 
     geo = binding.select_geometry(w.n_qheads, w.n_kvheads, args.union, w.topk, w.head_dim, w.n_rows)
+    # gather ceiling on this workload's own K cache and selected rows (KV head 0)
+    valid = w.indices[w.indices >= 0].astype(np.int64) * w.n_kvheads
+    n_pieces = min(len(valid) // 128, 4096)
+    table = torch.from_numpy(valid[: n_pieces * 128].astype(np.int32).reshape(n_pieces, 128)).to(dev)
+    k_rows = k.view(-1, w.head_dim)
+    binding.probe_gather_ceiling(k_rows, table, pieces_per_cta=200)
+    ceiling_gbs = max(binding.probe_gather_ceiling(k_rows, table) for _ in range(3))
     for _ in range(args.warmup):
         call()
     torch.cuda.synchronize()
@@ -332,6 +339,10 @@ def run_gpu(args, rank, world, local_rank):
         "roofline_us": max(t_tc, t_hbm) * 1e6,
         "gathered_bytes": stats["gathered"],
         "gather_gbs": stats["gathered"] / kernel_s / 1e9,
+        "gather_ceiling_gbs": ceiling_gbs,
+        "frac_of_gather_ceiling": stats["gathered"] / kernel_s / 1e9 / ceiling_gbs,
+        "gather_ceiling_source": "qsa_probe_gather_ceiling on this workload's K cache and rows "
+                                 "(same engine and ring, no compute)",
         "kernel_ms": ms,
     }
     rows_total = w.n_rows * world

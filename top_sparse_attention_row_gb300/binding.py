@@ -22,7 +22,7 @@ STATUS_NAMES = {0: "QSA_OK", 1: "QSA_ERR_INVALID_ARG", 2: "QSA_ERR_UNSUPPORTED",
 EXPORTED = ["qsa_sparse_prefill", "qsa_sparse_prefill_ex", "qsa_workspace_bytes",
             "qsa_union_build", "qsa_select_geometry", "qsa_get_counters", "qsa_reset_counters",
             "qsa_status_string", "qsa_version", "qsa_get_device_status",
-            "qsa_sparse_prefill_noalloc"]
+            "qsa_sparse_prefill_noalloc", "qsa_probe_gather_ceiling"]
 
 # Size of the library-owned scratch array used by qsa_sparse_prefill_noalloc (include/qsa.h).
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -70,6 +70,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qsa_sparse_prefill_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, f32,
                                                i32, vp]
     lib.qsa_sparse_prefill_noalloc.restype = ctypes.c_int
+    lib.qsa_probe_gather_ceiling.argtypes = [vp, i64, vp, i64, i32, ctypes.POINTER(f32), vp]
+    lib.qsa_probe_gather_ceiling.restype = ctypes.c_int
     lib.qsa_workspace_bytes.argtypes = [i64, i32, i32]
     lib.qsa_workspace_bytes.restype = sz
     lib.qsa_union_build.argtypes = [vp, vp, i64, i32, i32, i64, vp, vp, vp, vp, vp]
@@ -218,6 +220,22 @@ def union_build(indices, topk_len, union_g: int, n_kv_slots: int = 0, want_sorte
                              _ptr(srt), _ptr(uidx), _ptr(ubits), _ptr(ulen), _stream_ptr(stream))
     _check(st, "qsa_union_build")
     return srt, uidx, ubits, ulen
+
+
+def probe_gather_ceiling(cache_rows, row_table, pieces_per_cta: int = 1500, stream=None) -> float:
+    """Gather-ceiling probe (qsa_probe_gather_ceiling).  cache_rows: [n_rows, 256] bf16 view of a
+    KV cache; row_table: [n_pieces, 128] int32 row numbers.  Returns GB/s over all SMs."""
+    import torch
+    lib = load_library()
+    _require(cache_rows, torch.bfloat16, "cache_rows", 2)
+    _require(row_table, torch.int32, "row_table", 2)
+    ms = ctypes.c_float(0.0)
+    st = lib.qsa_probe_gather_ceiling(_ptr(cache_rows), cache_rows.shape[0], _ptr(row_table),
+                                      row_table.shape[0], int(pieces_per_cta), ctypes.byref(ms),
+                                      _stream_ptr(stream))
+    _check(st, "qsa_probe_gather_ceiling")
+    sms = torch.cuda.get_device_properties(cache_rows.device).multi_processor_count
+    return sms * pieces_per_cta * 32768 / (ms.value * 1e-3) / 1e9
 
 
 def workspace_bytes(n_rows: int, topk: int, union_g: int) -> int:

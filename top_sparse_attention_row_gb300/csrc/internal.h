@@ -5,7 +5,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
-#include "../../include/qsa.h"
+#include "qsa.h"   // include/ is on the compiler include path
 
 namespace qsa {
 
@@ -17,7 +17,7 @@ constexpr int kSoftmaxWarps = 4;             // warps 0-3: softmax + epilogue (T
 constexpr int kMmaWarp = 4;                  // MMA issue + tensor-memory owner
 constexpr int kIndexWarp = 5;                // slot compaction, Q tile, item info
 constexpr int kProducerWarp0 = 6;            // first gather warp
-constexpr int kProducerWarps = 6;            // gather warps issuing every piece together
+constexpr int kProducerWarps = 6;            // gather warps, each owning one ring stage
 constexpr int kThreads = 32 * (kProducerWarp0 + kProducerWarps);
 constexpr int kMinStages = 4;                // ring must hold V(j) and K(j+1) together
 constexpr int kMaxStages = 8;

@@ -1,0 +1,131 @@
+// Gather-ceiling probe: how fast can one GB300 SM pull random half-rows (256 B) of a KV cache
+// from L2 into shared memory, with nothing else running?  It uses the same engine and shapes as
+// the attention kernel's producers -- cp.async 16-byte copies, 32 KiB pieces of 128 rows x 256 B,
+// 128-byte swizzled destinations, a 6-stage ring -- but the consumer only releases each stage,
+// so the result bounds what the gather side of the kernel can approach.
+//
+// Each of the six producer warps owns one stage of the ring and gathers every piece that lands
+// on it, so no two warps ever wait on different phases of one stage.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace qsa {
+namespace {
+
+constexpr int kProbeStages = 6;
+constexpr int kProbeWarps = kProbeStages + 1;     // six owners + one releasing consumer
+
+__device__ __forceinline__ unsigned long long probe_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ bool probe_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = probe_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (probe_ns() - t0 > 1000000000ull) {
+      *abort_flag = 1;
+      atomicExch(status, 1);
+      return false;
+    }
+  }
+  return true;
+}
+
+__global__ void __launch_bounds__(32 * kProbeWarps, 1)
+    gather_probe_kernel(const uint8_t* __restrict__ cache, const int32_t* __restrict__ rows,
+                        int64_t n_table_pieces, int32_t pieces_per_cta, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  const uint32_t full = base + kProbeStages * kStageBytes;
+  const uint32_t empty = full + 8 * kProbeStages;
+  __shared__ int abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kProbeStages; ++s) {
+      mbar_init(full + 8 * s, 32);
+      mbar_init(empty + 8 * s, 1);
+    }
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  volatile int* ab = &abort_flag;
+  if (warp < kProbeStages) {
+    const int st = warp;
+    for (int p = st; p < pieces_per_cta; p += kProbeStages) {
+      const uint32_t par = ((p / kProbeStages) & 1) ^ 1;
+      if (!__all_sync(0xffffffffu, probe_wait(empty + 8 * st, par, ab, status))) break;
+      const int32_t* prow = rows + ((blockIdx.x * 131 + p) % n_table_pieces) * kTileTokens;
+      const uint32_t dst = base + st * kStageBytes;
+      const int ch = lane & 15;
+#pragma unroll 8
+      for (int i = 0; i < 64; ++i) {
+        const int t = 2 * i + (lane >> 4);
+        const uint8_t* src = cache + static_cast<int64_t>(prow[t]) * (kHeadDim * 2) + ch * 16;
+        const uint32_t d = dst + (ch >> 3) * 16384 + t * 128 + (((ch & 7) ^ (t & 7)) << 4);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+      }
+      asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(full + 8 * st)
+                   : "memory");
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  } else {
+    for (int p = 0; p < pieces_per_cta; ++p) {
+      const int st = p % kProbeStages;
+      if (!__all_sync(0xffffffffu, probe_wait(full + 8 * st, (p / kProbeStages) & 1, ab, status)))
+        break;
+      if (lane == 0) mbar_arrive(empty + 8 * st);
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+}
+
+}  // namespace
+}  // namespace qsa
+
+extern "C" qsa_status qsa_probe_gather_ceiling(const void* cache, int64_t n_rows,
+                                               const int32_t* rows, int64_t n_table_pieces,
+                                               int32_t pieces_per_cta, float* ms_out,
+                                               void* stream_v) {
+  if (!cache || !rows || !ms_out || n_rows <= 0 || n_table_pieces <= 0 || pieces_per_cta <= 0)
+    return QSA_ERR_INVALID_ARG;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return QSA_ERR_CUDA;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  const int smem = qsa::kProbeStages * qsa::kStageBytes + 16 * qsa::kProbeStages + 1024;
+  if (cudaFuncSetAttribute(qsa::gather_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem) != cudaSuccess)
+    return QSA_ERR_CUDA;
+  int* status = nullptr;
+  // measurement helper, not the hot path: a 4-byte status word and two events per call
+  if (cudaMallocAsync(&status, sizeof(int), stream) != cudaSuccess) return QSA_ERR_CUDA;
+  cudaMemsetAsync(status, 0, sizeof(int), stream);
+  cudaEvent_t a, b;
+  cudaEventCreate(&a);
+  cudaEventCreate(&b);
+  cudaEventRecord(a, stream);
+  qsa::gather_probe_kernel<<<sms, 32 * qsa::kProbeWarps, smem, stream>>>(
+      static_cast<const uint8_t*>(cache), rows, n_table_pieces, pieces_per_cta, status);
+  cudaEventRecord(b, stream);
+  int h_status = 0;
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&h_status, status, sizeof(int), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  float ms = 0.f;
+  if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, a, b);
+  cudaEventDestroy(a);
+  cudaEventDestroy(b);
+  cudaFreeAsync(status, stream);
+  if (e != cudaSuccess) return QSA_ERR_CUDA;
+  if (h_status != 0) return QSA_ERR_TIMEOUT;
+  *ms_out = ms;
+  return QSA_OK;
+}
