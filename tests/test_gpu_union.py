@@ -27,23 +27,44 @@ def _dev(a):
 
 @pytest.mark.parametrize("G", [1, 2, 3, 4, 8])
 @pytest.mark.parametrize("with_len", [False, True])
-def test_union_build_bit_exact(B, G, with_len):
+@pytest.mark.parametrize("want_sorted", [True, False])     # bitonic kernel / bitmap kernel
+def test_union_build_bit_exact(B, G, with_len, want_sorted):
     import torch
     idx, tl = pins.union_case(400 + G, R=37, K=40, S=90, G=G, with_len=with_len)
-    srt, uidx, ubits, ulen = B.union_build(_dev(idx), _dev(tl), G)
+    srt, uidx, ubits, ulen = B.union_build(_dev(idx), _dev(tl), G, want_sorted=want_sorted)
     torch.cuda.synchronize()
     e_idx, e_bits, e_len = oracle.union_build(idx, tl, G)
-    assert np.array_equal(srt.cpu().numpy(), oracle.sorted_rows(idx, tl))
+    if want_sorted:
+        assert np.array_equal(srt.cpu().numpy(), oracle.sorted_rows(idx, tl))
     assert np.array_equal(ulen.cpu().numpy(), e_len)
     assert np.array_equal(uidx.cpu().numpy(), e_idx)
     assert np.array_equal(ubits.cpu().numpy(), e_bits)
+
+
+@pytest.mark.parametrize("S", [1 << 17, 600_000, 5_000_000])
+def test_union_build_wide_slot_ranges(B, S):
+    """Slot numbers beyond one bitmap window (131072 slots) take several windows; a slot
+    count filter also applies."""
+    import torch
+    rng = np.random.default_rng(S)
+    R, K, G = 45, 300, 4
+    base = rng.choice(S, size=K, replace=False)
+    idx = np.stack([np.where(rng.random(K) < 0.3, rng.integers(0, S, size=K), base) for _ in range(R)]).astype(np.int32)
+    idx[rng.random(idx.shape) < 0.05] = -1
+    for n_slots in (0, S // 2):
+        _, uidx, ubits, ulen = B.union_build(_dev(idx), None, G, n_kv_slots=n_slots, want_sorted=False)
+        torch.cuda.synchronize()
+        e_idx, e_bits, e_len = oracle.union_build(idx, None, G, n_kv_slots=n_slots)
+        assert np.array_equal(ulen.cpu().numpy(), e_len)
+        assert np.array_equal(uidx.cpu().numpy(), e_idx)
+        assert np.array_equal(ubits.cpu().numpy(), e_bits)
 
 
 def test_union_build_walk_bit_exact(B):
     import torch
     idx = W.random_walk_indices(np.random.default_rng(5), 700, 512)
     for G in (2, 4):
-        srt, uidx, ubits, ulen = B.union_build(_dev(idx), None, G)
+        srt, uidx, ubits, ulen = B.union_build(_dev(idx), None, G, want_sorted=False)
         torch.cuda.synchronize()
         e_idx, e_bits, e_len = oracle.union_build(idx, None, G)
         assert np.array_equal(ulen.cpu().numpy(), e_len)

@@ -286,9 +286,9 @@ qsa_status qsa_union_build(const int32_t* indices, const int32_t* topk_len, int6
   if (!indices || !union_idx || !union_bits || !union_len) return QSA_ERR_INVALID_ARG;
   if (n_rows < 0 || topk <= 0 || union_g < 1 || union_g > 8 || n_kv_slots < 0)
     return QSA_ERR_INVALID_ARG;
-  if (n_rows > INT32_MAX ||
-      qsa::union_build_smem_bytes(topk, union_g) > static_cast<size_t>(qsa::kUnionMaxSmem))
-    return QSA_ERR_UNSUPPORTED;
+  const size_t need = sorted_out ? qsa::union_sort_smem_bytes(topk, union_g)
+                                 : qsa::union_build_smem_bytes(topk, union_g);
+  if (n_rows > INT32_MAX || need > static_cast<size_t>(qsa::kUnionMaxSmem)) return QSA_ERR_UNSUPPORTED;
   if (n_rows == 0) return QSA_OK;
   int32_t sms = 0;
   qsa_status st = device_sms(&sms);

@@ -97,7 +97,8 @@ cudaError_t launch_union_build(const int32_t* indices, const int32_t* topk_len, 
                                int32_t topk, int32_t union_g, int64_t n_kv_slots,
                                int32_t* sorted_out, int32_t* union_idx, uint8_t* union_bits,
                                int32_t* union_len, bool pad_outputs, cudaStream_t stream);
-size_t union_build_smem_bytes(int32_t topk, int32_t union_g);
+size_t union_build_smem_bytes(int32_t topk, int32_t union_g);   // hot-path (bitmap) kernel
+size_t union_sort_smem_bytes(int32_t topk, int32_t union_g);    // sorted-rows (bitonic) kernel
 cudaError_t read_and_clear_device_status(cudaStream_t stream, int32_t* status);
 
 }  // namespace qsa

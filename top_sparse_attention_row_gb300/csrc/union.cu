@@ -6,12 +6,18 @@
 // selected and ORs in the bit of every row that did.  Accuracy Tests on the same page give the
 // contract: each slot once, bits = OR of owners, -1 dropped.
 //
-// Here the sort and the union build are one kernel: the group's G rows are loaded into shared
-// memory (invalid entries -- beyond topk_len, negative, >= n_kv_slots -- become INT_MAX), each
-// row is bitonic-sorted in place, every valid first occurrence is searched in the other rows,
-// and a block-wide scan over (row, rank) order gives each emitted slot its place in the
-// canonical list (row 0's emitted slots ascending, then row 1's, ...).  No atomics: the output
-// is deterministic.  Nothing outlives the call and nothing is read back to the host.
+// Two kernels produce the same lists, bits and lengths:
+//  * union_bitmap_kernel (the hot path): slot numbers are small integers, so each row's valid
+//    set is written as a bitmap over the group's slot window in shared memory -- a counting sort
+//    that also drops repeats.  A row's emitted slots are its bits not set in any earlier row's
+//    bitmap, its ownership bits come from one bit test per row, and popcount prefix sums give
+//    every emitted slot its place.  O(G*topk + G*window/32) work, a handful of barriers.
+//  * union_build_kernel (when the caller also wants each row's sorted slots with repeats, as
+//    qsa_union_build can return): rows are bitonic-sorted in shared memory and every first
+//    occurrence is searched (lower_bound) in the other rows, the pages' formulation.
+// The canonical order is row 0's emitted slots ascending, then row 1's, and so on.  Both are
+// deterministic (the bitmap kernel's atomicOr on shared words is order independent), keep
+// nothing past the call and read nothing back to the host.
 #include <atomic>
 #include <climits>
 
@@ -165,7 +171,198 @@ __global__ void __launch_bounds__(kUnionThreads)
   }
 }
 
+namespace {
+
+constexpr int kBmThreads = 256;
+constexpr int kBmMaxWords = 4096;      // bitmap window: up to 131072 slots per pass
+
+__device__ __forceinline__ int block_reduce_max(int v, int* scratch) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) scratch[w] = v;
+  __syncthreads();
+  int r = scratch[0];
+  for (int i = 1; i < kBmThreads / 32; ++i) r = max(r, scratch[i]);
+  return r;
+}
+
+__device__ __forceinline__ int block_reduce_min(int v, int* scratch) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) scratch[w] = v;
+  __syncthreads();
+  int r = scratch[0];
+  for (int i = 1; i < kBmThreads / 32; ++i) r = min(r, scratch[i]);
+  return r;
+}
+
+// Exclusive prefix of v over the block; *total gets the block sum.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* scratch, int* total) {
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  __syncthreads();
+  if (lane == 31) scratch[w] = incl;
+  __syncthreads();
+  int before = 0, sum = 0;
+  for (int i = 0; i < kBmThreads / 32; ++i) {
+    if (i < w) before += scratch[i];
+    sum += scratch[i];
+  }
+  *total = sum;
+  return before + incl - v;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kBmThreads)
+    union_bitmap_kernel(const int32_t* __restrict__ indices, const int32_t* __restrict__ topk_len,
+                        int64_t n_rows, int32_t topk, int32_t G, int32_t W, int64_t n_kv_slots,
+                        int32_t* __restrict__ union_idx, uint8_t* __restrict__ union_bits,
+                        int32_t* __restrict__ union_len, int32_t pad_outputs) {
+  extern __shared__ uint32_t sm_words[];
+  int32_t* ent = reinterpret_cast<int32_t*>(sm_words);    // [G][topk]: valid slot or -1
+  uint32_t* bm = sm_words + G * topk;                      // [G][W] bitmaps of one window
+  __shared__ int scratch[kBmThreads / 32];
+  __shared__ int row_total[8], row_base[8], row_done[8];
+
+  const int64_t group = blockIdx.x;
+  const int64_t r0 = group * G;
+  const int Gp = static_cast<int>(n_rows - r0 < G ? n_rows - r0 : G);
+  const int tid = threadIdx.x;
+  const int64_t cap = static_cast<int64_t>(G) * topk;
+  int32_t* out_idx = union_idx + group * cap;
+  uint8_t* out_bits = union_bits + group * cap;
+
+  // 1. valid slots of the group's rows (topk_len, negative, >= n_kv_slots filtered) and their max
+  int my_max = -1;
+  for (int e = tid; e < Gp * topk; e += kBmThreads) {
+    const int u = e / topk, j = e - u * topk;
+    const int64_t r = r0 + u;
+    int Lr = topk;
+    if (topk_len) Lr = min(max(topk_len[r], 0), topk);
+    int32_t x = -1;
+    if (j < Lr) x = indices[r * topk + j];
+    if (x < 0 || (n_kv_slots > 0 && x >= n_kv_slots)) x = -1;
+    ent[e] = x;
+    my_max = max(my_max, x);
+  }
+  const int gmax = block_reduce_max(my_max, scratch);
+  if (tid < 8) { row_total[tid] = 0; row_done[tid] = 0; }
+  __syncthreads();
+
+  // 2. windows of W*32 slots, ascending; two passes (counts, then placement) unless one window
+  //    covers every slot, in which case the bitmaps are built once.
+  const int64_t span = static_cast<int64_t>(W) * 32;
+  const bool one_window = gmax >= 0 && gmax < span;
+  for (int pass = 0; pass < 2 && gmax >= 0; ++pass) {
+    int64_t wbase = 0;
+    if (pass == 1) {
+      if (tid == 0) {
+        int acc = 0;
+        for (int t = 0; t < Gp; ++t) { row_base[t] = acc; acc += row_total[t]; }
+      }
+      __syncthreads();
+    }
+    while (wbase <= gmax) {
+      const int64_t need_words = (gmax - wbase) / 32 + 1;
+      const int active = static_cast<int>(need_words < W ? need_words : W);
+      const int wpt = (active + kBmThreads - 1) / kBmThreads;   // words per thread
+      if (!(pass == 1 && one_window)) {
+        for (int i = tid; i < Gp * active; i += kBmThreads) bm[(i / active) * W + i % active] = 0u;
+        __syncthreads();
+        for (int e = tid; e < Gp * topk; e += kBmThreads) {
+          const int32_t x = ent[e];
+          if (x >= wbase && x < wbase + span) {
+            const int u = e / topk;
+            const int off = static_cast<int>(x - wbase);
+            atomicOr(&bm[u * W + (off >> 5)], 1u << (off & 31));
+          }
+        }
+        __syncthreads();
+      }
+      const int w0 = tid * wpt, w1 = min(w0 + wpt, active);
+      for (int t = 0; t < Gp; ++t) {
+        // this thread's emitted count for row t in its words
+        int c = 0;
+        for (int w = w0; w < w1; ++w) {
+          uint32_t earlier = 0u;
+          for (int u = 0; u < t; ++u) earlier |= bm[u * W + w];
+          c += __popc(bm[t * W + w] & ~earlier);
+        }
+        int total = 0;
+        const int off = block_exclusive_scan(c, scratch, &total);
+        if (pass == 0) {
+          if (tid == 0) row_total[t] += total;
+        } else {
+          int pos = row_base[t] + row_done[t] + off;
+          for (int w = w0; w < w1; ++w) {
+            uint32_t earlier = 0u;
+            for (int u = 0; u < t; ++u) earlier |= bm[u * W + w];
+            uint32_t m = bm[t * W + w] & ~earlier;
+            while (m) {
+              const int b = __ffs(m) - 1;
+              m &= m - 1u;
+              uint32_t owners = 0u;
+              for (int u = 0; u < Gp; ++u) owners |= ((bm[u * W + w] >> b) & 1u) << u;
+              out_idx[pos] = static_cast<int32_t>(wbase + 32 * w + b);
+              out_bits[pos] = static_cast<uint8_t>(owners);
+              ++pos;
+            }
+          }
+          __syncthreads();
+          if (tid == 0) row_done[t] += total;
+        }
+        __syncthreads();
+      }
+      if (one_window) break;
+      // next window starts at the smallest slot past this one
+      int my_next = INT_MAX;
+      for (int e = tid; e < Gp * topk; e += kBmThreads) {
+        const int32_t x = ent[e];
+        if (x >= wbase + span) my_next = min(my_next, x);
+      }
+      const int nxt = block_reduce_min(my_next, scratch);
+      if (nxt == INT_MAX) break;
+      wbase = nxt;
+    }
+  }
+  int total = 0;
+  for (int t = 0; t < Gp; ++t) total += row_total[t];
+  if (tid == 0) union_len[group] = total;
+  if (pad_outputs) {
+    for (int64_t e = total + tid; e < cap; e += kBmThreads) {
+      out_idx[e] = -1;
+      out_bits[e] = 0;
+    }
+  }
+}
+
+int union_bitmap_words(int32_t topk, int32_t union_g) {
+  const int64_t ent = static_cast<int64_t>(union_g) * topk * 4;
+  const int64_t room = static_cast<int64_t>(kUnionMaxSmem) - ent;
+  if (room <= 0) return 0;
+  int64_t w = room / (static_cast<int64_t>(union_g) * 4);
+  w = w / kBmThreads * kBmThreads;
+  return static_cast<int>(w < kBmMaxWords ? w : kBmMaxWords);
+}
+
 size_t union_build_smem_bytes(int32_t topk, int32_t union_g) {
+  // shared memory of the bitmap kernel at its largest window (0 if not even 256 words fit)
+  const int w = union_bitmap_words(topk, union_g);
+  if (w < kBmThreads) return static_cast<size_t>(kUnionMaxSmem) + 1;
+  return static_cast<size_t>(union_g) * (static_cast<size_t>(topk) + w) * 4;
+}
+
+size_t union_sort_smem_bytes(int32_t topk, int32_t union_g) {
   const size_t Kp = static_cast<size_t>(next_pow2(topk));
   return static_cast<size_t>(union_g) * Kp * (sizeof(int32_t) + sizeof(uint16_t));
 }
@@ -175,8 +372,28 @@ cudaError_t launch_union_build(const int32_t* indices, const int32_t* topk_len, 
                                int32_t* sorted_out, int32_t* union_idx, uint8_t* union_bits,
                                int32_t* union_len, bool pad_outputs, cudaStream_t stream) {
   if (n_rows == 0) return cudaSuccess;
+  const int64_t n_groups = (n_rows + union_g - 1) / union_g;
+  if (sorted_out == nullptr) {
+    const int W = union_bitmap_words(topk, union_g);
+    if (W < kBmThreads) return cudaErrorInvalidValue;
+    const size_t smem = static_cast<size_t>(union_g) * (static_cast<size_t>(topk) + W) * 4;
+    static std::atomic<int> bm_opted_in[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || bm_opted_in[dev].load() < static_cast<int>(smem)) {
+      e = cudaFuncSetAttribute(union_bitmap_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem));
+      if (e != cudaSuccess) return e;
+      if (dev >= 0 && dev < 64) bm_opted_in[dev].store(static_cast<int>(smem));
+    }
+    union_bitmap_kernel<<<static_cast<unsigned>(n_groups), kBmThreads, smem, stream>>>(
+        indices, topk_len, n_rows, topk, union_g, W, n_kv_slots, union_idx, union_bits, union_len,
+        pad_outputs ? 1 : 0);
+    return cudaGetLastError();
+  }
   const int Kp = next_pow2(topk);
-  const size_t smem = union_build_smem_bytes(topk, union_g);
+  const size_t smem = union_sort_smem_bytes(topk, union_g);
   static std::atomic<int> opted_in[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -187,7 +404,6 @@ cudaError_t launch_union_build(const int32_t* indices, const int32_t* topk_len, 
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) opted_in[dev].store(static_cast<int>(smem));
   }
-  const int64_t n_groups = (n_rows + union_g - 1) / union_g;
   union_build_kernel<<<static_cast<unsigned>(n_groups), kUnionThreads, smem, stream>>>(
       indices, topk_len, n_rows, topk, union_g, Kp, n_kv_slots, sorted_out, union_idx, union_bits,
       union_len, pad_outputs ? 1 : 0);
