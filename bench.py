@@ -231,8 +231,11 @@ def run_gpu(args, rank, world, local_rank):
     n_pieces = min(len(valid) // 128, 4096)
     table = torch.from_numpy(valid[: n_pieces * 128].astype(np.int32).reshape(n_pieces, 128)).to(dev)
     k_rows = k.view(-1, w.head_dim)
-    binding.probe_gather_ceiling(k_rows, table, pieces_per_cta=200)
-    ceiling_gbs = max(binding.probe_gather_ceiling(k_rows, table) for _ in range(3))
+    ceilings = {}
+    for eng in ("tma", "cpasync"):
+        binding.probe_gather_ceiling(k_rows, table, pieces_per_cta=200, engine=eng)
+        ceilings[eng] = max(binding.probe_gather_ceiling(k_rows, table, engine=eng) for _ in range(3))
+    ceiling_gbs = max(ceilings.values())
     for _ in range(args.warmup):
         call()
     torch.cuda.synchronize()
@@ -341,8 +344,9 @@ def run_gpu(args, rank, world, local_rank):
         "gather_gbs": stats["gathered"] / kernel_s / 1e9,
         "gather_ceiling_gbs": ceiling_gbs,
         "frac_of_gather_ceiling": stats["gathered"] / kernel_s / 1e9 / ceiling_gbs,
+        "gather_ceiling_by_engine_gbs": ceilings,
         "gather_ceiling_source": "qsa_probe_gather_ceiling on this workload's K cache and rows "
-                                 "(same engine and ring, no compute)",
+                                 "(the kernel's ring and engines, no compute; the faster engine)",
         "kernel_ms": ms,
     }
     rows_total = w.n_rows * world

@@ -159,15 +159,16 @@ qsa_status qsa_select_geometry(int32_t n_qheads, int32_t n_kvheads, int32_t unio
                                int32_t num_sms, qsa_geometry* out);
 
 /* Measurement helper: the gather ceiling.  Gathers the first 256 bytes of the cache rows listed
- * in `rows` ([n_table_pieces, 128] int32 row numbers < n_rows of a [n_rows, 256] bf16 cache),
- * 128 rows (32 KiB) per piece, `pieces_per_cta` pieces on every SM, into shared memory with the
- * attention kernel's gather engine and ring shape, and nothing else.  Writes the elapsed GPU
- * time in milliseconds to *ms_out (host pointer) and synchronises `stream`.  The pages motivate
+ * in `rows` ([n_table_pieces, 128] int32 row numbers < n_rows of a [n_rows, 256] bf16 cache,
+ * 16-byte aligned), 128 rows (32 KiB) per piece, `pieces_per_cta` pieces on every SM, into shared
+ * memory with one of the attention kernel's gather engines (engine 0 = cp.async 16-byte copies,
+ * 1 = TMA tile::gather4) and its ring shape, and nothing else.  Writes the elapsed GPU time in
+ * milliseconds to *ms_out (host pointer) and synchronises `stream`.  The pages motivate
  * it: the gather is the share of the sparse kernel that grows on newer parts ("DSA prefill ...
  * triton_sparse_mla", Speed Tests), so the kernel is judged against the measured gather rate. */
 qsa_status qsa_probe_gather_ceiling(const void* cache, int64_t n_rows, const int32_t* rows,
                                     int64_t n_table_pieces, int32_t pieces_per_cta,
-                                    float* ms_out, void* stream);
+                                    int32_t engine, float* ms_out, void* stream);
 
 void qsa_get_counters(qsa_counters* out);   /* host pointer */
 void qsa_reset_counters(void);

@@ -99,6 +99,11 @@ def test_entry_validation_before_any_cuda_call(lib):
     assert ub(None, None, 10, 16, 2, 0, None, fake, fake, fake, None) == 1
     assert ub(fake, None, 10, 16, 0, 0, None, fake, fake, fake, None) == 1
     assert ub(fake, None, 10, 1 << 16, 8, 0, None, fake, fake, fake, None) == 2
+    pr = lib.qsa_probe_gather_ceiling
+    ms = ctypes.c_float(0.0)
+    assert pr(fake, 1000, fake, 4, 10, 2, ctypes.byref(ms), None) == 1      # unknown engine
+    assert pr(fake + 8, 1000, fake, 4, 10, 1, ctypes.byref(ms), None) == 1  # misaligned cache
+    assert pr(fake, 1000, fake, 0, 10, 0, ctypes.byref(ms), None) == 1      # empty row table
 
 
 def test_workspace_bytes(lib):

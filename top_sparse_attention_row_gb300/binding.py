@@ -70,7 +70,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qsa_sparse_prefill_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, f32,
                                                i32, vp]
     lib.qsa_sparse_prefill_noalloc.restype = ctypes.c_int
-    lib.qsa_probe_gather_ceiling.argtypes = [vp, i64, vp, i64, i32, ctypes.POINTER(f32), vp]
+    lib.qsa_probe_gather_ceiling.argtypes = [vp, i64, vp, i64, i32, i32, ctypes.POINTER(f32), vp]
     lib.qsa_probe_gather_ceiling.restype = ctypes.c_int
     lib.qsa_workspace_bytes.argtypes = [i64, i32, i32]
     lib.qsa_workspace_bytes.restype = sz
@@ -222,17 +222,22 @@ def union_build(indices, topk_len, union_g: int, n_kv_slots: int = 0, want_sorte
     return srt, uidx, ubits, ulen
 
 
-def probe_gather_ceiling(cache_rows, row_table, pieces_per_cta: int = 1500, stream=None) -> float:
+GATHER_ENGINES = {"cpasync": 0, "tma": 1}
+
+
+def probe_gather_ceiling(cache_rows, row_table, pieces_per_cta: int = 1500, engine: str = "tma",
+                         stream=None) -> float:
     """Gather-ceiling probe (qsa_probe_gather_ceiling).  cache_rows: [n_rows, 256] bf16 view of a
-    KV cache; row_table: [n_pieces, 128] int32 row numbers.  Returns GB/s over all SMs."""
+    KV cache; row_table: [n_pieces, 128] int32 row numbers; engine: "tma" (tile::gather4) or
+    "cpasync".  Returns GB/s over all SMs."""
     import torch
     lib = load_library()
     _require(cache_rows, torch.bfloat16, "cache_rows", 2)
     _require(row_table, torch.int32, "row_table", 2)
     ms = ctypes.c_float(0.0)
     st = lib.qsa_probe_gather_ceiling(_ptr(cache_rows), cache_rows.shape[0], _ptr(row_table),
-                                      row_table.shape[0], int(pieces_per_cta), ctypes.byref(ms),
-                                      _stream_ptr(stream))
+                                      row_table.shape[0], int(pieces_per_cta),
+                                      GATHER_ENGINES[engine], ctypes.byref(ms), _stream_ptr(stream))
     _check(st, "qsa_probe_gather_ceiling")
     sms = torch.cuda.get_device_properties(cache_rows.device).multi_processor_count
     return sms * pieces_per_cta * 32768 / (ms.value * 1e-3) / 1e9

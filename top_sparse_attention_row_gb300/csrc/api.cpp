@@ -128,12 +128,12 @@ void to_public(const Geometry& g, qsa_geometry* out) {
   out->n_items = g.n_items;
 }
 
-// Gather engine: cp.async 16-byte copies by default; QSA_GATHER=tma selects TMA tile::gather4
-// (both are exact; the switch exists to compare them).
+// Gather engine: TMA tile::gather4 by default; QSA_GATHER=cpasync selects cp.async 16-byte
+// copies (both are exact; the switch exists to compare them).
 bool gather_engine_is_tma() {
   static const bool tma = [] {
     const char* e = std::getenv("QSA_GATHER");
-    return e != nullptr && std::strcmp(e, "tma") == 0;
+    return e == nullptr || std::strcmp(e, "cpasync") != 0;
   }();
   return tma;
 }

@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "qsa.h"   // include/ is on the compiler include path
@@ -91,6 +92,9 @@ __host__ __device__ inline SmemLayout smem_layout(int np, int stages, int slot_c
 }
 
 // Host launchers (prefill.cu / union.cu).  Return cudaSuccess or the launch error.
+// TMA map over a KV cache viewed as [rows, 256] bf16 (row = slot x kv_heads + kv_head),
+// box 64 x 1 with 128-byte swizzle: the gather4 source of the attention kernel and the probe.
+cudaError_t make_cache_map(CUtensorMap* m, const void* cache, int64_t rows);
 cudaError_t launch_prefill(const PrefillParams& p, const Geometry& g, const void* k_cache,
                            const void* v_cache, int64_t tmap_rows, cudaStream_t stream);
 cudaError_t launch_union_build(const int32_t* indices, const int32_t* topk_len, int64_t n_rows,

@@ -760,6 +760,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
+}  // namespace
+
 // 2-D map over a KV cache viewed as [rows = slots x kv_heads, 256] bf16, box 64 x 1, SW128.
 cudaError_t make_cache_map(CUtensorMap* m, const void* cache, int64_t rows) {
   auto enc = tensor_map_encoder();
@@ -774,6 +776,8 @@ cudaError_t make_cache_map(CUtensorMap* m, const void* cache, int64_t rows) {
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
+
+namespace {
 
 template <int NP, bool UNION>
 cudaError_t launch_np(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,

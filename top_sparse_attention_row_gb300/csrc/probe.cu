@@ -1,8 +1,9 @@
 // Gather-ceiling probe: how fast can one GB300 SM pull random half-rows (256 B) of a KV cache
-// from L2 into shared memory, with nothing else running?  It uses the same engine and shapes as
-// the attention kernel's producers -- cp.async 16-byte copies, 32 KiB pieces of 128 rows x 256 B,
-// 128-byte swizzled destinations, a 6-stage ring -- but the consumer only releases each stage,
-// so the result bounds what the gather side of the kernel can approach.
+// from L2 into shared memory, with nothing else running?  It uses the same engines and shapes as
+// the attention kernel's producers -- TMA tile::gather4 (4 rows x 128 B per op) or cp.async
+// 16-byte copies, 32 KiB pieces of 128 rows x 256 B, 128-byte swizzled destinations, a 6-stage
+// ring -- but the consumer only releases each stage, so the result bounds what the gather side
+// of the kernel can approach.
 //
 // Each of the six producer warps owns one stage of the ring and gathers every piece that lands
 // on it, so no two warps ever wait on different phases of one stage.
@@ -36,8 +37,9 @@ __device__ bool probe_wait(uint32_t bar, uint32_t parity, volatile int* abort_fl
 }
 
 __global__ void __launch_bounds__(32 * kProbeWarps, 1)
-    gather_probe_kernel(const uint8_t* __restrict__ cache, const int32_t* __restrict__ rows,
-                        int64_t n_table_pieces, int32_t pieces_per_cta, int* status) {
+    gather_probe_kernel(const __grid_constant__ CUtensorMap tm, const uint8_t* __restrict__ cache,
+                        const int32_t* __restrict__ rows, int64_t n_table_pieces,
+                        int32_t pieces_per_cta, int use_tma, int* status) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -47,7 +49,7 @@ __global__ void __launch_bounds__(32 * kProbeWarps, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kProbeStages; ++s) {
-      mbar_init(full + 8 * s, 32);
+      mbar_init(full + 8 * s, use_tma ? 1 : 32);
       mbar_init(empty + 8 * s, 1);
     }
     abort_flag = 0;
@@ -57,11 +59,23 @@ __global__ void __launch_bounds__(32 * kProbeWarps, 1)
   volatile int* ab = &abort_flag;
   if (warp < kProbeStages) {
     const int st = warp;
+    int last = -1;   // newest piece this warp issued
     for (int p = st; p < pieces_per_cta; p += kProbeStages) {
       const uint32_t par = ((p / kProbeStages) & 1) ^ 1;
       if (!__all_sync(0xffffffffu, probe_wait(empty + 8 * st, par, ab, status))) break;
       const int32_t* prow = rows + ((blockIdx.x * 131 + p) % n_table_pieces) * kTileTokens;
       const uint32_t dst = base + st * kStageBytes;
+      if (use_tma) {
+        // lane: rows 4*lane .. 4*lane+3, two gather4 ops (dims 0-63 and 64-127)
+        const int4 y = *reinterpret_cast<const int4*>(prow + 4 * lane);
+        if (lane == 0) mbar_arrive_expect_tx(full + 8 * st, kStageBytes);
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          tma_gather4(dst + c * 16384 + lane * 512, &tm, c * 64, y.x, y.y, y.z, y.w, full + 8 * st);
+        last = p;
+        continue;
+      }
       const int ch = lane & 15;
 #pragma unroll 8
       for (int i = 0; i < 64; ++i) {
@@ -73,7 +87,16 @@ __global__ void __launch_bounds__(32 * kProbeWarps, 1)
       asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(full + 8 * st)
                    : "memory");
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
+    if (!use_tma) {
+      asm volatile("cp.async.wait_all;" ::: "memory");
+    } else if (*ab && last >= 0 && lane == 0) {
+      // after an abort the consumer may not have waited for this stage: let the newest copy
+      // land (bounded) before the block exits
+      const unsigned long long t0 = probe_ns();
+      while (!mbar_try_wait(full + 8 * st, (last / kProbeStages) & 1) &&
+             probe_ns() - t0 < 1000000000ull) {
+      }
+    }
   } else {
     for (int p = 0; p < pieces_per_cta; ++p) {
       const int st = p % kProbeStages;
@@ -91,15 +114,18 @@ __global__ void __launch_bounds__(32 * kProbeWarps, 1)
 
 extern "C" qsa_status qsa_probe_gather_ceiling(const void* cache, int64_t n_rows,
                                                const int32_t* rows, int64_t n_table_pieces,
-                                               int32_t pieces_per_cta, float* ms_out,
-                                               void* stream_v) {
-  if (!cache || !rows || !ms_out || n_rows <= 0 || n_table_pieces <= 0 || pieces_per_cta <= 0)
+                                               int32_t pieces_per_cta, int32_t engine,
+                                               float* ms_out, void* stream_v) {
+  if (!cache || !rows || !ms_out || n_rows <= 0 || n_table_pieces <= 0 || pieces_per_cta <= 0 ||
+      (engine != 0 && engine != 1) || (reinterpret_cast<uintptr_t>(cache) & 15u) != 0)
     return QSA_ERR_INVALID_ARG;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return QSA_ERR_CUDA;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  CUtensorMap tm;
+  if (qsa::make_cache_map(&tm, cache, n_rows) != cudaSuccess) return QSA_ERR_CUDA;
   const int smem = qsa::kProbeStages * qsa::kStageBytes + 16 * qsa::kProbeStages + 1024;
   if (cudaFuncSetAttribute(qsa::gather_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            smem) != cudaSuccess)
@@ -113,7 +139,8 @@ extern "C" qsa_status qsa_probe_gather_ceiling(const void* cache, int64_t n_rows
   cudaEventCreate(&b);
   cudaEventRecord(a, stream);
   qsa::gather_probe_kernel<<<sms, 32 * qsa::kProbeWarps, smem, stream>>>(
-      static_cast<const uint8_t*>(cache), rows, n_table_pieces, pieces_per_cta, status);
+      tm, static_cast<const uint8_t*>(cache), rows, n_table_pieces, pieces_per_cta, engine,
+      status);
   cudaEventRecord(b, stream);
   int h_status = 0;
   cudaError_t e = cudaGetLastError();
