@@ -39,7 +39,8 @@ UNIT = "query-rows/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = ["top_sparse_attention_row_gb300/csrc/prefill.cu",
                   "top_sparse_attention_row_gb300/csrc/ptx.cuh",
-                  "top_sparse_attention_row_gb300/csrc/internal.h"]
+                  "top_sparse_attention_row_gb300/csrc/internal.h",
+                  "top_sparse_attention_row_gb300/csrc/paged.cuh"]
 
 DESCRIPTIONS = {
     "group6_32k": "group-6 prefill chunk: 8192 rows at the end of a 32768 context, 6 Q / 1 KV, "
@@ -207,11 +208,20 @@ def run_gpu(args, rank, world, local_rank):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
 
     h_q, h_k, h_v = bf(w.q).pin_memory(), bf(w.k).pin_memory(), bf(w.v).pin_memory()
-    h_idx = torch.from_numpy(w.indices).pin_memory()
+    paged = args.paged
+    if paged and "page_table" not in w.meta:
+        raise SystemExit(f"--paged needs a paged workload; {args.config} has no page table")
+    h_idx = torch.from_numpy(w.meta["logical_indices"] if paged else w.indices).pin_memory()
     h_tl = None if w.topk_len is None else torch.from_numpy(w.topk_len).pin_memory()
+    # paged calls: ragged row offsets, per-request KV lengths and the page table
+    h_meta = ()
+    if paged:
+        h_meta = tuple(torch.from_numpy(np.ascontiguousarray(w.meta[key], dtype=np.int32)).pin_memory()
+                       for key in ("cu_seqlens_q", "kv_lens_array", "page_table"))
     q, k, v = h_q.to(dev), h_k.to(dev), h_v.to(dev)
     idx = h_idx.to(dev)
     tl = None if h_tl is None else h_tl.to(dev)
+    d_meta = tuple(t.to(dev) for t in h_meta)
     out = torch.empty_like(q)
     lse = torch.empty((w.n_rows, w.n_qheads), dtype=torch.float32, device=dev)
     ws = None
@@ -222,8 +232,14 @@ def run_gpu(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
 
     def call():
-        binding.sparse_prefill(q, k, v, idx, tl, w.scale, out=out, lse=lse, union_g=args.union,
-                               workspace=ws, stream=stream)
+        if paged:
+            cu, kvl, pt = d_meta
+            binding.sparse_prefill_paged(q, k, v, idx, tl, cu, kvl, pt, w.meta["page_size"], w.scale,
+                                         n_pages=w.meta["n_pages"], out=out, lse=lse,
+                                         union_g=args.union, stream=stream)
+        else:
+            binding.sparse_prefill(q, k, v, idx, tl, w.scale, out=out, lse=lse, union_g=args.union,
+                                   workspace=ws, stream=stream)
 
     geo = binding.select_geometry(w.n_qheads, w.n_kvheads, args.union, w.topk, w.head_dim, w.n_rows)
     # gather ceiling on this workload's own K cache and selected rows (KV head 0)
@@ -269,7 +285,8 @@ def run_gpu(args, rank, world, local_rank):
     # end to end: pinned host inputs -> device, call, result -> host, every step
     e_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     e_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_idx) + ((h_tl,) if h_tl is not None else ()))
+    h2d = sum(t.numel() * t.element_size()
+              for t in (h_q, h_k, h_v, h_idx) + ((h_tl,) if h_tl is not None else ()) + h_meta)
     d2h = e_out.numel() * e_out.element_size() + e_lse.numel() * e_lse.element_size()
 
     def e2e_step():
@@ -279,6 +296,8 @@ def run_gpu(args, rank, world, local_rank):
         idx.copy_(h_idx, non_blocking=True)
         if tl is not None:
             tl.copy_(h_tl, non_blocking=True)
+        for d, h in zip(d_meta, h_meta):
+            d.copy_(h, non_blocking=True)
         call()
         e_out.copy_(out, non_blocking=True)
         e_lse.copy_(lse, non_blocking=True)
@@ -330,7 +349,7 @@ def run_gpu(args, rank, world, local_rank):
     if os.path.exists(tpath):
         with open(tpath) as f:
             tj = json.load(f)
-        key = f"{args.config}:union{args.union}"
+        key = f"{args.config}:union{args.union}" + (":paged" if paged else "")
         ent = tj.get(key)
         if ent and ent.get("kernel_sha") == kernel_sha():
             traffic = ent.get("dram_bytes_per_launch")
@@ -359,6 +378,8 @@ def run_gpu(args, rank, world, local_rank):
                    "rows": w.n_rows, "n_qheads": w.n_qheads, "n_kvheads": w.n_kvheads,
                    "head_dim": w.head_dim, "topk": w.topk, "union_g": args.union,
                    "valid_slots": stats["valid_slots"], "geometry": geo,
+                   "indices": ("logical positions + page table, translated in the kernels "
+                               "(qsa_sparse_prefill_paged)" if paged else "physical slots"),
                    "l2": "flushed before every timed step (512 MiB memset outside the events)",
                    "parallelism": f"{world} independent shard(s), no collective"},
         "roofline": roofline,
@@ -416,6 +437,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="group6_32k")
     ap.add_argument("--union", type=int, default=0)
+    ap.add_argument("--paged", action="store_true",
+                    help="paged workloads: pass logical positions and the page table "
+                         "(qsa_sparse_prefill_paged) instead of translated slots")
     ap.add_argument("--cpu-rows", type=int, default=8192)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -110,6 +110,41 @@ qsa_status qsa_sparse_prefill_ex(const void* q, const void* k_cache, const void*
                                  void* workspace, size_t workspace_bytes,
                                  const qsa_geometry* forced, void* stream);
 
+/* Paged entry: the indexer's slots are LOGICAL positions inside each row's request, and the
+ * library translates them through the request's page table in the kernels (no translated index
+ * tensor is written).  The pages route a batch's top-k indices through a PAGED or a RAGGED
+ * transform chosen per batch kind, key the valid length on the cache sequence lengths, and serve
+ * with paged KV caches of 64 or 128 slots per page ("DSA prefill ... triton_sparse_mla",
+ * Modifications: Robustness, and the review follow-up on MIXED batches; "[QSA] Tune sm120 sparse
+ * prefill geometry", serving command --page-size 128).
+ *   k_cache, v_cache [n_pages * page_size, n_kvheads, head_dim] bf16: physical page p holds slots
+ *               p*page_size .. p*page_size + page_size - 1 (the layout of qsa_sparse_prefill).
+ *   indices     [n_rows, topk] int32 logical positions in the row's request, < 0 = padding.
+ *   cu_seqlens_q [n_requests + 1] int32: rows of request i are cu_seqlens_q[i] .. [i+1] - 1;
+ *               non-decreasing, [0] = 0, [n_requests] = n_rows (not checked: the device data is
+ *               not read on the host).
+ *   kv_lens     [n_requests] int32 logical KV length of each request, nullable; a position at or
+ *               past it is padding.
+ *   page_table  [n_requests, pages_per_req] int32 physical page of each logical page, < 0 = none.
+ *   n_pages     physical pages in the caches; > 0 = pages >= n_pages are padding (gathers are
+ *               bounds-checked), 0 = unchecked.
+ * Position x of request i reads physical slot page_table[i][x / page_size] * page_size +
+ * x % page_size.  It is padding when x < 0, x >= kv_lens[i], x / page_size >= pages_per_req, or
+ * the page is < 0 or >= n_pages.  Everything else (topk_len, union_g, lse, errors, streams)
+ * is as for qsa_sparse_prefill; with union_g > 1 the groups are union_g consecutive rows and
+ * may span requests (the union is built over physical slots).
+ * Errors: QSA_ERR_INVALID_ARG for a null cu_seqlens_q or page_table, n_requests < 1,
+ * pages_per_req < 1, page_size < 1 or n_pages < 0; QSA_ERR_UNSUPPORTED when
+ * n_pages * page_size * n_kvheads >= 2^31. */
+qsa_status qsa_sparse_prefill_paged(const void* q, const void* k_cache, const void* v_cache,
+                                    const int32_t* indices, const int32_t* topk_len,
+                                    const int32_t* cu_seqlens_q, const int32_t* kv_lens,
+                                    const int32_t* page_table, void* out, float* lse,
+                                    int64_t n_rows, int32_t n_requests, int32_t pages_per_req,
+                                    int32_t page_size, int64_t n_pages, int32_t n_qheads,
+                                    int32_t n_kvheads, int32_t head_dim, int32_t topk, float scale,
+                                    int32_t union_g, void* stream);
+
 /* Allocation-free variant of qsa_sparse_prefill (same arguments, same results).  The pages
  * have no counterpart: it exists for callers that must not allocate device memory -- code
  * whose GPU memory is owned entirely by a framework's pool, latency-critical loops where an

@@ -27,6 +27,11 @@ Functions and the passages they follow:
 * ``union.union_attention`` -- attention of each token of a group over the
   union list restricted to its own ownership bit (same page: the bitmask
   restores each token's own softmax support, identical to per-token).
+* ``paged.sparse_prefill_paged`` -- the same attention when each row's slots
+  are logical positions of its request, read through a page table with
+  ragged request metadata ("DSA prefill ... triton_sparse_mla", Robustness:
+  PAGED / RAGGED index transforms, valid length from the cache sequence
+  lengths; "[QSA] Tune sm120 sparse prefill geometry": paged serving cache).
 
 Every function is pinned by ``tests/test_oracle_pins.py`` against facts that
 do not come from this package: dense causal attention from a library routine
@@ -36,3 +41,5 @@ arithmetic for the union.
 """
 from .attention import sparse_prefill, sparse_prefill_rows, valid_slots  # noqa: F401
 from .union import sorted_rows, union_build, union_attention  # noqa: F401
+from .paged import (sparse_prefill_paged, sparse_prefill_paged_rows,  # noqa: F401
+                    physical_indices, request_of_rows)

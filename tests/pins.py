@@ -363,3 +363,111 @@ def check_union_attention(build, attend_union, per_token):
         if not (_close(O1, O2, 1e-12) and _close(L1, L2, 1e-12)):
             fails.append(f"union attention != per-token (G={G})")
     return fails
+
+
+# ----------------------------------------------------------------------------- paged
+
+def paged_case(seed, with_kv_lens=True, bad_page=False):
+    """Requests with contiguous per-request K/V, scattered page by page into a shuffled paged
+    cache by slicing (no per-position arithmetic).  Returns the paged call's arguments and the
+    per-request contiguous arrays that give the expected result."""
+    rng = _rng(seed)
+    ps, Hq, Hkv, D, K = 8, 4, 2, 8, 24
+    rows_per_req = [3, 0, 4, 2]                 # request 1 is empty: cu_seqlens repeats
+    full_pages = [5, 1, 7, 2]                   # pages holding data
+    kv_lens = [37, 5, 50, 16]                   # <= full_pages * ps
+    pages_per_req = max(full_pages) + 1         # trailing columns of the table are -1
+    spare = 3                                   # physical pages after the mapped ones, junk
+    mapped = sum(full_pages)
+    perm = rng.permutation(mapped)
+    kc = np.zeros(((mapped + spare) * ps, Hkv, D))
+    vc = np.zeros(((mapped + spare) * ps, Hkv, D))
+    kc[:] = rng.standard_normal(kc.shape)       # spare pages hold junk
+    vc[:] = rng.standard_normal(vc.shape)
+    table = np.full((len(full_pages), pages_per_req), -1, dtype=np.int64)
+    contig_k, contig_v, off = [], [], 0
+    for i, m in enumerate(full_pages):
+        ki = rng.standard_normal((m * ps, Hkv, D))
+        vi = rng.standard_normal((m * ps, Hkv, D))
+        for pg in range(m):
+            pid = int(perm[off + pg])
+            table[i, pg] = pid
+            kc[pid * ps:(pid + 1) * ps] = ki[pg * ps:(pg + 1) * ps]
+            vc[pid * ps:(pid + 1) * ps] = vi[pg * ps:(pg + 1) * ps]
+        off += m
+        contig_k.append(ki)
+        contig_v.append(vi)
+    R = sum(rows_per_req)
+    cu = np.concatenate([[0], np.cumsum(rows_per_req)]).astype(np.int64)
+    q = rng.standard_normal((R, Hq, D))
+    idx = np.full((R, K), -1, dtype=np.int64)
+    req_rows = []
+    r = 0
+    for i, n in enumerate(rows_per_req):
+        for _ in range(n):
+            hi = pages_per_req * ps + 3           # some positions past every limit
+            idx[r] = rng.integers(-2, hi, size=K)
+            req_rows.append(i)
+            r += 1
+    tl = rng.integers(K // 2, K + 1, size=R)
+    # The call declares only the mapped pages (n_pages = mapped); a table entry naming a spare
+    # page (present in memory, holding junk) is then out of range and its positions are padding.
+    n_pages = mapped + spare
+    if bad_page:
+        n_pages = mapped
+        table[2, 3] = mapped + 1
+    return dict(q=q, kc=kc, vc=vc, idx=idx, tl=tl, cu=cu,
+                kv_lens=np.array(kv_lens) if with_kv_lens else None, table=table, ps=ps,
+                n_pages=n_pages, contig_k=contig_k, contig_v=contig_v, req_rows=req_rows,
+                full_pages=full_pages, kv_lens_list=kv_lens, bad_page=bad_page)
+
+
+def paged_expected(c, scale):
+    """Per row: the plain oracle over the request's contiguous K/V with logical positions as
+    slots and the request's valid length as the slot count."""
+    from oracle import sparse_prefill_rows
+    R, Hq, D = c["q"].shape
+    O = np.zeros((R, Hq, D))
+    L = np.full((R, Hq), -np.inf)
+    for r, i in enumerate(c["req_rows"]):
+        n_valid = c["kv_lens_list"][i] if c["kv_lens"] is not None else c["full_pages"][i] * c["ps"]
+        row = c["idx"][r].copy()
+        if c["bad_page"] and i == 2:
+            row[(row >= 0) & (row // c["ps"] == 3)] = -1
+        Or, Lr = sparse_prefill_rows(c["q"][r:r + 1], c["contig_k"][i], c["contig_v"][i],
+                                     row[None, :], c["tl"][r:r + 1], scale, [0], n_valid)
+        O[r], L[r] = Or[0], Lr[0]
+    return O, L
+
+
+def check_paged_vs_contiguous(fn):
+    fails = []
+    for seed, (kvl, bad) in enumerate([(True, False), (False, False), (True, True)]):
+        c = paged_case(300 + seed, with_kv_lens=kvl, bad_page=bad)
+        try:
+            O, L = fn(c["q"], c["kc"], c["vc"], c["idx"], c["tl"], c["cu"], c["kv_lens"],
+                      c["table"], c["ps"], 0.41, c["n_pages"])
+        except Exception as e:          # a translation that leaves the cache fails the pin
+            fails.append(f"paged call raised {type(e).__name__} (kv_lens={kvl}, bad page={bad})")
+            continue
+        Oe, Le = paged_expected(c, 0.41)
+        if not (_close(O, Oe, 1e-12) and _close(L, Le, 1e-12)):
+            fails.append(f"paged != contiguous per request (kv_lens={kvl}, bad page={bad})")
+    return fails
+
+
+def check_paged_identity(fn):
+    """page_size 1, one request, identity table: the indices are the physical slots."""
+    from oracle import sparse_prefill
+    rng = _rng(310)
+    S, R, Hq, Hkv, D, K = 30, 7, 4, 1, 8, 12
+    q = rng.standard_normal((R, Hq, D))
+    k = rng.standard_normal((S, Hkv, D))
+    v = rng.standard_normal((S, Hkv, D))
+    idx = rng.integers(-1, S, size=(R, K))
+    O, L = fn(q, k, v, idx, None, np.array([0, R]), None, np.arange(S)[None, :], 1, 0.3, 0)
+    Oe, Le = sparse_prefill(q, k, v, idx, None, 0.3)
+    return [] if (_close(O, Oe, 1e-12) and _close(L, Le, 1e-12)) else ["identity paging"]
+
+
+PAGED_CHECKS = [check_paged_vs_contiguous, check_paged_identity]

@@ -99,6 +99,17 @@ def test_entry_validation_before_any_cuda_call(lib):
     assert ub(None, None, 10, 16, 2, 0, None, fake, fake, fake, None) == 1
     assert ub(fake, None, 10, 16, 0, 0, None, fake, fake, fake, None) == 1
     assert ub(fake, None, 10, 1 << 16, 8, 0, None, fake, fake, fake, None) == 2
+    pg = lib.qsa_sparse_prefill_paged
+    #        q     k     v     idx   tl    cu    kvl   table out   lse   R   nreq ppr ps npages hq hkv d  topk scale  G
+    assert pg(fake, fake, fake, fake, None, None, None, fake, fake, None, 10, 2, 4, 64, 0, 6, 1, 256, 64, 0.0625, 0, None) == 1
+    assert pg(fake, fake, fake, fake, None, fake, None, None, fake, None, 10, 2, 4, 64, 0, 6, 1, 256, 64, 0.0625, 0, None) == 1
+    assert pg(fake, fake, fake, fake, None, fake, None, fake, fake, None, 10, 0, 4, 64, 0, 6, 1, 256, 64, 0.0625, 0, None) == 1
+    assert pg(fake, fake, fake, fake, None, fake, None, fake, fake, None, 10, 2, 0, 64, 0, 6, 1, 256, 64, 0.0625, 0, None) == 1
+    assert pg(fake, fake, fake, fake, None, fake, None, fake, fake, None, 10, 2, 4, 0, 0, 6, 1, 256, 64, 0.0625, 0, None) == 1
+    assert pg(fake, fake, fake, fake, None, fake, None, fake, fake, None, 10, 2, 4, 64, -1, 6, 1, 256, 64, 0.0625, 0, None) == 1
+    assert pg(fake, fake, fake, fake, None, fake, None, fake, fake, None, 10, 2, 4, 64, 1 << 26, 6, 1, 256, 64, 0.0625, 0, None) == 2
+    assert pg(fake, fake, fake, fake, None, fake, None, fake, fake, None, 10, 2, 4, 64, 0, 6, 1, 128, 64, 0.0625, 0, None) == 2
+    assert pg(fake, fake, fake, fake, None, fake, None, fake, fake, None, 0, 2, 4, 64, 0, 6, 1, 256, 64, 0.0625, 0, None) == 0
     pr = lib.qsa_probe_gather_ceiling
     ms = ctypes.c_float(0.0)
     assert pr(fake, 1000, fake, 4, 10, 2, ctypes.byref(ms), None) == 1      # unknown engine

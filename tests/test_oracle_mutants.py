@@ -95,3 +95,50 @@ def _union_mutant(kind):
 @pytest.mark.parametrize("kind", ["no_self_bit", "keeps_minus_one", "descending_order"])
 def test_union_mutant_is_caught(kind):
     assert pins.check_union_bruteforce(_union_mutant(kind))
+
+
+def _paged_mutant(kind):
+    """A copy of the paged oracle's translation with one planted mistake."""
+    from oracle.attention import sparse_prefill_rows
+
+    def translate(indices, cu, kv_lens, table, ps, n_pages):
+        idx = np.asarray(indices, dtype=np.int64)
+        table = np.asarray(table, dtype=np.int64)
+        cu = np.asarray(cu, dtype=np.int64)
+        out = np.full(idx.shape, -1, dtype=np.int64)
+        for r in range(idx.shape[0]):
+            cands = [i for i in range(len(cu) - 1) if cu[i] <= r]
+            i = cands[0] if kind == "first_request_not_last" else cands[-1]
+            if kind == "next_request" and i + 1 < len(cu) - 1:
+                i += 1
+            for j, x in enumerate(idx[r]):
+                if x < 0:
+                    continue
+                if kv_lens is not None and kind != "kv_lens_ignored" and x >= kv_lens[i]:
+                    continue
+                page = x // ps
+                if page >= table.shape[1]:
+                    continue
+                pid = table[i, page]
+                if pid < 0 or (n_pages > 0 and pid >= n_pages and kind != "n_pages_ignored"):
+                    continue
+                off = (x // ps) % ps if kind == "offset_from_page" else x % ps
+                out[r, j] = pid * ps + off
+        return out
+
+    def fn(q, kc, vc, indices, topk_len, cu, kv_lens, table, ps, scale, n_pages=0):
+        phys = translate(indices, cu, kv_lens, table, ps, n_pages)
+        return sparse_prefill_rows(q, kc, vc, phys, topk_len, scale, np.arange(q.shape[0]))
+    return fn
+
+
+def test_paged_unmutated_copy_passes():
+    fn = _paged_mutant("none")
+    assert [f for c in pins.PAGED_CHECKS for f in c(fn)] == []
+
+
+@pytest.mark.parametrize("kind", ["first_request_not_last", "next_request", "kv_lens_ignored",
+                                  "n_pages_ignored", "offset_from_page"])
+def test_paged_mutant_is_caught(kind):
+    fn = _paged_mutant(kind)
+    assert [f for c in pins.PAGED_CHECKS for f in c(fn)], f"mutant {kind} passed every pin"

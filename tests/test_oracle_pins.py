@@ -63,3 +63,8 @@ def test_sorted_rows_vs_python_sorted():
         want = sorted(int(x) for x in idx[r, :L] if x >= 0)
         assert srt[r, :len(want)].tolist() == want
         assert np.all(srt[r, len(want):] == -1)
+
+
+@pytest.mark.parametrize("check", pins.PAGED_CHECKS, ids=lambda c: c.__name__)
+def test_paged_pin(check):
+    assert check(oracle.sparse_prefill_paged) == []

@@ -22,7 +22,8 @@ STATUS_NAMES = {0: "QSA_OK", 1: "QSA_ERR_INVALID_ARG", 2: "QSA_ERR_UNSUPPORTED",
 EXPORTED = ["qsa_sparse_prefill", "qsa_sparse_prefill_ex", "qsa_workspace_bytes",
             "qsa_union_build", "qsa_select_geometry", "qsa_get_counters", "qsa_reset_counters",
             "qsa_status_string", "qsa_version", "qsa_get_device_status",
-            "qsa_sparse_prefill_noalloc", "qsa_probe_gather_ceiling"]
+            "qsa_sparse_prefill_noalloc", "qsa_probe_gather_ceiling",
+            "qsa_sparse_prefill_paged"]
 
 # Size of the library-owned scratch array used by qsa_sparse_prefill_noalloc (include/qsa.h).
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -70,6 +71,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qsa_sparse_prefill_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, f32,
                                                i32, vp]
     lib.qsa_sparse_prefill_noalloc.restype = ctypes.c_int
+    lib.qsa_sparse_prefill_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, i32,
+                                             i32, i64, i32, i32, i32, i32, f32, i32, vp]
+    lib.qsa_sparse_prefill_paged.restype = ctypes.c_int
     lib.qsa_probe_gather_ceiling.argtypes = [vp, i64, vp, i64, i32, i32, ctypes.POINTER(f32), vp]
     lib.qsa_probe_gather_ceiling.restype = ctypes.c_int
     lib.qsa_workspace_bytes.argtypes = [i64, i32, i32]
@@ -168,6 +172,46 @@ def sparse_prefill(q, k_cache, v_cache, indices, topk_len, scale: float, *, out=
                                     _ptr(topk_len), _ptr(out), _ptr(lse), R, Hq, Hkv, D, topk,
                                     float(scale), int(union_g), s)
     _check(st, "qsa_sparse_prefill")
+    return out, lse
+
+
+def sparse_prefill_paged(q, k_cache, v_cache, indices, topk_len, cu_seqlens_q, kv_lens, page_table,
+                         page_size: int, scale: float, *, n_pages: int = 0, out=None, lse=None,
+                         union_g: int = 0, want_lse: bool = True, stream=None):
+    """Paged call (qsa_sparse_prefill_paged): indices [R, topk] int32 are logical positions in
+    each row's request; cu_seqlens_q [n_requests + 1] int32 row offsets; kv_lens [n_requests]
+    int32 or None; page_table [n_requests, pages_per_req] int32; k_cache / v_cache
+    [n_pages * page_size, Hkv, D] bf16.  The translation to physical slots runs in the kernels."""
+    import torch
+    lib = load_library()
+    _require(q, torch.bfloat16, "q", 3)
+    _require(k_cache, torch.bfloat16, "k_cache", 3)
+    _require(v_cache, torch.bfloat16, "v_cache", 3)
+    _require(indices, torch.int32, "indices", 2)
+    _require(topk_len, torch.int32, "topk_len", 1)
+    _require(cu_seqlens_q, torch.int32, "cu_seqlens_q", 1)
+    _require(kv_lens, torch.int32, "kv_lens", 1)
+    _require(page_table, torch.int32, "page_table", 2)
+    R, Hq, D = q.shape
+    Hkv = k_cache.shape[1]
+    topk = indices.shape[1]
+    n_req = page_table.shape[0]
+    if indices.shape[0] != R or (topk_len is not None and topk_len.shape[0] != R):
+        raise ValueError("indices / topk_len rows must match q")
+    if cu_seqlens_q.shape[0] != n_req + 1 or (kv_lens is not None and kv_lens.shape[0] != n_req):
+        raise ValueError("cu_seqlens_q / kv_lens must match the page table's requests")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((R, Hq), dtype=torch.float32, device=q.device)
+    _require(out, torch.bfloat16, "out", 3)
+    _require(lse, torch.float32, "lse", 2)
+    st = lib.qsa_sparse_prefill_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(indices),
+                                      _ptr(topk_len), _ptr(cu_seqlens_q), _ptr(kv_lens),
+                                      _ptr(page_table), _ptr(out), _ptr(lse), R, n_req,
+                                      page_table.shape[1], int(page_size), int(n_pages), Hq, Hkv,
+                                      D, topk, float(scale), int(union_g), _stream_ptr(stream))
+    _check(st, "qsa_sparse_prefill_paged")
     return out, lse
 
 

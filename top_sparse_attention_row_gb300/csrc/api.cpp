@@ -167,7 +167,7 @@ qsa_status run(const void* q, const void* k_cache, const void* v_cache, const in
                const int32_t* topk_len, void* out, float* lse, int64_t n_rows, int32_t n_qheads,
                int32_t n_kvheads, int32_t head_dim, int32_t topk, float scale, int32_t union_g,
                int64_t n_kv_slots, void* workspace, size_t workspace_bytes,
-               const qsa_geometry* forced, void* stream_v) {
+               const qsa_geometry* forced, const qsa::PagedAddr* paged, void* stream_v) {
   if (!q || !k_cache || !v_cache || !indices || !out) return QSA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
     return QSA_ERR_INVALID_ARG;
@@ -215,6 +215,7 @@ qsa_status run(const void* q, const void* k_cache, const void* v_cache, const in
   p.scale_log2 = scale * 1.4426950408889634f;
   const int64_t tmap_rows = n_kv_slots > 0 ? n_kv_slots * n_kvheads : static_cast<int64_t>(INT32_MAX);
   p.pad_row = static_cast<int32_t>(tmap_rows);
+  if (paged) p.pa = *paged;
 
   void* ws = nullptr;
   bool own_ws = false;
@@ -235,7 +236,8 @@ qsa_status run(const void* q, const void* k_cache, const void* v_cache, const in
     cudaError_t e = qsa::launch_union_build(indices, topk_len, n_rows, topk, g.union_g, n_kv_slots,
                                             nullptr, const_cast<int32_t*>(p.union_idx),
                                             const_cast<uint8_t*>(p.union_bits),
-                                            const_cast<int32_t*>(p.union_len), false, stream);
+                                            const_cast<int32_t*>(p.union_len), false, paged,
+                                            stream);
     if (e != cudaSuccess) {
       if (own_ws) cudaFreeAsync(ws, stream);
       return QSA_ERR_CUDA;
@@ -261,7 +263,38 @@ qsa_status qsa_sparse_prefill(const void* q, const void* k_cache, const void* v_
                               int64_t n_rows, int32_t n_qheads, int32_t n_kvheads, int32_t head_dim,
                               int32_t topk, float scale, int32_t union_g, void* stream) {
   return run(q, k_cache, v_cache, indices, topk_len, out, lse, n_rows, n_qheads, n_kvheads,
-             head_dim, topk, scale, union_g, 0, nullptr, 0, nullptr, stream);
+             head_dim, topk, scale, union_g, 0, nullptr, 0, nullptr, nullptr, stream);
+}
+
+qsa_status qsa_sparse_prefill_paged(const void* q, const void* k_cache, const void* v_cache,
+                                    const int32_t* indices, const int32_t* topk_len,
+                                    const int32_t* cu_seqlens_q, const int32_t* kv_lens,
+                                    const int32_t* page_table, void* out, float* lse,
+                                    int64_t n_rows, int32_t n_requests, int32_t pages_per_req,
+                                    int32_t page_size, int64_t n_pages, int32_t n_qheads,
+                                    int32_t n_kvheads, int32_t head_dim, int32_t topk, float scale,
+                                    int32_t union_g, void* stream) {
+  if (!cu_seqlens_q || !page_table) return QSA_ERR_INVALID_ARG;
+  if (n_requests < 1 || pages_per_req < 1 || page_size < 1 || n_pages < 0)
+    return QSA_ERR_INVALID_ARG;
+  int64_t n_kv_slots = 0;
+  if (n_pages > 0) {
+    n_kv_slots = n_pages * page_size;
+    if (n_kvheads > 0 && n_kv_slots * n_kvheads >= INT32_MAX) return QSA_ERR_UNSUPPORTED;
+  }
+  qsa::PagedAddr pa{};
+  pa.page_table = page_table;
+  pa.cu_seqlens_q = cu_seqlens_q;
+  pa.kv_lens = kv_lens;
+  pa.n_requests = n_requests;
+  pa.pages_per_req = pages_per_req;
+  pa.page_size = page_size;
+  pa.page_shift = -1;
+  for (int s = 0; s < 31; ++s)
+    if ((int32_t{1} << s) == page_size) pa.page_shift = s;
+  pa.n_pages = n_pages;
+  return run(q, k_cache, v_cache, indices, topk_len, out, lse, n_rows, n_qheads, n_kvheads,
+             head_dim, topk, scale, union_g, n_kv_slots, nullptr, 0, nullptr, &pa, stream);
 }
 
 qsa_status qsa_sparse_prefill_ex(const void* q, const void* k_cache, const void* v_cache,
@@ -271,7 +304,8 @@ qsa_status qsa_sparse_prefill_ex(const void* q, const void* k_cache, const void*
                                  int64_t n_kv_slots, void* workspace, size_t workspace_bytes,
                                  const qsa_geometry* forced, void* stream) {
   return run(q, k_cache, v_cache, indices, topk_len, out, lse, n_rows, n_qheads, n_kvheads,
-             head_dim, topk, scale, union_g, n_kv_slots, workspace, workspace_bytes, forced, stream);
+             head_dim, topk, scale, union_g, n_kv_slots, workspace, workspace_bytes, forced, nullptr,
+             stream);
 }
 
 size_t qsa_workspace_bytes(int64_t n_rows, int32_t topk, int32_t union_g) {
@@ -295,7 +329,7 @@ qsa_status qsa_union_build(const int32_t* indices, const int32_t* topk_len, int6
   if (st != QSA_OK) return st;
   cudaError_t e = qsa::launch_union_build(indices, topk_len, n_rows, topk, union_g, n_kv_slots,
                                           sorted_out, union_idx, union_bits, union_len, true,
-                                          static_cast<cudaStream_t>(stream));
+                                          nullptr, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return QSA_ERR_CUDA;
   g_launches.fetch_add(1);
   return QSA_OK;

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstddef>
+#include <climits>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -24,6 +25,19 @@ constexpr int kMinStages = 4;                // ring must hold V(j) and K(j+1) t
 constexpr int kMaxStages = 8;
 constexpr int kSmemLimit = 232448;           // 227 KiB opt-in dynamic shared memory
 constexpr int kUnionMaxSmem = 200 * 1024;    // union-build kernel shared-memory cap
+
+// In-kernel paged addressing: rows carry logical per-request positions, translated to physical
+// cache slots through a page table.  page_table == nullptr = the indices are physical slots.
+struct PagedAddr {
+  const int32_t* page_table;    // [n_requests, pages_per_req] physical page ids (< 0 = none)
+  const int32_t* cu_seqlens_q;  // [n_requests + 1] first row of each request, then n_rows
+  const int32_t* kv_lens;       // [n_requests] logical KV length (nullable = pages_per_req pages)
+  int32_t n_requests;
+  int32_t pages_per_req;        // row stride of page_table
+  int32_t page_size;
+  int32_t page_shift;           // log2(page_size) when a power of two, else -1
+  int64_t n_pages;              // physical pages in the cache (0 = unchecked)
+};
 
 // Everything the attention kernel needs besides the two tensor maps.
 struct PrefillParams {
@@ -51,6 +65,7 @@ struct PrefillParams {
   const uint8_t* k_bytes;       // caches as bytes, for the cp.async gather
   const uint8_t* v_bytes;
   float scale_log2;             // scale * log2(e)
+  PagedAddr pa;                 // per-token mode: page_table != nullptr = logical indices
 };
 
 struct Geometry {
@@ -100,7 +115,8 @@ cudaError_t launch_prefill(const PrefillParams& p, const Geometry& g, const void
 cudaError_t launch_union_build(const int32_t* indices, const int32_t* topk_len, int64_t n_rows,
                                int32_t topk, int32_t union_g, int64_t n_kv_slots,
                                int32_t* sorted_out, int32_t* union_idx, uint8_t* union_bits,
-                               int32_t* union_len, bool pad_outputs, cudaStream_t stream);
+                               int32_t* union_len, bool pad_outputs, const PagedAddr* paged,
+                               cudaStream_t stream);
 size_t union_build_smem_bytes(int32_t topk, int32_t union_g);   // hot-path (bitmap) kernel
 size_t union_sort_smem_bytes(int32_t topk, int32_t union_g);    // sorted-rows (bitonic) kernel
 cudaError_t read_and_clear_device_status(cudaStream_t stream, int32_t* status);

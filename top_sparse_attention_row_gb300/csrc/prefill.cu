@@ -42,6 +42,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "paged.cuh"
 #include "ptx.cuh"
 
 namespace qsa {
@@ -270,16 +271,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         cp_async_commit_wait_all();
         __syncwarp();
         int32_t n = 0;
-        for (int j0 = 0; j0 < Lr; j0 += 32) {
-          const int j = j0 + lane;
-          const int32_t x = j < Lr ? sl[j] : -1;
-          bool valid = x >= 0 && (p.n_kv_slots == 0 || x < p.n_kv_slots);
-          const int64_t y = static_cast<int64_t>(x) * p.n_kvheads + kvh;
-          valid = valid && y < static_cast<int64_t>(p.pad_row);
-          const uint32_t m = __ballot_sync(0xffffffffu, valid);
-          if (valid) sl[n + __popc(m & ((1u << lane) - 1u))] = static_cast<int32_t>(y);
-          n += __popc(m);
-          __syncwarp();
+        if (p.pa.page_table == nullptr) {
+          for (int j0 = 0; j0 < Lr; j0 += 32) {
+            const int j = j0 + lane;
+            const int32_t x = j < Lr ? sl[j] : -1;
+            bool valid = x >= 0 && (p.n_kv_slots == 0 || x < p.n_kv_slots);
+            const int64_t y = static_cast<int64_t>(x) * p.n_kvheads + kvh;
+            valid = valid && y < static_cast<int64_t>(p.pad_row);
+            const uint32_t m = __ballot_sync(0xffffffffu, valid);
+            if (valid) sl[n + __popc(m & ((1u << lane) - 1u))] = static_cast<int32_t>(y);
+            n += __popc(m);
+            __syncwarp();
+          }
+        } else {
+          // Logical positions of the row's request -> physical slots through the page table.
+          // Eight page-table loads per lane are in flight at once; every lane has read its
+          // positions of a 256-slot block before the first ballot, so compacting in place
+          // never overwrites an unread entry.
+          const int32_t req = paged_request_of_row(p.pa, row0, lane);
+          const int32_t kvl = paged_kv_len(p.pa, req);
+          for (int j0 = 0; j0 < Lr; j0 += 256) {
+            int64_t ps[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int j = j0 + 32 * u + lane;
+              ps[u] = paged_slot(p.pa, req, kvl, j < Lr ? sl[j] : -1);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int64_t x = ps[u];
+              bool valid = x >= 0 && (p.n_kv_slots == 0 || x < p.n_kv_slots);
+              const int64_t y = x * p.n_kvheads + kvh;
+              valid = valid && y < static_cast<int64_t>(p.pad_row);
+              const uint32_t m = __ballot_sync(0xffffffffu, valid);
+              if (valid) sl[n + __popc(m & ((1u << lane) - 1u))] = static_cast<int32_t>(y);
+              n += __popc(m);
+            }
+            __syncwarp();
+          }
         }
         nv = n;
       } else {

@@ -22,6 +22,7 @@
 #include <climits>
 
 #include "internal.h"
+#include "paged.cuh"
 
 namespace qsa {
 
@@ -227,12 +228,13 @@ __global__ void __launch_bounds__(kBmThreads)
     union_bitmap_kernel(const int32_t* __restrict__ indices, const int32_t* __restrict__ topk_len,
                         int64_t n_rows, int32_t topk, int32_t G, int32_t W, int64_t n_kv_slots,
                         int32_t* __restrict__ union_idx, uint8_t* __restrict__ union_bits,
-                        int32_t* __restrict__ union_len, int32_t pad_outputs) {
+                        int32_t* __restrict__ union_len, int32_t pad_outputs, PagedAddr pa) {
   extern __shared__ uint32_t sm_words[];
   int32_t* ent = reinterpret_cast<int32_t*>(sm_words);    // [G][topk]: valid slot or -1
   uint32_t* bm = sm_words + G * topk;                      // [G][W] bitmaps of one window
   __shared__ int scratch[kBmThreads / 32];
   __shared__ int row_total[8], row_base[8], row_done[8];
+  __shared__ int32_t row_req[8], row_kvlen[8];
 
   const int64_t group = blockIdx.x;
   const int64_t r0 = group * G;
@@ -242,7 +244,23 @@ __global__ void __launch_bounds__(kBmThreads)
   int32_t* out_idx = union_idx + group * cap;
   uint8_t* out_bits = union_bits + group * cap;
 
-  // 1. valid slots of the group's rows (topk_len, negative, >= n_kv_slots filtered) and their max
+  // 0. paged indices: every row's request and KV length (warp 0, one row at a time)
+  const bool paged = pa.page_table != nullptr;
+  if (paged) {
+    if (tid < 32) {
+      for (int u = 0; u < Gp; ++u) {
+        const int32_t req = paged_request_of_row(pa, r0 + u, tid);
+        if (tid == 0) {
+          row_req[u] = req;
+          row_kvlen[u] = paged_kv_len(pa, req);
+        }
+      }
+    }
+    __syncthreads();
+  }
+
+  // 1. valid slots of the group's rows (topk_len, negative, >= n_kv_slots filtered; logical
+  //    positions translated through the page table) and their max
   int my_max = -1;
   for (int e = tid; e < Gp * topk; e += kBmThreads) {
     const int u = e / topk, j = e - u * topk;
@@ -251,6 +269,10 @@ __global__ void __launch_bounds__(kBmThreads)
     if (topk_len) Lr = min(max(topk_len[r], 0), topk);
     int32_t x = -1;
     if (j < Lr) x = indices[r * topk + j];
+    if (paged) {
+      const int64_t slot = paged_slot(pa, row_req[u], row_kvlen[u], x);
+      x = slot > static_cast<int64_t>(INT32_MAX) ? -1 : static_cast<int32_t>(slot);
+    }
     if (x < 0 || (n_kv_slots > 0 && x >= n_kv_slots)) x = -1;
     ent[e] = x;
     my_max = max(my_max, x);
@@ -370,8 +392,13 @@ size_t union_sort_smem_bytes(int32_t topk, int32_t union_g) {
 cudaError_t launch_union_build(const int32_t* indices, const int32_t* topk_len, int64_t n_rows,
                                int32_t topk, int32_t union_g, int64_t n_kv_slots,
                                int32_t* sorted_out, int32_t* union_idx, uint8_t* union_bits,
-                               int32_t* union_len, bool pad_outputs, cudaStream_t stream) {
+                               int32_t* union_len, bool pad_outputs, const PagedAddr* paged,
+                               cudaStream_t stream) {
   if (n_rows == 0) return cudaSuccess;
+  // The sorted-rows kernel takes physical slots only.
+  if (paged != nullptr && sorted_out != nullptr) return cudaErrorInvalidValue;
+  PagedAddr pa{};
+  if (paged != nullptr) pa = *paged;
   const int64_t n_groups = (n_rows + union_g - 1) / union_g;
   if (sorted_out == nullptr) {
     const int W = union_bitmap_words(topk, union_g);
@@ -389,7 +416,7 @@ cudaError_t launch_union_build(const int32_t* indices, const int32_t* topk_len, 
     }
     union_bitmap_kernel<<<static_cast<unsigned>(n_groups), kBmThreads, smem, stream>>>(
         indices, topk_len, n_rows, topk, union_g, W, n_kv_slots, union_idx, union_bits, union_len,
-        pad_outputs ? 1 : 0);
+        pad_outputs ? 1 : 0, pa);
     return cudaGetLastError();
   }
   const int Kp = next_pow2(topk);

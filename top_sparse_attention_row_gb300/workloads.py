@@ -216,6 +216,7 @@ def make_mixed(seed: int = 4, new_tokens=(512, 2048, 4096, 8192),
     k = randn_bf16(rng, (S, n_kvheads, HEAD_DIM))
     v = randn_bf16(rng, (S, n_kvheads, HEAD_DIM))
     idx = np.full((R, topk), -1, dtype=np.int32)
+    logical_idx = np.full((R, topk), -1, dtype=np.int32)
     tlen = np.zeros(R, dtype=np.int32)
     pos = np.zeros(R, dtype=np.int64)
     req_of_row = np.zeros(R, dtype=np.int32)
@@ -226,13 +227,22 @@ def make_mixed(seed: int = 4, new_tokens=(512, 2048, 4096, 8192),
             p = pre + j
             n = min(p + 1, topk)
             logical = rng.choice(p + 1, size=n, replace=False)
+            logical_idx[r, :n] = logical
             idx[r, :n] = pt[logical // page_size] * page_size + logical % page_size
             tlen[r] = n
             pos[r] = p
             req_of_row[r] = i
             r += 1
+    # The same batch as the paged call takes it: logical positions, ragged row offsets and one
+    # page-table row per request (-1 past the request's pages).
+    table = np.full((len(page_tables), max(pages_per_req)), -1, dtype=np.int32)
+    for i, pt in enumerate(page_tables):
+        table[i, :len(pt)] = pt
+    cu_seqlens_q = np.concatenate([[0], np.cumsum(new_tokens)]).astype(np.int32)
     meta = dict(page_size=page_size, page_tables=page_tables, prefixes=list(prefixes),
-                new_tokens=list(new_tokens), kv_lens=kv_lens, req_of_row=req_of_row)
+                new_tokens=list(new_tokens), kv_lens=kv_lens, req_of_row=req_of_row,
+                logical_indices=logical_idx, page_table=table, cu_seqlens_q=cu_seqlens_q,
+                kv_lens_array=np.asarray(kv_lens, dtype=np.int32), n_pages=n_pages)
     return Workload("mixed_paged", q, k, v, idx, tlen, 1.0 / 16.0, pos, meta)
 
 
