@@ -37,10 +37,12 @@ if ROOT not in sys.path:
 METRIC = "sparse prefill query-rows/s (topk 2051, d=256, bf16) and % of gather/MMA roofline"
 UNIT = "query-rows/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ["top_sparse_attention_row_gb300/csrc/prefill.cu",
-                  "top_sparse_attention_row_gb300/csrc/ptx.cuh",
-                  "top_sparse_attention_row_gb300/csrc/internal.h",
-                  "top_sparse_attention_row_gb300/csrc/paged.cuh"]
+_COMMON_KERNEL_SOURCES = ["top_sparse_attention_row_gb300/csrc/ptx.cuh",
+                          "top_sparse_attention_row_gb300/csrc/internal.h",
+                          "top_sparse_attention_row_gb300/csrc/paged.cuh",
+                          "top_sparse_attention_row_gb300/csrc/compact.cuh"]
+KERNEL_SOURCES = ["top_sparse_attention_row_gb300/csrc/prefill.cu"] + _COMMON_KERNEL_SOURCES
+MLA_KERNEL_SOURCES = ["top_sparse_attention_row_gb300/csrc/mla.cu"] + _COMMON_KERNEL_SOURCES
 
 DESCRIPTIONS = {
     "group6_32k": "group-6 prefill chunk: 8192 rows at the end of a 32768 context, 6 Q / 1 KV, "
@@ -52,12 +54,16 @@ DESCRIPTIONS = {
     "mixed_paged": "mixed batch 512/2048/4096/8192 new tokens over prefixes 0/16k/32k/64k, "
                    "6 Q / 1 KV, topk 2051, per-row topk_len, paged cache (64), shuffled pages",
     "tiny": "tiny: 256 rows at positions 256..511, 6 Q / 1 KV, topk 128",
+    "mla_8k": "MLA shape: 8192-token prefill from position 0, 8 heads, d_qk 576 (512 latent + 64 "
+              "rope) / d_v 512 over one latent KV row per token, topk 2048, random-walk indices",
+    "mla_4k": "MLA shape, 4096-token prefill (as mla_8k)",
+    "mla_2k": "MLA shape, 2048-token prefill (as mla_8k; every row selects its whole prefix)",
 }
 
 
-def kernel_sha() -> str:
+def kernel_sha(mla: bool = False) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in (MLA_KERNEL_SOURCES if mla else KERNEL_SOURCES):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -76,6 +82,8 @@ def workload_stats(w):
     """Algorithmic FLOPs / bytes of one call (unpadded heads, valid slots only)."""
     v = w.valid_counts().astype(np.int64)
     D, Hq, Hkv = w.head_dim, w.n_qheads, w.n_kvheads
+    if w.meta.get("mla"):
+        return mla_stats(w, v)
     flops = int(4 * Hq * D * v.sum())                       # QK^T + PV, 2 flops per MAC
     idx = w.indices
     mask = idx >= 0
@@ -88,6 +96,22 @@ def workload_stats(w):
     gathered = int(v.sum()) * Hkv * D * 2 * 2                 # every (row, slot) K+V read
     return dict(flops=flops, bytes=kv_unique + io, unique_slots=unique_slots, gathered=gathered,
                 valid_slots=int(v.sum()))
+
+
+def mla_stats(w, v):
+    """MLA shape: QK^T over 576 dims and PV over 512 per (row, head, valid slot); each slot is one
+    1152-byte latent row, gathered once for both."""
+    Dqk, Dv, H = w.q.shape[2], w.meta["d_v"], w.n_qheads
+    flops = int(2 * H * (Dqk + Dv) * v.sum())
+    idx = w.indices
+    mask = idx >= 0
+    if w.topk_len is not None:
+        mask &= np.arange(idx.shape[1])[None, :] < np.clip(w.topk_len, 0, idx.shape[1])[:, None]
+    unique_slots = int(np.unique(idx[mask]).size)
+    io = (w.n_rows * H * (Dqk + Dv) * 2 + idx.size * 4 + w.n_rows * H * 4
+          + (0 if w.topk_len is None else w.n_rows * 4))
+    return dict(flops=flops, bytes=unique_slots * Dqk * 2 + io, unique_slots=unique_slots,
+                gathered=int(v.sum()) * Dqk * 2, valid_slots=int(v.sum()))
 
 
 # ------------------------------------------------------------------------- CPU oracle leg
@@ -105,7 +129,11 @@ def _oracle_init(name, seed_kw):
 def _oracle_rows(rows):
     import oracle
     w = _W
-    oracle.sparse_prefill_rows(w.q, w.k, w.v, w.indices, w.topk_len, w.scale, rows)
+    if w.meta.get("mla"):
+        oracle.sparse_mla_prefill_rows(w.q, w.k.reshape(w.k.shape[0], -1), w.indices, w.topk_len,
+                                       w.scale, rows, w.meta["d_v"])
+    else:
+        oracle.sparse_prefill_rows(w.q, w.k, w.v, w.indices, w.topk_len, w.scale, rows)
     return len(rows)
 
 
@@ -207,7 +235,15 @@ def run_gpu(args, rank, world, local_rank):
     def bf(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
 
-    h_q, h_k, h_v = bf(w.q).pin_memory(), bf(w.k).pin_memory(), bf(w.v).pin_memory()
+    mla = bool(w.meta.get("mla"))
+    if mla and args.paged:
+        raise SystemExit("--paged applies to the d=256 workloads")
+    h_q = bf(w.q).pin_memory()
+    if mla:   # one latent cache [S, 576]; V is its first 512 dims, not a separate tensor
+        h_k = bf(w.k.reshape(w.k.shape[0], -1)).pin_memory()
+        h_v = h_k[:0]
+    else:
+        h_k, h_v = bf(w.k).pin_memory(), bf(w.v).pin_memory()
     paged = args.paged
     if paged and "page_table" not in w.meta:
         raise SystemExit(f"--paged needs a paged workload; {args.config} has no page table")
@@ -222,7 +258,8 @@ def run_gpu(args, rank, world, local_rank):
     idx = h_idx.to(dev)
     tl = None if h_tl is None else h_tl.to(dev)
     d_meta = tuple(t.to(dev) for t in h_meta)
-    out = torch.empty_like(q)
+    out = (torch.empty((w.n_rows, w.n_qheads, w.meta["d_v"]), dtype=torch.bfloat16, device=dev)
+           if mla else torch.empty_like(q))
     lse = torch.empty((w.n_rows, w.n_qheads), dtype=torch.float32, device=dev)
     ws = None
     if args.union > 1:
@@ -232,7 +269,10 @@ def run_gpu(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
 
     def call():
-        if paged:
+        if mla:
+            binding.sparse_mla_prefill(q, k, idx, tl, w.scale, out=out, lse=lse, union_g=args.union,
+                                       stream=stream)
+        elif paged:
             cu, kvl, pt = d_meta
             binding.sparse_prefill_paged(q, k, v, idx, tl, cu, kvl, pt, w.meta["page_size"], w.scale,
                                          n_pages=w.meta["n_pages"], out=out, lse=lse,
@@ -241,12 +281,20 @@ def run_gpu(args, rank, world, local_rank):
             binding.sparse_prefill(q, k, v, idx, tl, w.scale, out=out, lse=lse, union_g=args.union,
                                    workspace=ws, stream=stream)
 
-    geo = binding.select_geometry(w.n_qheads, w.n_kvheads, args.union, w.topk, w.head_dim, w.n_rows)
-    # gather ceiling on this workload's own K cache and selected rows (KV head 0)
-    valid = w.indices[w.indices >= 0].astype(np.int64) * w.n_kvheads
+    if mla:
+        geo = binding.select_mla_geometry(w.n_qheads, args.union, w.topk, w.n_rows)
+    else:
+        geo = binding.select_geometry(w.n_qheads, w.n_kvheads, args.union, w.topk, w.head_dim,
+                                      w.n_rows)
+    # gather ceiling on this workload's own K cache and selected rows (KV head 0), through a
+    # view of the cache as 512-byte rows (for the 1152-byte MLA rows: the row holding each
+    # selected slot's first bytes)
+    valid = w.indices[w.indices >= 0].astype(np.int64)
+    valid = valid * w.n_kvheads if not mla else (valid * w.q.shape[2]) // 256
     n_pieces = min(len(valid) // 128, 4096)
     table = torch.from_numpy(valid[: n_pieces * 128].astype(np.int32).reshape(n_pieces, 128)).to(dev)
-    k_rows = k.view(-1, w.head_dim)
+    k_flat = k.reshape(-1)
+    k_rows = k_flat[: (k_flat.numel() // 256) * 256].view(-1, 256)
     ceilings = {}
     for eng in ("tma", "cpasync"):
         binding.probe_gather_ceiling(k_rows, table, pieces_per_cta=200, engine=eng)
@@ -351,7 +399,7 @@ def run_gpu(args, rank, world, local_rank):
             tj = json.load(f)
         key = f"{args.config}:union{args.union}" + (":paged" if paged else "")
         ent = tj.get(key)
-        if ent and ent.get("kernel_sha") == kernel_sha():
+        if ent and ent.get("kernel_sha") == kernel_sha(mla):
             traffic = ent.get("dram_bytes_per_launch")
     roofline = {
         "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,

@@ -145,6 +145,30 @@ qsa_status qsa_sparse_prefill_paged(const void* q, const void* k_cache, const vo
                                     int32_t n_kvheads, int32_t head_dim, int32_t topk, float scale,
                                     int32_t union_g, void* stream);
 
+/* MLA-shaped sparse prefill ("DSA prefill ... triton_sparse_mla", Motivation and Speed Tests:
+ * one latent KV row per token, kv_lora_rank 512 + qk_rope_head_dim 64 = 576 dims for QK^T, the
+ * 512 latent dims as V, topk 2048, 8 heads at TP8, union G = 2 / 4).  Every query head attends
+ * over its row's selected slots of the single latent KV head.
+ *   q        [n_rows, n_heads, d_qk]  bf16
+ *   kv_cache [n_slots, d_qk]          bf16; K = the whole row, V = its first d_v dims
+ *   indices  [n_rows, topk] int32 physical slots (< 0 = padding); topk_len as above
+ *   out      [n_rows, n_heads, d_v]   bf16;  lse [n_rows, n_heads] fp32 (nullable)
+ *   d_qk must be 576 and d_v 512 (QSA_ERR_UNSUPPORTED otherwise).  union_g as in
+ *   qsa_sparse_prefill; a union needs union_g * n_heads <= 32, otherwise the per-token path
+ *   runs and counts a fallback.  n_kv_slots: 0 = unchecked, > 0 = slots >= n_kv_slots are
+ *   padding.  q, kv_cache and out must be 16-byte aligned.  Union workspace is allocated on
+ *   `stream` (cudaMallocAsync / cudaFreeAsync).  Errors, streams and determinism are as for
+ *   qsa_sparse_prefill. */
+qsa_status qsa_sparse_mla_prefill(const void* q, const void* kv_cache, const int32_t* indices,
+                                  const int32_t* topk_len, void* out, float* lse, int64_t n_rows,
+                                  int32_t n_heads, int32_t d_qk, int32_t d_v, int32_t topk,
+                                  float scale, int32_t union_g, int64_t n_kv_slots, void* stream);
+
+/* Host-only geometry selection for qsa_sparse_mla_prefill (stages = latent ring depth). */
+qsa_status qsa_select_mla_geometry(int32_t n_heads, int32_t union_g, int32_t topk, int32_t d_qk,
+                                   int32_t d_v, int64_t n_rows, int32_t num_sms,
+                                   qsa_geometry* out);
+
 /* Allocation-free variant of qsa_sparse_prefill (same arguments, same results).  The pages
  * have no counterpart: it exists for callers that must not allocate device memory -- code
  * whose GPU memory is owned entirely by a framework's pool, latency-critical loops where an

@@ -32,6 +32,9 @@ Functions and the passages they follow:
   ragged request metadata ("DSA prefill ... triton_sparse_mla", Robustness:
   PAGED / RAGGED index transforms, valid length from the cache sequence
   lengths; "[QSA] Tune sm120 sparse prefill geometry": paged serving cache).
+* ``mla.sparse_mla_prefill`` -- the MLA shape: one latent row per slot whose
+  576 dims are the key and whose first 512 dims are the value, shared by every
+  head ("DSA prefill ... triton_sparse_mla", Motivation and Speed Tests).
 
 Every function is pinned by ``tests/test_oracle_pins.py`` against facts that
 do not come from this package: dense causal attention from a library routine
@@ -43,3 +46,4 @@ from .attention import sparse_prefill, sparse_prefill_rows, valid_slots  # noqa:
 from .union import sorted_rows, union_build, union_attention  # noqa: F401
 from .paged import (sparse_prefill_paged, sparse_prefill_paged_rows,  # noqa: F401
                     physical_indices, request_of_rows)
+from .mla import sparse_mla_prefill, sparse_mla_prefill_rows  # noqa: F401

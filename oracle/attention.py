@@ -50,10 +50,10 @@ def valid_slots(index_row: np.ndarray, topk_len_r, n_kv_slots: int = 0) -> np.nd
 
 
 def _attend(qg: np.ndarray, ksel: np.ndarray, vsel: np.ndarray, scale: float):
-    """qg [g, D], ksel/vsel [n, D] -> (O [g, D], lse [g]) in float64."""
-    g, D = qg.shape
-    if ksel.shape[0] == 0:
-        return np.zeros((g, D)), np.full(g, -np.inf)
+    """qg [g, D], ksel [n, D], vsel [n, Dv] -> (O [g, Dv], lse [g]) in float64."""
+    g = qg.shape[0]
+    if ksel.shape[0] == 0:                       # no valid slot: O = 0, LSE = -inf
+        return np.zeros((g, vsel.shape[1])), np.full(g, -np.inf)
     s = scale * (qg @ ksel.T)                    # [g, n]
     m = s.max(axis=1, keepdims=True)
     p = np.exp(s - m)

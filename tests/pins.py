@@ -471,3 +471,66 @@ def check_paged_identity(fn):
 
 
 PAGED_CHECKS = [check_paged_vs_contiguous, check_paged_identity]
+
+
+# ----------------------------------------------------------------------------- MLA
+
+def mla_case(seed, S=40, R=14, H=4, Dqk=12, Dv=8):
+    """Rows at positions S-R..S-1 selecting their whole causal prefix (shuffled, -1 padded)."""
+    rng = _rng(seed)
+    pos = np.arange(S - R, S)
+    q = rng.standard_normal((R, H, Dqk))
+    kv = rng.standard_normal((S, Dqk))
+    topk = S + 5
+    idx = np.full((R, topk), -1, dtype=np.int64)
+    for r, p in enumerate(pos):
+        perm = rng.permutation(p + 1)
+        slots = rng.choice(topk, size=p + 1, replace=False)
+        idx[r, slots] = perm
+    return q, kv, idx, pos, Dv
+
+
+def check_mla_dense(fn):
+    """Whole-prefix selection equals dense causal attention with keys = the full latent row and
+    values = its first d_v dims (torch's math attention; LSE by torch.logsumexp)."""
+    fails = []
+    for seed, (H, Dqk, Dv) in enumerate([(4, 12, 8), (1, 9, 9), (3, 16, 5)]):
+        q, kv, idx, pos, Dv = mla_case(400 + seed, H=H, Dqk=Dqk, Dv=Dv)
+        scale = 0.29
+        O, L = fn(q, kv, idx, None, scale, Dv)
+        tq = torch.from_numpy(q).permute(1, 0, 2)[None]                      # [1, H, R, Dqk]
+        tk = torch.from_numpy(kv)[None, None].expand(1, H, -1, -1)
+        tv = torch.from_numpy(kv[:, :Dv])[None, None].expand(1, H, -1, -1)
+        keypos = torch.arange(kv.shape[0])[None, :]
+        mask = torch.where(keypos <= torch.from_numpy(pos)[:, None], 0.0, float("-inf")).double()
+        out = torch.ops.aten._scaled_dot_product_attention_math(tq, tk, tv, attn_mask=mask,
+                                                                scale=scale)[0]
+        lse = torch.logsumexp(scale * tq @ tk.transpose(-1, -2) + mask, dim=-1)
+        Od = out[0].permute(1, 0, 2).numpy()
+        Ld = lse[0].permute(1, 0).numpy()
+        if not (_close(O, Od, 1e-10) and _close(L, Ld, 1e-10)):
+            fails.append(f"MLA dense mismatch (H={H}, d_qk={Dqk}, d_v={Dv})")
+    return fails
+
+
+def check_mla_vs_padded_gqa(fn):
+    """The MLA layout as one KV head: key = the latent row, value = its first d_v dims padded
+    with zeros to d_qk.  The plain (pinned) oracle must give O in the first d_v dims, zeros
+    after, and the same LSE; topk_len and padding included."""
+    from oracle import sparse_prefill
+    rng = _rng(410)
+    R, S, H, Dqk, Dv, K = 9, 30, 5, 12, 7, 20
+    q = rng.standard_normal((R, H, Dqk))
+    kv = rng.standard_normal((S, Dqk))
+    idx = rng.integers(-2, S, size=(R, K))
+    tl = rng.integers(0, K + 1, size=R)
+    tl[0] = 0                                   # rows with no valid slot: O = 0, LSE = -inf
+    idx[1] = -1
+    O, L = fn(q, kv, idx, tl, 0.37, Dv)
+    vpad = np.concatenate([kv[:, :Dv], np.zeros((S, Dqk - Dv))], axis=1)
+    Og, Lg = sparse_prefill(q, kv[:, None, :], vpad[:, None, :], idx, tl, 0.37)
+    ok = _close(O, Og[:, :, :Dv], 1e-12) and _close(L, Lg, 1e-12) and np.all(Og[:, :, Dv:] == 0)
+    return [] if ok else ["MLA != padded single-KV-head attention"]
+
+
+MLA_CHECKS = [check_mla_dense, check_mla_vs_padded_gqa]

@@ -130,3 +130,32 @@ def test_counters_reset(lib):
     from top_sparse_attention_row_gb300 import binding as B
     B.reset_counters()
     assert all(v == 0 for v in B.counters().values())
+
+
+def test_mla_selector(lib):
+    """MLA geometry: N = heads (or G x heads) padded to 16/32, a 5-stage latent ring when it fits,
+    union fallback past 32 columns, head chunks past 32 heads, d_qk/d_v other than 576/512
+    unsupported."""
+    from top_sparse_attention_row_gb300 import binding as B
+    g = B.select_mla_geometry(8, 0, 2048, 8192, num_sms=152)
+    assert (g["n_pad"], g["cols"], g["stages"], g["union_g"], g["tmem_cols"]) == (16, 8, 5, 1, 128)
+    assert g["grid"] == 152 and g["n_items"] == 8192 and g["smem_bytes"] <= 232448
+    g = B.select_mla_geometry(8, 4, 2048, 8192, num_sms=152)
+    assert (g["n_pad"], g["cols"], g["union_g"], g["n_items"], g["tmem_cols"]) == (32, 32, 4, 2048, 256)
+    assert g["stages"] == 4
+    g = B.select_mla_geometry(16, 4, 2048, 100, num_sms=152)     # 64 columns: per-token instead
+    assert g["union_g"] == 1 and g["n_pad"] == 16
+    g = B.select_mla_geometry(40, 0, 2048, 10, num_sms=152)      # two chunks of 20 heads
+    assert g["head_chunks"] == 2 and g["cols"] == 20 and g["n_pad"] == 32 and g["n_items"] == 20
+    sel = lib.qsa_select_mla_geometry
+    out = B.Geometry()
+    assert sel(8, 0, 2048, 512, 512, 10, 152, ctypes.byref(out)) == 2
+    assert sel(8, 0, 2048, 576, 256, 10, 152, ctypes.byref(out)) == 2
+    assert sel(0, 0, 2048, 576, 512, 10, 152, ctypes.byref(out)) == 1
+    assert sel(8, 0, 1 << 16, 576, 512, 10, 152, ctypes.byref(out)) == 2   # slot list too large
+    f = lib.qsa_sparse_mla_prefill
+    fake = 1 << 20
+    assert f(None, fake, fake, None, fake, None, 10, 8, 576, 512, 2048, 0.04, 0, 0, None) == 1
+    assert f(fake, fake + 8, fake, None, fake, None, 10, 8, 576, 512, 2048, 0.04, 0, 0, None) == 1
+    assert f(fake, fake, fake, None, fake, None, 10, 8, 576, 256, 2048, 0.04, 0, 0, None) == 2
+    assert f(fake, fake, fake, None, fake, None, 0, 8, 576, 512, 2048, 0.04, 0, 0, None) == 0

@@ -1,0 +1,124 @@
+"""The MLA-shaped kernel (qsa_sparse_mla_prefill: d_qk 576, d_v 512, one latent KV row per slot)
+against the MLA oracle, per-token and union, small cases in full and the 8192-token workloads on
+sampled rows (GPU only).  Bounds: O max-abs 2e-2, LSE relative 1e-3 (helpers.py)."""
+import numpy as np
+import pytest
+
+import oracle
+from helpers import assert_parity
+from top_sparse_attention_row_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    from top_sparse_attention_row_gb300 import build, binding
+    build.build()
+    binding.load_library()
+    return binding
+
+
+def dev(w):
+    import torch
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+    q = bf(w.q)
+    kv = bf(w.k.reshape(w.k.shape[0], -1))
+    idx = torch.from_numpy(np.ascontiguousarray(w.indices, dtype=np.int32)).cuda()
+    tl = None if w.topk_len is None else torch.from_numpy(np.ascontiguousarray(w.topk_len, dtype=np.int32)).cuda()
+    return q, kv, idx, tl
+
+
+def run(B, w, union_g=0, n_kv_slots=0):
+    import torch
+    q, kv, idx, tl = dev(w)
+    out, lse = B.sparse_mla_prefill(q, kv, idx, tl, w.scale, union_g=union_g, n_kv_slots=n_kv_slots)
+    torch.cuda.synchronize()
+    assert B.device_status() == 0
+    return out, lse
+
+
+def ref(w, rows=None, n_kv_slots=0):
+    rows = np.arange(w.n_rows) if rows is None else rows
+    return oracle.sparse_mla_prefill_rows(w.q, w.k.reshape(w.k.shape[0], -1), w.indices, w.topk_len,
+                                          w.scale, rows, 512, n_kv_slots)
+
+
+def chunk_mla(n_rows, context, n_heads, topk, seed):
+    """n_rows rows at the end of a context, uniform causal selections (several tiles + tail)."""
+    rng = np.random.default_rng(seed)
+    pos = np.arange(context - n_rows, context)
+    q = W.randn_bf16(rng, (n_rows, n_heads, 576))
+    kv = W.randn_bf16(rng, (context, 1, 576))
+    idx = W.causal_uniform_indices(rng, pos, topk)
+    return W.Workload("mla_chunk", q, kv, kv[:, :, :512], idx, None, 1.0 / 24.0, pos)
+
+
+@pytest.mark.parametrize("heads", [8, 1, 16, 32, 40])
+def test_mla_multi_tile_ragged(B, heads):
+    # 2051 slots = 16 full tiles + a 3-slot tail; early rows have short prefixes
+    w = chunk_mla(n_rows=48, context=2300, n_heads=heads, topk=2051, seed=heads)
+    out, lse = run(B, w)
+    O, L = ref(w)
+    assert_parity(out, lse, O, L, what=f"mla {heads} heads")
+
+
+@pytest.mark.parametrize("topk", [1, 17, 128, 129, 640])
+def test_mla_topk_widths(B, topk):
+    w = chunk_mla(n_rows=40, context=900, n_heads=8, topk=topk, seed=100 + topk)
+    out, lse = run(B, w)
+    O, L = ref(w)
+    assert_parity(out, lse, O, L, what=f"mla topk {topk}")
+
+
+@pytest.mark.parametrize("G,heads", [(2, 8), (4, 8), (2, 16), (3, 8)])
+def test_mla_union_equals_per_token_oracle(B, G, heads):
+    w = W.make_mla(seed=20 + G, n_rows=601, topk=256, n_heads=heads, name="mla_union_small")
+    before = B.counters()
+    out, lse = run(B, w, union_g=G)
+    after = B.counters()
+    assert after["calls_union"] == before["calls_union"] + 1
+    O, L = ref(w)
+    assert_parity(out, lse, O, L, what=f"mla union G={G} heads={heads}")
+
+
+def test_mla_union_fallback_counted(B):
+    w = W.make_mla(seed=30, n_rows=64, topk=128, n_heads=16, name="mla_fallback")
+    before = B.counters()
+    out, lse = run(B, w, union_g=4)                      # 4 x 16 = 64 columns > 32
+    after = B.counters()
+    assert after["union_fallbacks"] == before["union_fallbacks"] + 1
+    O, L = ref(w)
+    assert_parity(out, lse, O, L, what="mla union fallback")
+
+
+def test_mla_edge_rows(B):
+    """All -1, topk_len 0 and short, other negatives, duplicates (weighted twice), slots past
+    n_kv_slots."""
+    w = chunk_mla(n_rows=10, context=700, n_heads=8, topk=300, seed=55)
+    idx = w.indices.copy()
+    tl = np.full(10, 300, dtype=np.int32)
+    idx[0] = -1
+    tl[1] = 0
+    tl[2] = 5
+    idx[3, ::4] = -7
+    idx[4, 10:20] = idx[4, 0:10]                           # duplicates
+    idx[5, 0:30] = 650                                     # >= n_kv_slots below: padding
+    w = W.Workload("mla_edge", w.q, w.k, w.v, idx, tl, w.scale, w.positions)
+    out, lse = run(B, w, n_kv_slots=600)
+    O, L = ref(w, n_kv_slots=600)
+    assert np.isneginf(L[0]).all() and np.isneginf(L[1]).all()
+    assert_parity(out, lse, O, L, what="mla edge rows")
+
+
+@pytest.mark.parametrize("G", [0, 2, 4])
+def test_mla_full_size_8k(B, G):
+    """The 8192-token MLA prefill (8 heads, topk 2048, random walk) as the benchmark runs it,
+    against the oracle on sampled rows (first tile rows, walk rows, group tails)."""
+    w = W.make("mla_8k")
+    out, lse = run(B, w, union_g=G)
+    rows = np.unique(np.concatenate([np.arange(0, w.n_rows, 409), [1, 2, 3, 2047, 2048, 2049,
+                                                                     8189, 8190, 8191]]))
+    O, L = ref(w, rows=rows)
+    assert_parity(out, lse, O, L, rows=rows, what=f"mla_8k G={G}")

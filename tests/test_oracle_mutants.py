@@ -142,3 +142,37 @@ def test_paged_unmutated_copy_passes():
 def test_paged_mutant_is_caught(kind):
     fn = _paged_mutant(kind)
     assert [f for c in pins.PAGED_CHECKS for f in c(fn)], f"mutant {kind} passed every pin"
+
+
+def _mla_mutant(kind):
+    """A copy of the MLA oracle with one planted mistake."""
+    def fn(q, kv, idx, tl, scale, d_v):
+        R, H, D = q.shape
+        O = np.zeros((R, H, d_v))
+        L = np.full((R, H), -np.inf)
+        for r in range(R):
+            J = valid_slots(idx[r], None if tl is None else tl[r])
+            if len(J) == 0:
+                continue
+            rows = np.asarray(kv, dtype=np.float64)[J]
+            keys = rows[:, :d_v] if kind == "key_drops_rope" else rows
+            vals = rows[:, D - d_v:] if kind == "value_from_tail" else rows[:, :d_v]
+            for h in range(H):
+                qh = np.asarray(q[r, 0 if kind == "head_zero_for_all" else h], dtype=np.float64)
+                qk = qh[:d_v] if kind == "key_drops_rope" else qh
+                s = scale * (keys @ qk)
+                m = s.max()
+                p = np.exp(s - m)
+                O[r, h] = (p @ vals) / p.sum()
+                L[r, h] = m + np.log(p.sum())
+        return O, L
+    return fn
+
+
+def test_mla_unmutated_copy_passes():
+    assert [f for c in pins.MLA_CHECKS for f in c(_mla_mutant("none"))] == []
+
+
+@pytest.mark.parametrize("kind", ["key_drops_rope", "value_from_tail", "head_zero_for_all"])
+def test_mla_mutant_is_caught(kind):
+    assert [f for c in pins.MLA_CHECKS for f in c(_mla_mutant(kind))], f"mutant {kind} passed"

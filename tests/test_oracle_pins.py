@@ -68,3 +68,9 @@ def test_sorted_rows_vs_python_sorted():
 @pytest.mark.parametrize("check", pins.PAGED_CHECKS, ids=lambda c: c.__name__)
 def test_paged_pin(check):
     assert check(oracle.sparse_prefill_paged) == []
+
+
+@pytest.mark.parametrize("check", pins.MLA_CHECKS, ids=lambda c: c.__name__)
+def test_mla_pin(check):
+    fn = lambda q, kv, idx, tl, scale, d_v: oracle.sparse_mla_prefill(q, kv, idx, tl, scale, d_v)
+    assert check(fn) == []

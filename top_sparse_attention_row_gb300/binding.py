@@ -23,7 +23,7 @@ EXPORTED = ["qsa_sparse_prefill", "qsa_sparse_prefill_ex", "qsa_workspace_bytes"
             "qsa_union_build", "qsa_select_geometry", "qsa_get_counters", "qsa_reset_counters",
             "qsa_status_string", "qsa_version", "qsa_get_device_status",
             "qsa_sparse_prefill_noalloc", "qsa_probe_gather_ceiling",
-            "qsa_sparse_prefill_paged"]
+            "qsa_sparse_prefill_paged", "qsa_sparse_mla_prefill", "qsa_select_mla_geometry"]
 
 # Size of the library-owned scratch array used by qsa_sparse_prefill_noalloc (include/qsa.h).
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -74,6 +74,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qsa_sparse_prefill_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, i32,
                                              i32, i64, i32, i32, i32, i32, f32, i32, vp]
     lib.qsa_sparse_prefill_paged.restype = ctypes.c_int
+    lib.qsa_sparse_mla_prefill.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, f32, i32,
+                                           i64, vp]
+    lib.qsa_sparse_mla_prefill.restype = ctypes.c_int
+    lib.qsa_select_mla_geometry.argtypes = [i32, i32, i32, i32, i32, i64, i32, ctypes.POINTER(Geometry)]
+    lib.qsa_select_mla_geometry.restype = ctypes.c_int
     lib.qsa_probe_gather_ceiling.argtypes = [vp, i64, vp, i64, i32, i32, ctypes.POINTER(f32), vp]
     lib.qsa_probe_gather_ceiling.restype = ctypes.c_int
     lib.qsa_workspace_bytes.argtypes = [i64, i32, i32]
@@ -213,6 +218,45 @@ def sparse_prefill_paged(q, k_cache, v_cache, indices, topk_len, cu_seqlens_q, k
                                       D, topk, float(scale), int(union_g), _stream_ptr(stream))
     _check(st, "qsa_sparse_prefill_paged")
     return out, lse
+
+
+def sparse_mla_prefill(q, kv_cache, indices, topk_len, scale: float, *, out=None, lse=None,
+                       union_g: int = 0, n_kv_slots: int = 0, want_lse: bool = True, stream=None):
+    """MLA shape (qsa_sparse_mla_prefill): q [R, H, 576] bf16, kv_cache [S, 576] bf16 (the first
+    512 dims are the value), indices [R, topk] int32 physical slots, topk_len [R] int32 or None.
+    Returns O [R, H, 512] bf16 and LSE [R, H] fp32."""
+    import torch
+    lib = load_library()
+    _require(q, torch.bfloat16, "q", 3)
+    _require(kv_cache, torch.bfloat16, "kv_cache", 2)
+    _require(indices, torch.int32, "indices", 2)
+    _require(topk_len, torch.int32, "topk_len", 1)
+    R, H, Dqk = q.shape
+    Dv = 512
+    topk = indices.shape[1]
+    if indices.shape[0] != R or (topk_len is not None and topk_len.shape[0] != R):
+        raise ValueError("indices / topk_len rows must match q")
+    if kv_cache.shape[1] != Dqk:
+        raise ValueError("kv_cache rows must have q's head dim")
+    if out is None:
+        out = torch.empty((R, H, Dv), dtype=torch.bfloat16, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((R, H), dtype=torch.float32, device=q.device)
+    _require(out, torch.bfloat16, "out", 3)
+    _require(lse, torch.float32, "lse", 2)
+    st = lib.qsa_sparse_mla_prefill(_ptr(q), _ptr(kv_cache), _ptr(indices), _ptr(topk_len), _ptr(out),
+                                    _ptr(lse), R, H, Dqk, Dv, topk, float(scale), int(union_g),
+                                    int(n_kv_slots), _stream_ptr(stream))
+    _check(st, "qsa_sparse_mla_prefill")
+    return out, lse
+
+
+def select_mla_geometry(n_heads, union_g, topk, n_rows, num_sms=0, d_qk=576, d_v=512) -> dict:
+    g = Geometry()
+    st = load_library().qsa_select_mla_geometry(n_heads, union_g, topk, d_qk, d_v, n_rows, num_sms,
+                                                ctypes.byref(g))
+    _check(st, "qsa_select_mla_geometry")
+    return g.as_dict()
 
 
 def sparse_prefill_noalloc(q, k_cache, v_cache, indices, topk_len, scale: float, *, out=None,

@@ -114,6 +114,78 @@ qsa_status select(int32_t Hq, int32_t Hkv, int32_t union_g, int32_t topk, int32_
   return QSA_OK;
 }
 
+// MLA shape (d_qk 576, d_v 512, one latent KV row per slot): N = heads (or G x heads) padded
+// to 16 or 32; the latent ring takes 5 stages when shared memory allows (one spare stage lets
+// the next tile's first latent chunk overlap the softmax), else 4.
+qsa_status select_mla(int32_t n_heads, int32_t union_g, int32_t topk, int32_t d_qk, int32_t d_v,
+                      int64_t n_rows, int32_t num_sms, qsa::MlaGeometry* g, bool* fell_back) {
+  *fell_back = false;
+  if (n_heads <= 0 || topk <= 0 || n_rows < 0 || d_qk <= 0 || d_v <= 0 || union_g < 0 ||
+      union_g > 8 || num_sms <= 0)
+    return QSA_ERR_INVALID_ARG;
+  if (d_qk != qsa::kMlaDqk || d_v != qsa::kMlaDv) return QSA_ERR_UNSUPPORTED;
+  if (n_rows > INT32_MAX) return QSA_ERR_UNSUPPORTED;
+  auto stages_for = [](int np, int slot_cap) {
+    for (int rp = qsa::kMlaPairs + 1; rp >= qsa::kMlaPairs; --rp)
+      if (qsa::mla_smem_layout(np, rp, slot_cap).total <= qsa::kSmemLimit) return rp;
+    return 0;
+  };
+  int G = union_g <= 1 ? 1 : union_g;
+  if (G > 1) {
+    const int np_u = static_cast<int>(round_up(static_cast<int64_t>(G) * n_heads, 16));
+    const bool legal = static_cast<int64_t>(G) * n_heads <= qsa::kMlaMaxNPad &&
+                       stages_for(np_u, 0) > 0 &&
+                       qsa::union_build_smem_bytes(topk, G) <= static_cast<size_t>(qsa::kUnionMaxSmem) &&
+                       static_cast<int64_t>(G) * topk <= INT32_MAX / 2;
+    if (!legal) {
+      G = 1;
+      *fell_back = true;
+    }
+  }
+  int chunks, chunk_cols, slot_cap;
+  if (G == 1) {
+    chunks = static_cast<int>(ceil_div(n_heads, qsa::kMlaMaxNPad));
+    chunk_cols = static_cast<int>(ceil_div(n_heads, chunks));
+    slot_cap = static_cast<int>(round_up(topk, qsa::kTileTokens));
+  } else {
+    chunks = 1;
+    chunk_cols = G * n_heads;
+    slot_cap = 0;
+  }
+  const int np = static_cast<int>(round_up(chunk_cols, 16));
+  const int rp = stages_for(np, slot_cap);
+  if (rp == 0) return QSA_ERR_UNSUPPORTED;   // per-token slot list too large for topk
+  const int64_t n_groups = ceil_div(n_rows, G);
+  const int64_t n_items = n_groups * chunks;
+  g->np = np;
+  g->cols = chunk_cols;
+  g->head_chunks = chunks;
+  g->chunk_cols = chunk_cols;
+  g->union_g = G;
+  g->pair_stages = rp;
+  g->grid = static_cast<int>(n_items < num_sms ? n_items : num_sms);
+  g->smem_bytes = qsa::mla_smem_layout(np, rp, slot_cap).total;
+  g->tmem_cols = pow2_at_least(6 * np);
+  g->slot_cap = slot_cap;
+  g->n_items = n_items;
+  g->n_groups = static_cast<int>(n_groups);
+  return QSA_OK;
+}
+
+void mla_to_public(const qsa::MlaGeometry& g, qsa_geometry* out) {
+  out->tile_tokens = qsa::kTileTokens;
+  out->stages = g.pair_stages;
+  out->n_pad = g.np;
+  out->cols = g.cols;
+  out->head_chunks = g.head_chunks;
+  out->union_g = g.union_g;
+  out->grid = g.grid;
+  out->threads = qsa::kThreads;
+  out->smem_bytes = g.smem_bytes;
+  out->tmem_cols = g.tmem_cols;
+  out->n_items = g.n_items;
+}
+
 void to_public(const Geometry& g, qsa_geometry* out) {
   out->tile_tokens = qsa::kTileTokens;
   out->stages = g.stages;
@@ -254,9 +326,106 @@ qsa_status run(const void* q, const void* k_cache, const void* v_cache, const in
   return QSA_OK;
 }
 
+qsa_status run_mla(const void* q, const void* kv_cache, const int32_t* indices,
+                   const int32_t* topk_len, void* out, float* lse, int64_t n_rows, int32_t n_heads,
+                   int32_t d_qk, int32_t d_v, int32_t topk, float scale, int32_t union_g,
+                   int64_t n_kv_slots, const qsa::PagedAddr* paged, void* stream_v) {
+  if (!q || !kv_cache || !indices || !out) return QSA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(out)) return QSA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || n_kv_slots < 0) return QSA_ERR_INVALID_ARG;
+  if (n_kv_slots >= INT32_MAX) return QSA_ERR_UNSUPPORTED;
+  qsa::MlaGeometry g{};
+  bool fell_back = false;
+  qsa_status st = select_mla(n_heads, union_g, topk, d_qk, d_v, n_rows, 1, &g, &fell_back);
+  if (st != QSA_OK) return st;
+  if (n_rows == 0) return QSA_OK;
+  int32_t sms = 0;
+  st = device_sms(&sms);
+  if (st != QSA_OK) return st;
+  st = select_mla(n_heads, union_g, topk, d_qk, d_v, n_rows, sms, &g, &fell_back);
+  if (st != QSA_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+
+  qsa::MlaParams p{};
+  p.q = static_cast<const uint16_t*>(q);
+  p.indices = indices;
+  p.topk_len = topk_len;
+  p.out = static_cast<uint16_t*>(out);
+  p.lse = lse;
+  if (qsa::device_status_address(&p.status) != cudaSuccess) return QSA_ERR_CUDA;
+  p.n_rows = n_rows;
+  p.n_items = g.n_items;
+  p.n_kv_slots = n_kv_slots;
+  p.n_heads = n_heads;
+  p.topk = topk;
+  p.union_g = g.union_g;
+  p.n_groups = g.n_groups;
+  p.head_chunks = g.head_chunks;
+  p.chunk_cols = g.chunk_cols;
+  p.pair_stages = g.pair_stages;
+  p.slot_cap = g.slot_cap;
+  p.tmem_cols = g.tmem_cols;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  const int64_t tmap_rows = n_kv_slots > 0 ? n_kv_slots : static_cast<int64_t>(INT32_MAX);
+  p.pad_row = static_cast<int32_t>(tmap_rows);
+  if (paged) p.pa = *paged;
+
+  void* ws = nullptr;
+  if (g.union_g > 1) {
+    const WsLayout w = ws_layout(n_rows, topk, g.union_g);
+    if (cudaMallocAsync(&ws, w.total, stream) != cudaSuccess) return QSA_ERR_CUDA;
+    uint8_t* b = static_cast<uint8_t*>(ws);
+    p.union_idx = reinterpret_cast<int32_t*>(b + w.idx);
+    p.union_bits = b + w.bits;
+    p.union_len = reinterpret_cast<int32_t*>(b + w.len);
+    cudaError_t e = qsa::launch_union_build(indices, topk_len, n_rows, topk, g.union_g, n_kv_slots,
+                                            nullptr, const_cast<int32_t*>(p.union_idx),
+                                            const_cast<uint8_t*>(p.union_bits),
+                                            const_cast<int32_t*>(p.union_len), false, paged,
+                                            stream);
+    if (e != cudaSuccess) {
+      cudaFreeAsync(ws, stream);
+      return QSA_ERR_CUDA;
+    }
+    g_launches.fetch_add(1);
+  }
+  cudaError_t e = qsa::launch_mla(p, g, kv_cache, tmap_rows, stream);
+  if (ws) cudaFreeAsync(ws, stream);
+  if (e != cudaSuccess) return QSA_ERR_CUDA;
+  g_launches.fetch_add(1);
+  if (g.union_g > 1) g_calls_union.fetch_add(1); else g_calls_per_token.fetch_add(1);
+  if (fell_back) g_union_fallbacks.fetch_add(1);
+  return QSA_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+qsa_status qsa_sparse_mla_prefill(const void* q, const void* kv_cache, const int32_t* indices,
+                                  const int32_t* topk_len, void* out, float* lse, int64_t n_rows,
+                                  int32_t n_heads, int32_t d_qk, int32_t d_v, int32_t topk,
+                                  float scale, int32_t union_g, int64_t n_kv_slots, void* stream) {
+  return run_mla(q, kv_cache, indices, topk_len, out, lse, n_rows, n_heads, d_qk, d_v, topk, scale,
+                 union_g, n_kv_slots, nullptr, stream);
+}
+
+qsa_status qsa_select_mla_geometry(int32_t n_heads, int32_t union_g, int32_t topk, int32_t d_qk,
+                                   int32_t d_v, int64_t n_rows, int32_t num_sms,
+                                   qsa_geometry* out) {
+  if (!out) return QSA_ERR_INVALID_ARG;
+  if (num_sms <= 0) {
+    qsa_status st = device_sms(&num_sms);
+    if (st != QSA_OK) return st;
+  }
+  qsa::MlaGeometry g{};
+  bool fb = false;
+  qsa_status st = select_mla(n_heads, union_g, topk, d_qk, d_v, n_rows, num_sms, &g, &fb);
+  if (st != QSA_OK) return st;
+  mla_to_public(g, out);
+  return QSA_OK;
+}
+
 
 qsa_status qsa_sparse_prefill(const void* q, const void* k_cache, const void* v_cache,
                               const int32_t* indices, const int32_t* topk_len, void* out, float* lse,

@@ -106,10 +106,78 @@ __host__ __device__ inline SmemLayout smem_layout(int np, int stages, int slot_c
   return L;
 }
 
+// ---------------------------------------------------------------------------- MLA shape
+// One latent KV row per slot: d_qk = 512 latent + 64 rope dims, V = the latent dims of the same
+// row, one KV head shared by every query head.
+constexpr int kMlaDqk = 576;
+constexpr int kMlaDv = 512;
+constexpr int kMlaPairs = kMlaDv / 128;            // 32 KiB latent pieces per tile (128 dims)
+constexpr int kMlaRopeBytes = kTileTokens * 128;  // 128 slots x 64 rope dims bf16 = 16 KiB
+constexpr int kMlaMaxNPad = 32;
+
+struct MlaParams {
+  const uint16_t* q;            // bf16 bits [n_rows, n_heads, 576]
+  const int32_t* indices;       // per-token mode
+  const int32_t* topk_len;      // nullable
+  uint16_t* out;                // bf16 bits [n_rows, n_heads, 512]
+  float* lse;                   // nullable
+  const int32_t* union_idx;     // union mode: [n_groups, union_g * topk]
+  const uint8_t* union_bits;
+  const int32_t* union_len;
+  int32_t* status;              // device status word (0x100 | wait site on a timeout)
+  int64_t n_rows;
+  int64_t n_items;
+  int64_t n_kv_slots;           // 0 = unchecked
+  int32_t n_heads;
+  int32_t topk;
+  int32_t union_g;
+  int32_t n_groups;
+  int32_t head_chunks, chunk_cols;
+  int32_t pair_stages;          // latent ring depth (4 or 5)
+  int32_t slot_cap;
+  int32_t pad_row;
+  int32_t tmem_cols;
+  float scale_log2;
+  PagedAddr pa;                 // page_table == nullptr = physical slots
+};
+
+struct MlaSmemLayout {
+  int pairs, rope, qbuf, pbuf, slots, bars, misc, total;
+  int q_bytes, p_bytes;
+};
+__host__ __device__ inline MlaSmemLayout mla_smem_layout(int np, int pair_stages, int slot_cap) {
+  MlaSmemLayout L;
+  L.q_bytes = np * kMlaDqk * 2;
+  L.p_bytes = np * 256;
+  L.pairs = 0;
+  L.rope = pair_stages * kStageBytes;
+  L.qbuf = L.rope + kMlaRopeBytes;
+  L.pbuf = L.qbuf + L.q_bytes;
+  L.slots = L.pbuf + 2 * L.p_bytes;
+  L.bars = L.slots + 2 * slot_cap * 4;
+  // pair full/empty[stages], rope full/empty, s_full[2], s_free[2], p_full[2], pv_done[2],
+  // item_full[2], item_empty[2], q_empty, q_full, final
+  L.misc = L.bars + (2 * pair_stages + 2 + 15) * 8;
+  const int misc_bytes = 2 * 8 * 4 + 2 * 4 * np * 4 + 32;
+  L.total = L.misc + misc_bytes + 1024;
+  return L;
+}
+
+struct MlaGeometry {
+  int np, cols, head_chunks, chunk_cols, union_g, pair_stages, grid, smem_bytes, tmem_cols;
+  int slot_cap, n_groups;
+  int64_t n_items;
+};
+
+cudaError_t launch_mla(const MlaParams& p, const MlaGeometry& g, const void* kv_cache,
+                       int64_t tmap_rows, cudaStream_t stream);
+// Device address of the attention kernels' status word (prefill.cu), for kernels in other units.
+cudaError_t device_status_address(int32_t** addr);
+
 // Host launchers (prefill.cu / union.cu).  Return cudaSuccess or the launch error.
-// TMA map over a KV cache viewed as [rows, 256] bf16 (row = slot x kv_heads + kv_head),
-// box 64 x 1 with 128-byte swizzle: the gather4 source of the attention kernel and the probe.
-cudaError_t make_cache_map(CUtensorMap* m, const void* cache, int64_t rows);
+// TMA map over a KV cache viewed as [rows, row_elems] bf16 (row = slot x kv_heads + kv_head),
+// box 64 x 1 with 128-byte swizzle: the gather4 source of the attention kernels and the probe.
+cudaError_t make_cache_map(CUtensorMap* m, const void* cache, int64_t rows, int row_elems);
 cudaError_t launch_prefill(const PrefillParams& p, const Geometry& g, const void* k_cache,
                            const void* v_cache, int64_t tmap_rows, cudaStream_t stream);
 cudaError_t launch_union_build(const int32_t* indices, const int32_t* topk_len, int64_t n_rows,

@@ -42,7 +42,7 @@
 #include <mutex>
 
 #include "internal.h"
-#include "paged.cuh"
+#include "compact.cuh"
 #include "ptx.cuh"
 
 namespace qsa {
@@ -266,50 +266,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (p.topk_len) Lr = min(max(p.topk_len[row0], 0), p.topk);
         int32_t* const sl = reinterpret_cast<int32_t*>(gbase + L.slots) + b * slot_cap;
         const uint32_t sl_u32 = base + L.slots + b * slot_cap * 4;
-        const int32_t* src = p.indices + static_cast<int64_t>(row0) * p.topk;
-        for (int j = lane; j < Lr; j += 32) cp_async_4(sl_u32 + 4 * j, src + j);
-        cp_async_commit_wait_all();
-        __syncwarp();
-        int32_t n = 0;
-        if (p.pa.page_table == nullptr) {
-          for (int j0 = 0; j0 < Lr; j0 += 32) {
-            const int j = j0 + lane;
-            const int32_t x = j < Lr ? sl[j] : -1;
-            bool valid = x >= 0 && (p.n_kv_slots == 0 || x < p.n_kv_slots);
-            const int64_t y = static_cast<int64_t>(x) * p.n_kvheads + kvh;
-            valid = valid && y < static_cast<int64_t>(p.pad_row);
-            const uint32_t m = __ballot_sync(0xffffffffu, valid);
-            if (valid) sl[n + __popc(m & ((1u << lane) - 1u))] = static_cast<int32_t>(y);
-            n += __popc(m);
-            __syncwarp();
-          }
-        } else {
-          // Logical positions of the row's request -> physical slots through the page table.
-          // Eight page-table loads per lane are in flight at once; every lane has read its
-          // positions of a 256-slot block before the first ballot, so compacting in place
-          // never overwrites an unread entry.
-          const int32_t req = paged_request_of_row(p.pa, row0, lane);
-          const int32_t kvl = paged_kv_len(p.pa, req);
-          for (int j0 = 0; j0 < Lr; j0 += 256) {
-            int64_t ps[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int j = j0 + 32 * u + lane;
-              ps[u] = paged_slot(p.pa, req, kvl, j < Lr ? sl[j] : -1);
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int64_t x = ps[u];
-              bool valid = x >= 0 && (p.n_kv_slots == 0 || x < p.n_kv_slots);
-              const int64_t y = x * p.n_kvheads + kvh;
-              valid = valid && y < static_cast<int64_t>(p.pad_row);
-              const uint32_t m = __ballot_sync(0xffffffffu, valid);
-              if (valid) sl[n + __popc(m & ((1u << lane) - 1u))] = static_cast<int32_t>(y);
-              n += __popc(m);
-            }
-            __syncwarp();
-          }
-        }
+        const int32_t n = compact_row_slots(p.indices + static_cast<int64_t>(row0) * p.topk, Lr, sl,
+                                            sl_u32, p.n_kv_slots, p.n_kvheads, kvh, p.pad_row, p.pa,
+                                            row0, lane);
         nv = n;
       } else {
         nv = p.union_len[group];
@@ -791,12 +750,13 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 }  // namespace
 
-// 2-D map over a KV cache viewed as [rows = slots x kv_heads, 256] bf16, box 64 x 1, SW128.
-cudaError_t make_cache_map(CUtensorMap* m, const void* cache, int64_t rows) {
+// 2-D map over a KV cache viewed as [rows, row_elems] bf16 (rows = slots x kv_heads), box 64 x 1,
+// 128-byte swizzle.
+cudaError_t make_cache_map(CUtensorMap* m, const void* cache, int64_t rows, int row_elems) {
   auto enc = tensor_map_encoder();
   if (!enc) return cudaErrorNotSupported;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim * 2)};
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_elems), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_elems) * 2};
   const cuuint32_t box[2] = {64, 1};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), dims,
@@ -833,9 +793,9 @@ cudaError_t launch_prefill(const PrefillParams& p, const Geometry& g, const void
                            const void* v_cache, int64_t tmap_rows, cudaStream_t stream) {
   if (g.n_items == 0) return cudaSuccess;
   CUtensorMap tk, tv;
-  cudaError_t e = make_cache_map(&tk, k_cache, tmap_rows);
+  cudaError_t e = make_cache_map(&tk, k_cache, tmap_rows, kHeadDim);
   if (e != cudaSuccess) return e;
-  e = make_cache_map(&tv, v_cache, tmap_rows);
+  e = make_cache_map(&tv, v_cache, tmap_rows, kHeadDim);
   if (e != cudaSuccess) return e;
   const bool u = p.union_g > 1;
   switch (g.np) {
@@ -845,6 +805,13 @@ cudaError_t launch_prefill(const PrefillParams& p, const Geometry& g, const void
     case 64: return u ? launch_np<64, true>(tk, tv, p, g, stream) : launch_np<64, false>(tk, tv, p, g, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t device_status_address(int32_t** addr) {
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_device_status);
+  *addr = static_cast<int32_t*>(p);
+  return e;
 }
 
 cudaError_t read_and_clear_device_status(cudaStream_t stream, int32_t* status) {

@@ -125,7 +125,7 @@ extern "C" qsa_status qsa_probe_gather_ceiling(const void* cache, int64_t n_rows
     return QSA_ERR_CUDA;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
   CUtensorMap tm;
-  if (qsa::make_cache_map(&tm, cache, n_rows) != cudaSuccess) return QSA_ERR_CUDA;
+  if (qsa::make_cache_map(&tm, cache, n_rows, qsa::kHeadDim) != cudaSuccess) return QSA_ERR_CUDA;
   const int smem = qsa::kProbeStages * qsa::kStageBytes + 16 * qsa::kProbeStages + 1024;
   if (cudaFuncSetAttribute(qsa::gather_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            smem) != cudaSuccess)

@@ -190,6 +190,28 @@ def make_union(seed: int = 3, n_rows: int = 8192, topk: int = 2048) -> Workload:
     return Workload("union_8k", q, k, v, idx, None, 1.0 / 16.0, pos)
 
 
+MLA_DQK, MLA_DV = 576, 512
+
+
+def make_mla(seed: int = 5, n_rows: int = 8192, topk: int = 2048, n_heads: int = 8,
+             name: str = "mla_8k", indices: str = "walk") -> Workload:
+    """MLA-shaped prefill of n_rows tokens from position 0: n_heads query heads of 576 dims over
+    one latent KV row per token (576 dims as key, the first 512 as value), topk 2048.  Indices:
+    "walk" = the calibrated random walk of the union workload, "uniform" = distinct uniform
+    positions of each row's causal prefix.  k holds the latent rows as [S, 1, 576] and v is the
+    view of their first 512 dims; scale = 1/sqrt(576)."""
+    rng = np.random.default_rng(seed)
+    pos = np.arange(n_rows)
+    q = randn_bf16(rng, (n_rows, n_heads, MLA_DQK))
+    kv = randn_bf16(rng, (n_rows, 1, MLA_DQK))
+    if indices == "walk":
+        idx = random_walk_indices(rng, n_rows, topk)
+    else:
+        idx = causal_uniform_indices(rng, pos, topk)
+    return Workload(name, q, kv, kv[:, :, :MLA_DV], idx, None, 1.0 / 24.0, pos,
+                    dict(mla=True, d_v=MLA_DV))
+
+
 def make_mixed(seed: int = 4, new_tokens=(512, 2048, 4096, 8192),
                prefixes=(0, 16384, 32768, 65536), page_size: int = 64,
                n_qheads: int = 6, n_kvheads: int = 1, topk: int = 2051) -> Workload:
@@ -253,6 +275,9 @@ CONFIGS = {
     "group12_128k_12q1kv": lambda seed=2: make_group12(seed, n_qheads=12, n_kvheads=1),
     "union_8k": make_union,
     "mixed_paged": make_mixed,
+    "mla_8k": make_mla,
+    "mla_4k": lambda seed=6: make_mla(seed, n_rows=4096, name="mla_4k"),
+    "mla_2k": lambda seed=7: make_mla(seed, n_rows=2048, name="mla_2k"),
 }
 
 
