@@ -477,6 +477,68 @@ def run_reference(args, rank, world):
     }
 
 
+def run_page_split(args):
+    """The touched-page re-layout of a decode step (qsa_split_touched_pages: mark + masked split)
+    on a 4096-page pool of 256-token pages, against the full split of the same pool.  Time per
+    call with CUDA events; the L2 is flushed before every timed call."""
+    import torch
+    from top_sparse_attention_row_gb300 import binding, build as _build, workloads as W
+    _build.build()
+    binding.load_library()
+    dev = torch.device("cuda", 0)
+    w = W.make_page_split()
+    n, sps, dps, secs = w["n_src_pages"], w["src_page_size"], w["dst_page_size"], w["section_bytes"]
+    src = torch.from_numpy(w["pool"]).to(dev)
+    dst = torch.empty_like(src)
+    idx = torch.from_numpy(w["indices"]).to(dev)
+    mark = torch.empty(n, dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(args.steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    c0 = binding.counters()["kernel_launches"]
+    sampler = ClockSampler(0)
+    masked_ms = timed(lambda: binding.split_touched_pages(idx, src, dst, mark, n, sps, dps, secs,
+                                                          stream=stream))
+    clocks = sampler.stop()
+    launches = (binding.counters()["kernel_launches"] - c0) // (args.steps + args.warmup)
+    full_ms = timed(lambda: binding.page_split(src, dst, n, sps, dps, secs, stream=stream))
+    touched = int(mark.sum().item())
+    page_bytes = sps * sum(secs)
+    useful = 2 * touched * page_bytes + idx.numel() * 4 + n          # touched pages r+w, indices, mark
+    peaks, peak_src = load_peaks()
+    hbm = peaks["hbm_gbs"]
+    return {
+        "metric": "touched-page split time per decode step", "value": masked_ms, "unit": "ms",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": masked_ms,
+        "higher_is_better": False, "dtype": "u8", "data": "synthetic (seeded)",
+        "config": {"workload": f"{n} pages of {sps} tokens x {sum(secs)} B ({secs}), split to pages of "
+                               f"{dps}; 8 requests x 512-token windows", "name": "swa_page_split",
+                   "touched_pages": touched, "l2": "flushed before every timed call"},
+        "full_split_ms": full_ms,
+        "roofline": {"bound": "hbm", "kernel": "page_split_kernel (full split)",
+                     "achieved": 2 * n * page_bytes / (full_ms * 1e-3) / 1e9, "peak": hbm,
+                     "unit": "GB/s", "frac": 2 * n * page_bytes / (full_ms * 1e-3) / 1e9 / hbm,
+                     "peak_source": peak_src, "traffic": None},
+        "masked_useful_gbs": useful / (masked_ms * 1e-3) / 1e9,
+        "gpu_launches": launches, "clocks": clocks,
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -507,7 +569,10 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-    line = run_gpu(args, rank, world, local_rank)
+    if args.config == "swa_page_split":
+        line = run_page_split(args) if rank == 0 else None
+    else:
+        line = run_gpu(args, rank, world, local_rank)
     if line is not None:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -169,6 +169,36 @@ qsa_status qsa_select_mla_geometry(int32_t n_heads, int32_t union_g, int32_t top
                                    int32_t d_v, int64_t n_rows, int32_t num_sms,
                                    qsa_geometry* out);
 
+/* Touched-page mark and masked page split ("[SM120] Only split touched SWA pages in FlashMLA
+ * page-split kernel", Modifications): re-lay a KV pool from src_page_size-token pages to
+ * dst_page_size-token pages, copying only the pages that a step's sparse indices reference.
+ * Page layout (both pools): a page of P tokens holds n_sections sections one after another,
+ * section k being P x section_bytes[k] bytes, token-major.  Destination page p * ratio + i
+ * (ratio = src_page_size / dst_page_size) holds tokens i * dst_page_size ..
+ * (i + 1) * dst_page_size - 1 of source page p, section by section.
+ *   qsa_page_mark: mark [n_src_pages] uint8 (device, caller-owned) is zeroed, then
+ *     mark[t / src_page_size] = 1 for every index t >= 0 of indices [n_indices] (int32 token
+ *     slots of the source pool; slots past the pool are ignored).  No atomics, no host read.
+ *   qsa_page_split: copies every destination page whose source page is marked (mark NULL =
+ *     every page).  Destination pages of unmarked source pages are left untouched.  The launch
+ *     grid is n_src_pages * ratio CTAs whatever the mark holds, so a captured CUDA graph
+ *     replays it; an unmarked page costs one byte load.
+ *   qsa_split_touched_pages: mark + masked split in one call.
+ * Requirements: src_pool and dst_pool 16-byte aligned (host pointer section_bytes, each entry a
+ * positive multiple of 16, 1 <= n_sections <= 8), src_page_size a multiple of dst_page_size,
+ * n_src_pages * ratio < 2^31.  Errors: QSA_ERR_INVALID_ARG / QSA_ERR_UNSUPPORTED before any
+ * GPU work. */
+qsa_status qsa_page_mark(const int32_t* indices, int64_t n_indices, int32_t src_page_size,
+                         int64_t n_src_pages, uint8_t* mark, void* stream);
+qsa_status qsa_page_split(const void* src_pool, void* dst_pool, const uint8_t* mark,
+                          int64_t n_src_pages, int32_t src_page_size, int32_t dst_page_size,
+                          int32_t n_sections, const int32_t* section_bytes, void* stream);
+qsa_status qsa_split_touched_pages(const int32_t* indices, int64_t n_indices, const void* src_pool,
+                                   void* dst_pool, uint8_t* mark, int64_t n_src_pages,
+                                   int32_t src_page_size, int32_t dst_page_size,
+                                   int32_t n_sections, const int32_t* section_bytes,
+                                   void* stream);
+
 /* Allocation-free variant of qsa_sparse_prefill (same arguments, same results).  The pages
  * have no counterpart: it exists for callers that must not allocate device memory -- code
  * whose GPU memory is owned entirely by a framework's pool, latency-critical loops where an

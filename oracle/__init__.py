@@ -35,6 +35,10 @@ Functions and the passages they follow:
 * ``mla.sparse_mla_prefill`` -- the MLA shape: one latent row per slot whose
   576 dims are the key and whose first 512 dims are the value, shared by every
   head ("DSA prefill ... triton_sparse_mla", Motivation and Speed Tests).
+* ``pages.page_mark`` / ``pages.page_split`` -- the touched-page mark and the
+  masked page split of "[SM120] Only split touched SWA pages in FlashMLA
+  page-split kernel" (Modifications; the masked split equals the full split on
+  every touched page and leaves the rest stale).
 
 Every function is pinned by ``tests/test_oracle_pins.py`` against facts that
 do not come from this package: dense causal attention from a library routine
@@ -47,3 +51,4 @@ from .union import sorted_rows, union_build, union_attention  # noqa: F401
 from .paged import (sparse_prefill_paged, sparse_prefill_paged_rows,  # noqa: F401
                     physical_indices, request_of_rows)
 from .mla import sparse_mla_prefill, sparse_mla_prefill_rows  # noqa: F401
+from .pages import page_mark, page_split  # noqa: F401

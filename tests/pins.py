@@ -534,3 +534,64 @@ def check_mla_vs_padded_gqa(fn):
 
 
 MLA_CHECKS = [check_mla_dense, check_mla_vs_padded_gqa]
+
+
+# ----------------------------------------------------------------------------- page split
+
+def page_pool_case(seed, n_pages=6, src_ps=8, sections=(32, 16, 48)):
+    """A source pool built from per-(page, token, section) byte blocks with array reshapes, and
+    the expected destination for each split ratio built the same way (no per-token offsets)."""
+    rng = _rng(seed)
+    blocks = [rng.integers(0, 256, size=(n_pages, src_ps, sb), dtype=np.uint8) for sb in sections]
+    # page p = concatenation over sections of blocks[k][p] flattened (token-major)
+    src = np.concatenate([np.concatenate([b[p].reshape(-1) for b in blocks]) for p in range(n_pages)])
+
+    def expected(dst_ps):
+        ratio = src_ps // dst_ps
+        pages = []
+        for p in range(n_pages):
+            for i in range(ratio):
+                pages.append(np.concatenate([b[p, i * dst_ps:(i + 1) * dst_ps].reshape(-1)
+                                             for b in blocks]))
+        return np.concatenate(pages)
+    return src, expected, list(sections)
+
+
+def check_page_split(split):
+    """split(src, dst, n_pages, src_ps, dst_ps, sections, mark) -> new dst (flat uint8)."""
+    fails = []
+    src, expected, secs = page_pool_case(500)
+    for dst_ps in (8, 4, 2, 1):
+        got = split(src, np.zeros_like(src), 6, 8, dst_ps, secs, None)
+        if not np.array_equal(got, expected(dst_ps)):
+            fails.append(f"full split to pages of {dst_ps}")
+    # masked: touched pages equal the full split, the others keep their stale bytes
+    stale = _rng(501).integers(0, 256, size=src.size, dtype=np.uint8)
+    mark = np.array([0, 1, 0, 0, 1, 1], dtype=np.uint8)
+    got = split(src, stale, 6, 8, 2, secs, mark)
+    full = expected(2)
+    pb = 8 * sum(secs)                         # page bytes are the same for both page sizes x ratio
+    for p in range(6):
+        want = full[p * pb:(p + 1) * pb] if mark[p] else stale[p * pb:(p + 1) * pb]
+        if not np.array_equal(got[p * pb:(p + 1) * pb], want):
+            fails.append(f"masked split, source page {p} (marked={bool(mark[p])})")
+    return fails
+
+
+def check_page_mark(mark_fn):
+    """mark_fn(indices, src_ps, n_pages) -> uint8 [n_pages]; against the set of pages of the
+    valid indices (padding and slots past the pool ignored)."""
+    rng = _rng(510)
+    idx = rng.integers(-3, 9 * 16 + 20, size=(5, 23))
+    got = mark_fn(idx, 16, 9)
+    want = np.zeros(9, dtype=np.uint8)
+    for page in {int(t) // 16 for t in idx.reshape(-1) if 0 <= t < 9 * 16}:
+        want[page] = 1
+    fails = [] if np.array_equal(got, want) else ["page mark != set of touched pages"]
+    # hand-chosen page boundaries: 15 -> page 0, 16 -> 1, 47 -> 2, 100 -> 6, 143 -> 8, 200 past
+    got = mark_fn(np.array([[15, 16, -1, 47], [100, 143, -2, 200]]), 16, 9)
+    if not np.array_equal(got, np.array([1, 1, 1, 0, 0, 0, 1, 0, 1], dtype=np.uint8)):
+        fails.append("page boundaries")
+    if mark_fn(np.full((2, 3), -1), 16, 9).any():
+        fails.append("padding marked a page")
+    return fails

@@ -159,3 +159,27 @@ def test_mla_selector(lib):
     assert f(fake, fake + 8, fake, None, fake, None, 10, 8, 576, 512, 2048, 0.04, 0, 0, None) == 1
     assert f(fake, fake, fake, None, fake, None, 10, 8, 576, 256, 2048, 0.04, 0, 0, None) == 2
     assert f(fake, fake, fake, None, fake, None, 0, 8, 576, 512, 2048, 0.04, 0, 0, None) == 0
+
+
+def test_page_split_validation(lib):
+    """Page mark / split argument errors come back before any GPU work."""
+    fake = 1 << 20
+    secs = (ctypes.c_int32 * 3)(512, 16, 128)
+    bad = (ctypes.c_int32 * 2)(512, 8)                     # not a multiple of 16
+    sp = lib.qsa_page_split
+    assert sp(None, fake, None, 10, 256, 64, 3, secs, None) == 1
+    assert sp(fake, fake, None, 10, 256, 96, 3, secs, None) == 1          # 256 % 96 != 0
+    assert sp(fake, fake, None, 10, 256, 64, 2, bad, None) == 1
+    assert sp(fake, fake, None, 10, 256, 64, 0, secs, None) == 1
+    assert sp(fake, fake, None, 10, 256, 64, 9, secs, None) == 1
+    assert sp(fake + 4, fake, None, 10, 256, 64, 3, secs, None) == 1
+    assert sp(fake, fake, None, 1 << 30, 256, 64, 3, secs, None) == 2     # grid past 2^31
+    assert sp(fake, fake, None, 0, 256, 64, 3, secs, None) == 0
+    pm = lib.qsa_page_mark
+    assert pm(fake, 10, 256, 10, None, None) == 1
+    assert pm(None, 10, 256, 10, fake, None) == 1
+    assert pm(fake, 10, 0, 10, fake, None) == 1
+    assert pm(fake, 10, 256, 0, fake, None) == 0
+    st = lib.qsa_split_touched_pages
+    assert st(fake, 10, fake, fake, None, 10, 256, 64, 3, secs, None) == 1
+    assert st(fake, 10, fake, fake, fake, 10, 256, 48, 3, secs, None) == 1

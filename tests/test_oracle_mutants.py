@@ -176,3 +176,46 @@ def test_mla_unmutated_copy_passes():
 @pytest.mark.parametrize("kind", ["key_drops_rope", "value_from_tail", "head_zero_for_all"])
 def test_mla_mutant_is_caught(kind):
     assert [f for c in pins.MLA_CHECKS for f in c(_mla_mutant(kind))], f"mutant {kind} passed"
+
+
+def _split_mutant(kind):
+    def split(src, dst, n_pages, src_ps, dst_ps, secs, mark):
+        ratio = src_ps // dst_ps
+        out = np.array(dst, copy=True)
+        dpb = dst_ps * sum(secs)
+        for p in range(n_pages):
+            if mark is not None and not mark[p]:
+                continue
+            for i in range(ratio):
+                q = p * ratio + i
+                ii = ratio - 1 - i if kind == "sub_page_reversed" else i
+                order = list(range(len(secs)))
+                if kind == "sections_swapped":
+                    order = order[::-1]
+                off = q * dpb
+                for k in order:
+                    sb = secs[k]
+                    soff = p * src_ps * sum(secs) + src_ps * sum(secs[:k]) + ii * dst_ps * sb
+                    out[off:off + dst_ps * sb] = src[soff:soff + dst_ps * sb]
+                    off += dst_ps * sb
+        return out
+    return split
+
+
+@pytest.mark.parametrize("kind", ["sub_page_reversed", "sections_swapped"])
+def test_page_split_mutant_is_caught(kind):
+    assert pins.check_page_split(_split_mutant(kind))
+
+
+def test_page_split_unmutated_copy_passes():
+    assert pins.check_page_split(_split_mutant("none")) == []
+
+
+def test_page_mark_mutant_is_caught():
+    def mark(idx, ps, n):                       # off by one: page (t + 1) // ps
+        m = np.zeros(n, dtype=np.uint8)
+        for t in np.asarray(idx).reshape(-1):
+            if t >= 0 and (t + 1) // ps < n:
+                m[(t + 1) // ps] = 1
+        return m
+    assert pins.check_page_mark(mark)

@@ -74,3 +74,12 @@ def test_paged_pin(check):
 def test_mla_pin(check):
     fn = lambda q, kv, idx, tl, scale, d_v: oracle.sparse_mla_prefill(q, kv, idx, tl, scale, d_v)
     assert check(fn) == []
+
+
+def test_page_split_pin():
+    fn = lambda src, dst, n, sps, dps, secs, mark: oracle.page_split(src, dst, n, sps, dps, secs, mark)
+    assert pins.check_page_split(fn) == []
+
+
+def test_page_mark_pin():
+    assert pins.check_page_mark(oracle.page_mark) == []

@@ -23,7 +23,8 @@ EXPORTED = ["qsa_sparse_prefill", "qsa_sparse_prefill_ex", "qsa_workspace_bytes"
             "qsa_union_build", "qsa_select_geometry", "qsa_get_counters", "qsa_reset_counters",
             "qsa_status_string", "qsa_version", "qsa_get_device_status",
             "qsa_sparse_prefill_noalloc", "qsa_probe_gather_ceiling",
-            "qsa_sparse_prefill_paged", "qsa_sparse_mla_prefill", "qsa_select_mla_geometry"]
+            "qsa_sparse_prefill_paged", "qsa_sparse_mla_prefill", "qsa_select_mla_geometry",
+            "qsa_page_mark", "qsa_page_split", "qsa_split_touched_pages"]
 
 # Size of the library-owned scratch array used by qsa_sparse_prefill_noalloc (include/qsa.h).
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -79,6 +80,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qsa_sparse_mla_prefill.restype = ctypes.c_int
     lib.qsa_select_mla_geometry.argtypes = [i32, i32, i32, i32, i32, i64, i32, ctypes.POINTER(Geometry)]
     lib.qsa_select_mla_geometry.restype = ctypes.c_int
+    lib.qsa_page_mark.argtypes = [vp, i64, i32, i64, vp, vp]
+    lib.qsa_page_mark.restype = ctypes.c_int
+    lib.qsa_page_split.argtypes = [vp, vp, vp, i64, i32, i32, i32, vp, vp]
+    lib.qsa_page_split.restype = ctypes.c_int
+    lib.qsa_split_touched_pages.argtypes = [vp, i64, vp, vp, vp, i64, i32, i32, i32, vp, vp]
+    lib.qsa_split_touched_pages.restype = ctypes.c_int
     lib.qsa_probe_gather_ceiling.argtypes = [vp, i64, vp, i64, i32, i32, ctypes.POINTER(f32), vp]
     lib.qsa_probe_gather_ceiling.restype = ctypes.c_int
     lib.qsa_workspace_bytes.argtypes = [i64, i32, i32]
@@ -257,6 +264,46 @@ def select_mla_geometry(n_heads, union_g, topk, n_rows, num_sms=0, d_qk=576, d_v
                                                 ctypes.byref(g))
     _check(st, "qsa_select_mla_geometry")
     return g.as_dict()
+
+
+def _sections(section_bytes):
+    arr = (ctypes.c_int32 * len(section_bytes))(*[int(b) for b in section_bytes])
+    return arr, len(section_bytes)
+
+
+def page_mark(indices, src_page_size: int, n_src_pages: int, *, mark=None, stream=None):
+    """qsa_page_mark: uint8 [n_src_pages] (zeroed, then 1 on every page a valid index touches)."""
+    import torch
+    _require(indices, torch.int32, "indices", None)
+    if mark is None:
+        mark = torch.empty(n_src_pages, dtype=torch.uint8, device=indices.device)
+    st = load_library().qsa_page_mark(_ptr(indices), indices.numel(), int(src_page_size),
+                                      int(n_src_pages), _ptr(mark), _stream_ptr(stream))
+    _check(st, "qsa_page_mark")
+    return mark
+
+
+def page_split(src_pool, dst_pool, n_src_pages: int, src_page_size: int, dst_page_size: int,
+               section_bytes, *, mark=None, stream=None):
+    """qsa_page_split over flat uint8 pools; mark None = every page."""
+    arr, n = _sections(section_bytes)
+    st = load_library().qsa_page_split(_ptr(src_pool), _ptr(dst_pool), _ptr(mark), int(n_src_pages),
+                                       int(src_page_size), int(dst_page_size), n, arr,
+                                       _stream_ptr(stream))
+    _check(st, "qsa_page_split")
+    return dst_pool
+
+
+def split_touched_pages(indices, src_pool, dst_pool, mark, n_src_pages: int, src_page_size: int,
+                        dst_page_size: int, section_bytes, *, stream=None):
+    """qsa_split_touched_pages: page mark + masked split in one call."""
+    arr, n = _sections(section_bytes)
+    st = load_library().qsa_split_touched_pages(_ptr(indices), indices.numel(), _ptr(src_pool),
+                                                _ptr(dst_pool), _ptr(mark), int(n_src_pages),
+                                                int(src_page_size), int(dst_page_size), n, arr,
+                                                _stream_ptr(stream))
+    _check(st, "qsa_split_touched_pages")
+    return dst_pool
 
 
 def sparse_prefill_noalloc(q, k_cache, v_cache, indices, topk_len, scale: float, *, out=None,

@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libqsa.so")
-SOURCES = ["prefill.cu", "mla.cu", "union.cu", "api.cpp", "noalloc.cu", "probe.cu"]
+SOURCES = ["prefill.cu", "mla.cu", "union.cu", "api.cpp", "noalloc.cu", "probe.cu", "pages.cu"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]

@@ -398,6 +398,24 @@ qsa_status run_mla(const void* q, const void* kv_cache, const int32_t* indices,
   return QSA_OK;
 }
 
+qsa_status page_split_args(const void* src_pool, void* dst_pool, int64_t n_src_pages,
+                           int32_t src_page_size, int32_t dst_page_size, int32_t n_sections,
+                           const int32_t* section_bytes, qsa::PageSections* sec) {
+  if (!src_pool || !dst_pool || !section_bytes || n_src_pages < 0 || src_page_size < 1 ||
+      dst_page_size < 1 || src_page_size % dst_page_size != 0 || n_sections < 1 ||
+      n_sections > qsa::kMaxPageSections || !aligned16(src_pool) || !aligned16(dst_pool))
+    return QSA_ERR_INVALID_ARG;
+  sec->n = n_sections;
+  sec->token_bytes = 0;
+  for (int k = 0; k < n_sections; ++k) {
+    if (section_bytes[k] <= 0 || section_bytes[k] % 16 != 0) return QSA_ERR_INVALID_ARG;
+    sec->bytes[k] = section_bytes[k];
+    sec->token_bytes += section_bytes[k];
+  }
+  if (n_src_pages * (src_page_size / dst_page_size) >= INT32_MAX) return QSA_ERR_UNSUPPORTED;
+  return QSA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -408,6 +426,58 @@ qsa_status qsa_sparse_mla_prefill(const void* q, const void* kv_cache, const int
                                   float scale, int32_t union_g, int64_t n_kv_slots, void* stream) {
   return run_mla(q, kv_cache, indices, topk_len, out, lse, n_rows, n_heads, d_qk, d_v, topk, scale,
                  union_g, n_kv_slots, nullptr, stream);
+}
+
+qsa_status qsa_page_mark(const int32_t* indices, int64_t n_indices, int32_t src_page_size,
+                         int64_t n_src_pages, uint8_t* mark, void* stream) {
+  if (!mark || (!indices && n_indices > 0) || n_indices < 0 || src_page_size < 1 || n_src_pages < 0)
+    return QSA_ERR_INVALID_ARG;
+  if (n_src_pages == 0) return QSA_OK;
+  int32_t sms = 0;
+  qsa_status st = device_sms(&sms);
+  if (st != QSA_OK) return st;
+  if (qsa::launch_page_mark(indices, n_indices, src_page_size, n_src_pages, mark, sms,
+                            static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return QSA_ERR_CUDA;
+  if (n_indices > 0) g_launches.fetch_add(1);
+  return QSA_OK;
+}
+
+
+qsa_status qsa_page_split(const void* src_pool, void* dst_pool, const uint8_t* mark,
+                          int64_t n_src_pages, int32_t src_page_size, int32_t dst_page_size,
+                          int32_t n_sections, const int32_t* section_bytes, void* stream) {
+  qsa::PageSections sec{};
+  qsa_status st = page_split_args(src_pool, dst_pool, n_src_pages, src_page_size, dst_page_size,
+                                  n_sections, section_bytes, &sec);
+  if (st != QSA_OK || n_src_pages == 0) return st;
+  int32_t sms = 0;
+  st = device_sms(&sms);
+  if (st != QSA_OK) return st;
+  if (qsa::launch_page_split(src_pool, dst_pool, mark, n_src_pages, src_page_size, dst_page_size,
+                             sec, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return QSA_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return QSA_OK;
+}
+
+qsa_status qsa_split_touched_pages(const int32_t* indices, int64_t n_indices, const void* src_pool,
+                                   void* dst_pool, uint8_t* mark, int64_t n_src_pages,
+                                   int32_t src_page_size, int32_t dst_page_size,
+                                   int32_t n_sections, const int32_t* section_bytes,
+                                   void* stream) {
+  qsa::PageSections sec{};
+  qsa_status st = page_split_args(src_pool, dst_pool, n_src_pages, src_page_size, dst_page_size,
+                                  n_sections, section_bytes, &sec);
+  if (st != QSA_OK) return st;
+  if (!mark || (!indices && n_indices > 0) || n_indices < 0) return QSA_ERR_INVALID_ARG;
+  st = qsa_page_mark(indices, n_indices, src_page_size, n_src_pages, mark, stream);
+  if (st != QSA_OK || n_src_pages == 0) return st;
+  if (qsa::launch_page_split(src_pool, dst_pool, mark, n_src_pages, src_page_size, dst_page_size,
+                             sec, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return QSA_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return QSA_OK;
 }
 
 qsa_status qsa_select_mla_geometry(int32_t n_heads, int32_t union_g, int32_t topk, int32_t d_qk,

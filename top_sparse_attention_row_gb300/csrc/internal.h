@@ -171,6 +171,19 @@ struct MlaGeometry {
 
 cudaError_t launch_mla(const MlaParams& p, const MlaGeometry& g, const void* kv_cache,
                        int64_t tmap_rows, cudaStream_t stream);
+// ---------------------------------------------------------------------------- page split
+constexpr int kMaxPageSections = 8;
+struct PageSections {          // per-token byte widths of a page's sections, in page order
+  int32_t n;
+  int32_t bytes[kMaxPageSections];
+  int64_t token_bytes;         // sum of bytes[]
+};
+cudaError_t launch_page_mark(const int32_t* indices, int64_t n_indices, int32_t src_page_size,
+                             int64_t n_src_pages, uint8_t* mark, int num_sms, cudaStream_t stream);
+cudaError_t launch_page_split(const void* src, void* dst, const uint8_t* mark, int64_t n_src_pages,
+                              int32_t src_page_size, int32_t dst_page_size,
+                              const PageSections& sec, cudaStream_t stream);
+
 // Device address of the attention kernels' status word (prefill.cu), for kernels in other units.
 cudaError_t device_status_address(int32_t** addr);
 

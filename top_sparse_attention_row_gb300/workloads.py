@@ -268,6 +268,30 @@ def make_mixed(seed: int = 4, new_tokens=(512, 2048, 4096, 8192),
     return Workload("mixed_paged", q, k, v, idx, tlen, 1.0 / 16.0, pos, meta)
 
 
+def make_page_split(seed: int = 8, n_src_pages: int = 4096, src_page_size: int = 256,
+                    dst_page_size: int = 64, batch: int = 8, window: int = 512,
+                    section_bytes=(512, 16, 128)) -> dict:
+    """A decode step's page re-layout: a pool of n_src_pages pages of src_page_size tokens, each
+    token 656 bytes in three sections (512 fp8 latent bytes, 16 bytes of scales, 128 bytes of
+    bf16 rope), split to pages of dst_page_size.  Each of `batch` requests owns a random set of
+    physical pages; its decode row selects the last `window` tokens of its context, so about
+    two source pages per request are touched.  Returns the pool bytes (uint8, flat), indices
+    [batch, window] int32 source slots and the shape."""
+    rng = np.random.default_rng(seed)
+    token_bytes = int(sum(section_bytes))
+    pool = rng.integers(0, 256, size=n_src_pages * src_page_size * token_bytes, dtype=np.uint8)
+    perm = rng.permutation(n_src_pages)
+    pages_per_req = n_src_pages // batch
+    idx = np.empty((batch, window), dtype=np.int32)
+    for b in range(batch):
+        pages = perm[b * pages_per_req:(b + 1) * pages_per_req]
+        ctx = int(rng.integers(window, pages_per_req * src_page_size))
+        logical = np.arange(ctx - window, ctx)
+        idx[b] = pages[logical // src_page_size] * src_page_size + logical % src_page_size
+    return dict(pool=pool, indices=idx, n_src_pages=n_src_pages, src_page_size=src_page_size,
+                dst_page_size=dst_page_size, section_bytes=list(section_bytes))
+
+
 CONFIGS = {
     "tiny": make_tiny,
     "group6_32k": make_group6,
