@@ -84,16 +84,17 @@ def workload_stats(w):
     D, Hq, Hkv = w.head_dim, w.n_qheads, w.n_kvheads
     if w.meta.get("mla"):
         return mla_stats(w, v)
+    elem = 1 if w.meta.get("fp8") else 2                     # cache bytes per element
     flops = int(4 * Hq * D * v.sum())                       # QK^T + PV, 2 flops per MAC
     idx = w.indices
     mask = idx >= 0
     if w.topk_len is not None:
         mask &= np.arange(idx.shape[1])[None, :] < np.clip(w.topk_len, 0, idx.shape[1])[:, None]
     unique_slots = int(np.unique(idx[mask]).size)
-    kv_unique = unique_slots * Hkv * D * 2 * 2               # K and V rows, bf16
+    kv_unique = unique_slots * Hkv * D * elem * 2            # K and V rows
     io = (2 * w.n_rows * Hq * D * 2 + idx.size * 4 + w.n_rows * Hq * 4
           + (0 if w.topk_len is None else w.n_rows * 4))
-    gathered = int(v.sum()) * Hkv * D * 2 * 2                 # every (row, slot) K+V read
+    gathered = int(v.sum()) * Hkv * D * elem * 2              # every (row, slot) K+V read
     return dict(flops=flops, bytes=kv_unique + io, unique_slots=unique_slots, gathered=gathered,
                 valid_slots=int(v.sum()))
 
@@ -119,11 +120,13 @@ def mla_stats(w, v):
 _W = None
 
 
-def _oracle_init(name, seed_kw):
+def _oracle_init(name, seed_kw, fp8_page_size=0):
     os.environ.setdefault("OMP_NUM_THREADS", "1")
     global _W
     from top_sparse_attention_row_gb300 import workloads as W
     _W = W.make(name, **seed_kw)
+    if fp8_page_size:
+        _W = W.with_fp8_cache(_W, fp8_page_size)
 
 
 def _oracle_rows(rows):
@@ -132,16 +135,20 @@ def _oracle_rows(rows):
     if w.meta.get("mla"):
         oracle.sparse_mla_prefill_rows(w.q, w.k.reshape(w.k.shape[0], -1), w.indices, w.topk_len,
                                        w.scale, rows, w.meta["d_v"])
+    elif w.meta.get("fp8"):
+        m = w.meta
+        oracle.sparse_prefill_fp8_rows(w.q, m["k8"], m["v8"], m["k_scale"], m["v_scale"],
+                                       m["fp8_page_size"], w.indices, w.topk_len, w.scale, rows)
     else:
         oracle.sparse_prefill_rows(w.q, w.k, w.v, w.indices, w.topk_len, w.scale, rows)
     return len(rows)
 
 
-def oracle_pool(name, seed_kw, cores):
+def oracle_pool(name, seed_kw, cores, fp8_page_size=0):
     for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
         os.environ[var] = "1"
     ctx = mp.get_context("spawn")
-    return ctx.Pool(cores, initializer=_oracle_init, initargs=(name, seed_kw))
+    return ctx.Pool(cores, initializer=_oracle_init, initargs=(name, seed_kw, fp8_page_size))
 
 
 def time_oracle(pool, n_rows, sample_rows, cores):
@@ -223,6 +230,10 @@ def run_gpu(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     seed_kw = {} if world == 1 else {"seed": 1000 + rank}
     w = W.make(args.config, **seed_kw)
+    if args.fp8:
+        if w.meta.get("mla") or args.paged:
+            raise SystemExit("--fp8 applies to the plain d=256 workloads")
+        w = W.with_fp8_cache(w, args.fp8_page_size)
     stats = workload_stats(w)
 
     # CPU baseline pool (spawned before any GPU work of this process matters; spawn is safe).
@@ -230,7 +241,7 @@ def run_gpu(args, rank, world, local_rank):
     pool = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cores = os.cpu_count() or 1
-        pool = oracle_pool(args.config, seed_kw, cores)
+        pool = oracle_pool(args.config, seed_kw, cores, args.fp8_page_size if args.fp8 else 0)
 
     def bf(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
@@ -242,6 +253,9 @@ def run_gpu(args, rank, world, local_rank):
     if mla:   # one latent cache [S, 576]; V is its first 512 dims, not a separate tensor
         h_k = bf(w.k.reshape(w.k.shape[0], -1)).pin_memory()
         h_v = h_k[:0]
+    elif args.fp8:   # e4m3 caches; their page scales travel with the metadata below
+        h_k = torch.from_numpy(w.meta["k8"]).pin_memory()
+        h_v = torch.from_numpy(w.meta["v8"]).pin_memory()
     else:
         h_k, h_v = bf(w.k).pin_memory(), bf(w.v).pin_memory()
     paged = args.paged
@@ -251,6 +265,9 @@ def run_gpu(args, rank, world, local_rank):
     h_tl = None if w.topk_len is None else torch.from_numpy(w.topk_len).pin_memory()
     # paged calls: ragged row offsets, per-request KV lengths and the page table
     h_meta = ()
+    if args.fp8:
+        h_meta = tuple(torch.from_numpy(np.ascontiguousarray(w.meta[key], dtype=np.float32)).pin_memory()
+                       for key in ("k_scale", "v_scale"))
     if paged:
         h_meta = tuple(torch.from_numpy(np.ascontiguousarray(w.meta[key], dtype=np.int32)).pin_memory()
                        for key in ("cu_seqlens_q", "kv_lens_array", "page_table"))
@@ -272,6 +289,10 @@ def run_gpu(args, rank, world, local_rank):
         if mla:
             binding.sparse_mla_prefill(q, k, idx, tl, w.scale, out=out, lse=lse, union_g=args.union,
                                        stream=stream)
+        elif args.fp8:
+            ks, vs = d_meta
+            binding.sparse_prefill_fp8(q, k, v, ks, vs, w.meta["fp8_page_size"], idx, tl, w.scale,
+                                       out=out, lse=lse, union_g=args.union, stream=stream)
         elif paged:
             cu, kvl, pt = d_meta
             binding.sparse_prefill_paged(q, k, v, idx, tl, cu, kvl, pt, w.meta["page_size"], w.scale,
@@ -291,6 +312,8 @@ def run_gpu(args, rank, world, local_rank):
     # selected slot's first bytes)
     valid = w.indices[w.indices >= 0].astype(np.int64)
     valid = valid * w.n_kvheads if not mla else (valid * w.q.shape[2]) // 256
+    if args.fp8:   # 256-byte e4m3 rows: the 512-byte probe row holding each slot's row
+        valid = valid // 2
     n_pieces = min(len(valid) // 128, 4096)
     table = torch.from_numpy(valid[: n_pieces * 128].astype(np.int32).reshape(n_pieces, 128)).to(dev)
     k_flat = k.reshape(-1)
@@ -420,7 +443,8 @@ def run_gpu(args, rank, world, local_rank):
     line = {
         "metric": METRIC, "value": rows_total / kernel_s, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16 MMA on e4m3 KV" if args.fp8 else "bf16",
         "data": "synthetic (seeded; no dataset or weights)",
         "config": {"workload": DESCRIPTIONS.get(args.config, args.config), "name": args.config,
                    "rows": w.n_rows, "n_qheads": w.n_qheads, "n_kvheads": w.n_kvheads,
@@ -428,6 +452,9 @@ def run_gpu(args, rank, world, local_rank):
                    "valid_slots": stats["valid_slots"], "geometry": geo,
                    "indices": ("logical positions + page table, translated in the kernels "
                                "(qsa_sparse_prefill_paged)" if paged else "physical slots"),
+                   "kv_cache": (f"e4m3 with fp32 scales per {args.fp8_page_size}-slot page and KV "
+                                "head, dequantised in the gather (qsa_sparse_prefill_fp8)"
+                                if args.fp8 else "bf16"),
                    "l2": "flushed before every timed step (512 MiB memset outside the events)",
                    "parallelism": f"{world} independent shard(s), no collective"},
         "roofline": roofline,
@@ -449,7 +476,7 @@ def run_reference(args, rank, world):
     from top_sparse_attention_row_gb300 import workloads as W
     w = W.make(args.config)
     cores = os.cpu_count() or 1
-    pool = oracle_pool(args.config, {}, cores)
+    pool = oracle_pool(args.config, {}, cores, args.fp8_page_size if args.fp8 else 0)
     sample = min(w.n_rows, args.cpu_rows)
     for _ in range(args.warmup):
         time_oracle(pool, w.n_rows, max(cores, sample // 8), cores)
@@ -550,6 +577,10 @@ def main():
     ap.add_argument("--paged", action="store_true",
                     help="paged workloads: pass logical positions and the page table "
                          "(qsa_sparse_prefill_paged) instead of translated slots")
+    ap.add_argument("--fp8", action="store_true",
+                    help="d=256 workloads: e4m3 K/V caches with per-page scales "
+                         "(qsa_sparse_prefill_fp8)")
+    ap.add_argument("--fp8-page-size", type=int, default=64)
     ap.add_argument("--cpu-rows", type=int, default=8192)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -145,6 +145,26 @@ qsa_status qsa_sparse_prefill_paged(const void* q, const void* k_cache, const vo
                                     int32_t n_kvheads, int32_t head_dim, int32_t topk, float scale,
                                     int32_t union_g, void* stream);
 
+/* FP8 KV cache: K and V stored as e4m3 bytes with a fp32 scale per page and KV head, dequantised
+ * in the gather ("DSA prefill ... triton_sparse_mla", Robustness and Accuracy Tests: the Triton
+ * kernel refuses a packed FP8 pool and takes dequantised rows; flashinfer consumes the FP8 pool
+ * with its scales).  The value of cache byte x at slot s, KV head h is
+ *   e4m3(x) * k_scale[(s / page_size) * n_kvheads + h]      (v_scale likewise)
+ * and the result is that of qsa_sparse_prefill on the dequantised caches.
+ *   k_cache, v_cache [n_slots, n_kvheads, head_dim] e4m3 bytes (16-byte aligned)
+ *   k_scale, v_scale [ceil(n_slots / page_size), n_kvheads] fp32 (device)
+ * Other arguments as qsa_sparse_prefill, plus n_kv_slots as in qsa_sparse_prefill_ex.  The
+ * tensor cores run fp16 operands here: q is rounded to fp16 (|q| must stay below 65504), the
+ * e4m3 values convert to fp16 exactly, and each slot's V scale multiplies its probability.
+ * Query columns per tile are capped at 32: larger head groups run in head chunks, and unions
+ * past 32 columns fall back to the per-token path (counted). */
+qsa_status qsa_sparse_prefill_fp8(const void* q, const void* k_cache, const void* v_cache,
+                                  const float* k_scale, const float* v_scale, int32_t page_size,
+                                  const int32_t* indices, const int32_t* topk_len, void* out,
+                                  float* lse, int64_t n_rows, int32_t n_qheads, int32_t n_kvheads,
+                                  int32_t head_dim, int32_t topk, float scale, int32_t union_g,
+                                  int64_t n_kv_slots, void* stream);
+
 /* MLA-shaped sparse prefill ("DSA prefill ... triton_sparse_mla", Motivation and Speed Tests:
  * one latent KV row per token, kv_lora_rank 512 + qk_rope_head_dim 64 = 576 dims for QK^T, the
  * 512 latent dims as V, topk 2048, 8 heads at TP8, union G = 2 / 4).  Every query head attends

@@ -39,6 +39,9 @@ Functions and the passages they follow:
   masked page split of "[SM120] Only split touched SWA pages in FlashMLA
   page-split kernel" (Modifications; the masked split equals the full split on
   every touched page and leaves the rest stale).
+* ``fp8.sparse_prefill_fp8`` -- the same attention over an e4m3 KV cache with
+  one scale per page and KV head, dequantised as e4m3(x) * scale ("DSA prefill
+  ... triton_sparse_mla", Robustness and Accuracy Tests: dequantised rows).
 
 Every function is pinned by ``tests/test_oracle_pins.py`` against facts that
 do not come from this package: dense causal attention from a library routine
@@ -52,3 +55,5 @@ from .paged import (sparse_prefill_paged, sparse_prefill_paged_rows,  # noqa: F4
                     physical_indices, request_of_rows)
 from .mla import sparse_mla_prefill, sparse_mla_prefill_rows  # noqa: F401
 from .pages import page_mark, page_split  # noqa: F401
+from .fp8 import (e4m3_decode, dequantize, sparse_prefill_fp8,  # noqa: F401
+                  sparse_prefill_fp8_rows)

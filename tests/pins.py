@@ -595,3 +595,51 @@ def check_page_mark(mark_fn):
     if mark_fn(np.full((2, 3), -1), 16, 9).any():
         fails.append("padding marked a page")
     return fails
+
+
+# ----------------------------------------------------------------------------- FP8 KV cache
+
+def check_e4m3_decode(decode):
+    """Every code against torch's float8_e4m3fn conversion, plus hand-checked values."""
+    codes = np.arange(256, dtype=np.uint8)
+    got = decode(codes)
+    want = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    fails = []
+    if not np.array_equal(np.isnan(got), np.isnan(want)) or \
+            not np.array_equal(got[~np.isnan(got)], want[~np.isnan(want)]):
+        fails.append("e4m3 decode != torch float8_e4m3fn")
+    hand = {0x38: 1.0, 0x7E: 448.0, 0xFE: -448.0, 0x01: 2.0 ** -9, 0x08: 2.0 ** -6,
+            0x3C: 1.5, 0x40: 2.0, 0x30: 0.5}
+    for c, v in hand.items():
+        if decode(np.array([c], dtype=np.uint8))[0] != v:
+            fails.append(f"code 0x{c:02x}")
+    if not (np.signbit(decode(np.array([0x80], dtype=np.uint8))[0]) and
+            decode(np.array([0x80], dtype=np.uint8))[0] == 0.0):
+        fails.append("code 0x80 is -0")
+    return fails
+
+
+def check_fp8_attention(fn):
+    """fn(q, k8, v8, k_scale, v_scale, page_size, idx, tl, scale) equals the plain (pinned)
+    oracle on caches the test dequantises with torch (float8 -> float64, times the page scale
+    broadcast over each page's slots)."""
+    from oracle import sparse_prefill
+    rng = _rng(600)
+    R, S, Hq, Hkv, D, K, ps = 7, 40, 4, 2, 16, 25, 8
+    q = rng.standard_normal((R, Hq, D))
+    k8 = rng.integers(0, 256, size=(S, Hkv, D), dtype=np.uint8)
+    v8 = rng.integers(0, 256, size=(S, Hkv, D), dtype=np.uint8)
+    k8[(k8 & 0x7F) == 0x7F] = 0x11                # keep NaN codes out of the attention check
+    v8[(v8 & 0x7F) == 0x7F] = 0x22
+    ksc = rng.uniform(0.01, 0.2, size=(S // ps, Hkv))
+    vsc = rng.uniform(0.5, 3.0, size=(S // ps, Hkv))
+    idx = rng.integers(-1, S, size=(R, K))
+    tl = rng.integers(0, K + 1, size=R)
+
+    def deq(c, sc):
+        vals = torch.from_numpy(c).view(torch.float8_e4m3fn).to(torch.float64)
+        per_slot = torch.from_numpy(sc).repeat_interleave(ps, dim=0)            # [S, Hkv]
+        return (vals * per_slot[:, :, None]).numpy()
+    O, L = fn(q, k8, v8, ksc, vsc, ps, idx, tl, 0.3)
+    Oe, Le = sparse_prefill(q, deq(k8, ksc), deq(v8, vsc), idx, tl, 0.3)
+    return [] if (_close(O, Oe, 1e-12) and _close(L, Le, 1e-12)) else ["FP8 attention != dequantised"]

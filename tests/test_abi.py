@@ -19,7 +19,7 @@ def lib():
 def declared_functions():
     src = open(os.path.join(ROOT, "include", "qsa.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(qsa_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(qsa_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -183,3 +183,15 @@ def test_page_split_validation(lib):
     st = lib.qsa_split_touched_pages
     assert st(fake, 10, fake, fake, None, 10, 256, 64, 3, secs, None) == 1
     assert st(fake, 10, fake, fake, fake, 10, 256, 48, 3, secs, None) == 1
+
+
+def test_fp8_entry_validation(lib):
+    f = lib.qsa_sparse_prefill_fp8
+    fake = 1 << 20
+    #        q     k     v     ks    vs    ps  idx   tl    out   lse   R   hq hkv d    topk scale  G  nkv
+    assert f(fake, fake, fake, None, fake, 64, fake, None, fake, None, 10, 6, 1, 256, 2051, 0.0625, 0, 0, None) == 1
+    assert f(fake, fake, fake, fake, None, 64, fake, None, fake, None, 10, 6, 1, 256, 2051, 0.0625, 0, 0, None) == 1
+    assert f(fake, fake, fake, fake, fake, 0, fake, None, fake, None, 10, 6, 1, 256, 2051, 0.0625, 0, 0, None) == 1
+    assert f(fake, fake + 8, fake, fake, fake, 64, fake, None, fake, None, 10, 6, 1, 256, 2051, 0.0625, 0, 0, None) == 1
+    assert f(fake, fake, fake, fake, fake, 64, fake, None, fake, None, 10, 6, 1, 128, 2051, 0.0625, 0, 0, None) == 2
+    assert f(fake, fake, fake, fake, fake, 64, fake, None, fake, None, 0, 6, 1, 256, 2051, 0.0625, 0, 0, None) == 0

@@ -219,3 +219,38 @@ def test_page_mark_mutant_is_caught():
                 m[(t + 1) // ps] = 1
         return m
     assert pins.check_page_mark(mark)
+
+
+def _e4m3_mutant(kind):
+    from oracle.fp8 import e4m3_decode
+
+    def decode(codes):
+        c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+        if kind == "bias_8":
+            e = (c >> 3) & 0xF
+            m = (c & 7) / 8.0
+            v = np.where(e == 0, m * 2.0 ** -7, (1 + m) * np.exp2(e - 8.0))
+            return np.where(c & 0x80, -v, v)
+        if kind == "no_subnormals":
+            v = e4m3_decode(codes)
+            return np.where(((c >> 3) & 0xF) == 0, 0.0, v)
+        return e4m3_decode(codes)
+    return decode
+
+
+@pytest.mark.parametrize("kind", ["bias_8", "no_subnormals"])
+def test_e4m3_mutant_is_caught(kind):
+    assert pins.check_e4m3_decode(_e4m3_mutant(kind))
+
+
+def test_fp8_scale_mutant_is_caught():
+    """Page scale indexed by slot instead of slot // page_size."""
+    from oracle.fp8 import e4m3_decode
+    from oracle import sparse_prefill
+
+    def fn(q, k8, v8, ksc, vsc, ps, idx, tl, scale):
+        def deq(c, sc):
+            per = np.asarray(sc)[np.minimum(np.arange(c.shape[0]), sc.shape[0] - 1)]
+            return e4m3_decode(c) * per[:, :, None]
+        return sparse_prefill(q, deq(k8, ksc), deq(v8, vsc), idx, tl, scale)
+    assert pins.check_fp8_attention(fn)

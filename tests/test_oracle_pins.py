@@ -83,3 +83,11 @@ def test_page_split_pin():
 
 def test_page_mark_pin():
     assert pins.check_page_mark(oracle.page_mark) == []
+
+
+def test_e4m3_decode_pin():
+    assert pins.check_e4m3_decode(oracle.e4m3_decode) == []
+
+
+def test_fp8_attention_pin():
+    assert pins.check_fp8_attention(oracle.sparse_prefill_fp8) == []

@@ -24,7 +24,8 @@ EXPORTED = ["qsa_sparse_prefill", "qsa_sparse_prefill_ex", "qsa_workspace_bytes"
             "qsa_status_string", "qsa_version", "qsa_get_device_status",
             "qsa_sparse_prefill_noalloc", "qsa_probe_gather_ceiling",
             "qsa_sparse_prefill_paged", "qsa_sparse_mla_prefill", "qsa_select_mla_geometry",
-            "qsa_page_mark", "qsa_page_split", "qsa_split_touched_pages"]
+            "qsa_page_mark", "qsa_page_split", "qsa_split_touched_pages",
+            "qsa_sparse_prefill_fp8"]
 
 # Size of the library-owned scratch array used by qsa_sparse_prefill_noalloc (include/qsa.h).
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -86,6 +87,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qsa_page_split.restype = ctypes.c_int
     lib.qsa_split_touched_pages.argtypes = [vp, i64, vp, vp, vp, i64, i32, i32, i32, vp, vp]
     lib.qsa_split_touched_pages.restype = ctypes.c_int
+    lib.qsa_sparse_prefill_fp8.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, i64, i32, i32,
+                                           i32, i32, f32, i32, i64, vp]
+    lib.qsa_sparse_prefill_fp8.restype = ctypes.c_int
     lib.qsa_probe_gather_ceiling.argtypes = [vp, i64, vp, i64, i32, i32, ctypes.POINTER(f32), vp]
     lib.qsa_probe_gather_ceiling.restype = ctypes.c_int
     lib.qsa_workspace_bytes.argtypes = [i64, i32, i32]
@@ -224,6 +228,39 @@ def sparse_prefill_paged(q, k_cache, v_cache, indices, topk_len, cu_seqlens_q, k
                                       page_table.shape[1], int(page_size), int(n_pages), Hq, Hkv,
                                       D, topk, float(scale), int(union_g), _stream_ptr(stream))
     _check(st, "qsa_sparse_prefill_paged")
+    return out, lse
+
+
+def sparse_prefill_fp8(q, k_cache, v_cache, k_scale, v_scale, page_size: int, indices, topk_len,
+                       scale: float, *, out=None, lse=None, union_g: int = 0, n_kv_slots: int = 0,
+                       want_lse: bool = True, stream=None):
+    """FP8 caches (qsa_sparse_prefill_fp8): k_cache / v_cache [S, Hkv, D] uint8 e4m3 codes,
+    k_scale / v_scale [ceil(S / page_size), Hkv] fp32; otherwise as sparse_prefill."""
+    import torch
+    lib = load_library()
+    _require(q, torch.bfloat16, "q", 3)
+    _require(k_cache, torch.uint8, "k_cache", 3)
+    _require(v_cache, torch.uint8, "v_cache", 3)
+    _require(k_scale, torch.float32, "k_scale", 2)
+    _require(v_scale, torch.float32, "v_scale", 2)
+    _require(indices, torch.int32, "indices", 2)
+    _require(topk_len, torch.int32, "topk_len", 1)
+    R, Hq, D = q.shape
+    Hkv = k_cache.shape[1]
+    topk = indices.shape[1]
+    if indices.shape[0] != R or (topk_len is not None and topk_len.shape[0] != R):
+        raise ValueError("indices / topk_len rows must match q")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((R, Hq), dtype=torch.float32, device=q.device)
+    _require(out, torch.bfloat16, "out", 3)
+    _require(lse, torch.float32, "lse", 2)
+    st = lib.qsa_sparse_prefill_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                    _ptr(v_scale), int(page_size), _ptr(indices), _ptr(topk_len),
+                                    _ptr(out), _ptr(lse), R, Hq, Hkv, D, topk, float(scale),
+                                    int(union_g), int(n_kv_slots), _stream_ptr(stream))
+    _check(st, "qsa_sparse_prefill_fp8")
     return out, lse
 
 

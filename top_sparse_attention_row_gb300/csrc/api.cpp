@@ -46,7 +46,9 @@ WsLayout ws_layout(int64_t n_rows, int32_t topk, int32_t G) {
 // steps the shared-memory tile down instead of failing).
 qsa_status select(int32_t Hq, int32_t Hkv, int32_t union_g, int32_t topk, int32_t head_dim,
                   int64_t n_rows, int32_t num_sms, const qsa_geometry* forced, Geometry* g,
-                  bool* fell_back, bool* stepped) {
+                  bool* fell_back, bool* stepped, bool fp8 = false) {
+  // FP8 caches run tiles of at most 32 query columns (fewer kernel instances).
+  const int max_np = fp8 ? qsa::kFp8MaxNPad : qsa::kMaxNPad;
   *fell_back = false;
   *stepped = false;
   if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || topk <= 0 || n_rows < 0 || head_dim <= 0 ||
@@ -58,7 +60,7 @@ qsa_status select(int32_t Hq, int32_t Hkv, int32_t union_g, int32_t topk, int32_
   int G = union_g <= 1 ? 1 : union_g;
   if (G > 1) {
     const int np_u = static_cast<int>(round_up(G * group, 16));
-    const bool legal = G * group <= qsa::kMaxNPad &&
+    const bool legal = G * group <= max_np &&
                        qsa::smem_layout(np_u, qsa::kMinStages, 0).total <= qsa::kSmemLimit &&
                        qsa::union_build_smem_bytes(topk, G) <= static_cast<size_t>(qsa::kUnionMaxSmem) &&
                        static_cast<int64_t>(G) * topk <= INT32_MAX / 2;
@@ -69,7 +71,7 @@ qsa_status select(int32_t Hq, int32_t Hkv, int32_t union_g, int32_t topk, int32_
   }
   int chunks, chunk_cols, np, slot_cap;
   if (G == 1) {
-    chunks = static_cast<int>(ceil_div(group, qsa::kMaxNPad));
+    chunks = static_cast<int>(ceil_div(group, max_np));
     chunk_cols = static_cast<int>(ceil_div(group, chunks));
     np = static_cast<int>(round_up(chunk_cols, 16));
     slot_cap = static_cast<int>(round_up(topk, qsa::kTileTokens));
@@ -235,11 +237,19 @@ qsa_status device_sms(int32_t* sms) {
   return QSA_OK;
 }
 
+// FP8 caches: e4m3 bytes with per-page, per-KV-head fp32 scales.
+struct Fp8Cache {
+  const float* k_scale;
+  const float* v_scale;
+  int32_t page_size;
+};
+
 qsa_status run(const void* q, const void* k_cache, const void* v_cache, const int32_t* indices,
                const int32_t* topk_len, void* out, float* lse, int64_t n_rows, int32_t n_qheads,
                int32_t n_kvheads, int32_t head_dim, int32_t topk, float scale, int32_t union_g,
                int64_t n_kv_slots, void* workspace, size_t workspace_bytes,
-               const qsa_geometry* forced, const qsa::PagedAddr* paged, void* stream_v) {
+               const qsa_geometry* forced, const qsa::PagedAddr* paged, void* stream_v,
+               const Fp8Cache* fp8 = nullptr) {
   if (!q || !k_cache || !v_cache || !indices || !out) return QSA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
     return QSA_ERR_INVALID_ARG;
@@ -250,14 +260,14 @@ qsa_status run(const void* q, const void* k_cache, const void* v_cache, const in
   bool fell_back = false, stepped = false;
   // Validate the shape on the host first (num_sms = 1 stands in until the device is known).
   qsa_status st = select(n_qheads, n_kvheads, union_g, topk, head_dim, n_rows, 1, forced, &g,
-                         &fell_back, &stepped);
+                         &fell_back, &stepped, fp8 != nullptr);
   if (st != QSA_OK) return st;
   if (n_rows == 0) return QSA_OK;
   int32_t sms = 0;
   st = device_sms(&sms);
   if (st != QSA_OK) return st;
   st = select(n_qheads, n_kvheads, union_g, topk, head_dim, n_rows, sms, forced, &g, &fell_back,
-              &stepped);
+              &stepped, fp8 != nullptr);
   if (st != QSA_OK) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
 
@@ -288,6 +298,12 @@ qsa_status run(const void* q, const void* k_cache, const void* v_cache, const in
   const int64_t tmap_rows = n_kv_slots > 0 ? n_kv_slots * n_kvheads : static_cast<int64_t>(INT32_MAX);
   p.pad_row = static_cast<int32_t>(tmap_rows);
   if (paged) p.pa = *paged;
+  if (fp8) {
+    p.k_scale = fp8->k_scale;
+    p.v_scale = fp8->v_scale;
+    p.page_size = fp8->page_size;
+    p.gather_tma = 1;   // the FP8 gather is TMA only
+  }
 
   void* ws = nullptr;
   bool own_ws = false;
@@ -503,6 +519,18 @@ qsa_status qsa_sparse_prefill(const void* q, const void* k_cache, const void* v_
                               int32_t topk, float scale, int32_t union_g, void* stream) {
   return run(q, k_cache, v_cache, indices, topk_len, out, lse, n_rows, n_qheads, n_kvheads,
              head_dim, topk, scale, union_g, 0, nullptr, 0, nullptr, nullptr, stream);
+}
+
+qsa_status qsa_sparse_prefill_fp8(const void* q, const void* k_cache, const void* v_cache,
+                                  const float* k_scale, const float* v_scale, int32_t page_size,
+                                  const int32_t* indices, const int32_t* topk_len, void* out,
+                                  float* lse, int64_t n_rows, int32_t n_qheads, int32_t n_kvheads,
+                                  int32_t head_dim, int32_t topk, float scale, int32_t union_g,
+                                  int64_t n_kv_slots, void* stream) {
+  if (!k_scale || !v_scale || page_size < 1) return QSA_ERR_INVALID_ARG;
+  const Fp8Cache f{k_scale, v_scale, page_size};
+  return run(q, k_cache, v_cache, indices, topk_len, out, lse, n_rows, n_qheads, n_kvheads,
+             head_dim, topk, scale, union_g, n_kv_slots, nullptr, 0, nullptr, nullptr, stream, &f);
 }
 
 qsa_status qsa_sparse_prefill_paged(const void* q, const void* k_cache, const void* v_cache,

@@ -15,6 +15,7 @@ constexpr int kHeadDim = 256;
 constexpr int kTileTokens = 128;             // gathered slots per MMA tile (MMA M)
 constexpr int kStageBytes = kTileTokens * 128 * 2;  // 128 slots x 128 dims bf16 = 32 KiB
 constexpr int kMaxNPad = 64;                 // largest MMA N per tile
+constexpr int kFp8MaxNPad = 32;              // largest MMA N per tile with FP8 caches
 constexpr int kSoftmaxWarps = 4;             // warps 0-3: softmax + epilogue (TMEM lanes 0-127)
 constexpr int kMmaWarp = 4;                  // MMA issue + tensor-memory owner
 constexpr int kIndexWarp = 5;                // slot compaction, Q tile, item info
@@ -66,6 +67,11 @@ struct PrefillParams {
   const uint8_t* v_bytes;
   float scale_log2;             // scale * log2(e)
   PagedAddr pa;                 // per-token mode: page_table != nullptr = logical indices
+  // FP8 e4m3 caches: the value of a cache byte x at slot s, KV head h is
+  // e4m3(x) * scale[(s / page_size) * n_kvheads + h]
+  const float* k_scale;
+  const float* v_scale;
+  int32_t page_size;
 };
 
 struct Geometry {
@@ -98,8 +104,8 @@ __host__ __device__ inline SmemLayout smem_layout(int np, int stages, int slot_c
   L.slots = L.pbuf + 2 * L.p_bytes;
   L.bars = L.slots + 2 * slot_cap * 4;
   // full[st], empty[st], s_full[2], s_free[2], p_full[2], pv_done[2], item_full[2],
-  // item_empty[2], q_empty, q_full, final
-  L.misc = L.bars + (2 * stages + 15) * 8;
+  // item_empty[2], q_empty, q_full, final, landed[st] (FP8 caches)
+  L.misc = L.bars + (3 * stages + 15) * 8;
   // info[2][8] int32, red[2][4][np] float, tmem base, abort flag, vote[3]
   int misc_bytes = 2 * 8 * 4 + 2 * 4 * np * 4 + 32;
   L.total = L.misc + misc_bytes + 1024;   // + alignment slack for the 1024-aligned base

@@ -37,8 +37,10 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include <atomic>
+#include <cstring>
 #include <mutex>
 
 #include "internal.h"
@@ -58,7 +60,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 enum WaitSite : int32_t {
   kSiteItemEmpty = 1, kSiteQEmpty, kSiteItemFull, kSiteStageEmpty, kSiteStageFull,
-  kSiteSFree, kSiteSFull, kSitePFull, kSitePvDone, kSiteDrain, kSiteQFull
+  kSiteSFree, kSiteSFull, kSitePFull, kSitePvDone, kSiteDrain, kSiteQFull, kSiteLanded
 };
 
 __device__ __forceinline__ unsigned long long global_ns() {
@@ -94,6 +96,27 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
   return v;
+}
+__device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+  __nv_bfloat162 b;
+  memcpy(&b, &v, 4);
+  const float2 f = __bfloat1622float2(b);
+  const __half2 h = __floats2half2_rn(f.x, f.y);
+  uint32_t r;
+  memcpy(&r, &h, 4);
+  return r;
+}
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
+  return make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
+                    bf16x2_to_f16x2(v.w));
 }
 __device__ __forceinline__ void sts_v4(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
@@ -145,7 +168,7 @@ __device__ __forceinline__ void decode_item(const PrefillParams& p, int64_t item
 
 }  // namespace
 
-template <int NP, bool UNION>
+template <int NP, bool UNION, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_prefill_kernel(const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV,
@@ -171,6 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t b_qempty = b_itemempty + 16;     // Q buffer free (MMA commit, once per item)
   const uint32_t b_qfull = b_qempty + 8;          // Q buffer written (index warp, once per item)
   const uint32_t b_fin = b_qempty + 16;           // MMA issuer drained
+  const uint32_t b_land = b_fin + 8;              // FP8: a stage's e4m3 bytes landed [R]
 
   ItemInfo* const info = reinterpret_cast<ItemInfo*>(gbase + L.misc);
   float* const red = reinterpret_cast<float*>(gbase + L.misc + 2 * sizeof(ItemInfo));  // [2][4][NP]
@@ -184,8 +208,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < R; ++s) {
-      mbar_init(b_full + 8 * s, p.gather_tma ? 1 : 32);   // owner warp: expect_tx, or 32 lane arrivals
+      // owner warp: expect_tx (TMA), one arrival after converting (FP8), or 32 lane arrivals
+      mbar_init(b_full + 8 * s, (p.gather_tma || FP8) ? 1 : 32);
       mbar_init(b_empty + 8 * s, 1);
+      if (FP8) mbar_init(b_land + 8 * s, 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(b_sfull + 8 * b, 1);
@@ -290,6 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t qb = base + L.qbuf;
       const int rg = lane >> 3, jc = lane & 7;
       auto q_store = [&](int c, uint4 v) {
+        if (FP8) v = bf16x8_to_f16x8(v);   // FP8 caches run the f16 MMA: Q in f16
         sts_v4(qb + rg * (NP * 128) + (c >> 3) * 1024 + (c & 7) * 128 + ((jc ^ (c & 7)) << 4), v);
       };
 #pragma unroll
@@ -347,6 +374,55 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const uint32_t stage = base + L.ring + st * kStageBytes;
+        if (FP8) {
+          // e4m3 half-rows (128 B) land in the stage's upper 16 KiB, then the warp rewrites the
+          // stage in place as the f16 tile: each lane takes whole rows (lane + 32k), reading a
+          // row's 128 bytes before writing its 256, so no row overwrites unread input.
+          int y0, y1, y2, y3;
+          if (UNION) {
+            y0 = uy.x; y1 = uy.y; y2 = uy.z; y3 = uy.w;
+          } else {
+            const int t = t0 + 4 * lane;
+            const int4 v = *reinterpret_cast<const int4*>(sl + t);
+            y0 = t + 0 < nv ? v.x : p.pad_row;
+            y1 = t + 1 < nv ? v.y : p.pad_row;
+            y2 = t + 2 < nv ? v.z : p.pad_row;
+            y3 = t + 3 < nv ? v.w : p.pad_row;
+          }
+          if (lane == 0) mbar_arrive_expect_tx(b_land + 8 * st, kStageBytes / 2);
+          __syncwarp();
+          tma_gather4(stage + 16384 + lane * 512, is_v ? &tmV : &tmK, half * 128, y0, y1, y2, y3,
+                      b_land + 8 * st);
+          issued = s + 1;
+          if (!__all_sync(0xffffffffu, wait_bar(b_land + 8 * st, (s / R) & 1, abort_flag, kSiteLanded))) {
+            aborted = true;
+            break;
+          }
+#pragma unroll 1
+          for (int k = 0; k < 4; ++k) {
+            const int t = lane + 32 * k;
+            const uint32_t sw = static_cast<uint32_t>(t & 7);
+            uint4 in[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) in[c] = lds_v4(stage + 16384 + t * 128 + ((c ^ sw) << 4));
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              // dims 16c .. 16c+15 of the half -> atom c / 4, 16-byte chunks 2(c % 4), 2(c % 4) + 1
+              const uint4 lo = make_uint4(e4m3x2_to_f16x2(in[c].x & 0xffffu), e4m3x2_to_f16x2(in[c].x >> 16),
+                                          e4m3x2_to_f16x2(in[c].y & 0xffffu), e4m3x2_to_f16x2(in[c].y >> 16));
+              const uint4 hi = make_uint4(e4m3x2_to_f16x2(in[c].z & 0xffffu), e4m3x2_to_f16x2(in[c].z >> 16),
+                                          e4m3x2_to_f16x2(in[c].w & 0xffffu), e4m3x2_to_f16x2(in[c].w >> 16));
+              const uint32_t row = stage + (c >> 2) * 16384 + t * 128;
+              const uint32_t j0 = static_cast<uint32_t>((c & 3) * 2);
+              sts_v4(row + ((j0 ^ sw) << 4), lo);
+              sts_v4(row + (((j0 + 1) ^ sw) << 4), hi);
+            }
+          }
+          fence_proxy_async_smem();   // generic writes -> tensor-core (async proxy) reads
+          __syncwarp();
+          if (lane == 0) mbar_arrive(b_full + 8 * st);
+          continue;
+        }
         if (tma) {
           // gather4 op (lane, c): slots 4*lane .. 4*lane+3, dims half*128 + 64c .. +63
           int y0, y1, y2, y3;
@@ -398,18 +474,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(b_itemempty + 8 * b);
     }
-    if (!tma) {
+    if (!tma && !FP8) {
       cp_async_wait_0();
     } else if (aborted && lane == 0) {
-      // Drain: wait (bounded) for the newest phase of every stage this warp filled.
+      // Drain: wait (bounded) for the newest copy into every stage this warp filled.
+      const uint32_t landed = FP8 ? b_land : b_full;
       for (uint32_t s = issued > static_cast<uint32_t>(R) ? issued - R : 0; s < issued; ++s)
         if (static_cast<int>(s % R) % W == pw)
-          wait_slow(b_full + 8 * (s % R), (s / R) & 1, abort_flag, kSiteDrain, kDrainLimitNs);
+          wait_slow(landed + 8 * (s % R), (s / R) & 1, abort_flag, kSiteDrain, kDrainLimitNs);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t kIdescQK = idesc_bf16_f32(128, NP, false, false);
-    constexpr uint32_t kIdescPV = idesc_bf16_f32(128, NP, true, false);
+    constexpr uint32_t kIdescQK = FP8 ? idesc_f16_f32(128, NP, false, false)
+                                      : idesc_bf16_f32(128, NP, false, false);
+    constexpr uint32_t kIdescPV = FP8 ? idesc_f16_f32(128, NP, true, false)
+                                      : idesc_bf16_f32(128, NP, true, false);
     uint32_t seq = 0, js = 0, it = 0;
     bool aborted = false;
     for (int64_t item = blockIdx.x; item < n_items && !aborted; item += stride, ++it) {
@@ -515,10 +594,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t b = it & 1, ph = (it >> 1) & 1;
       bad |= !wait_bar(b_itemfull + 8 * b, ph, abort_flag, kSiteItemFull);
       const ItemInfo I = info[b];
-      mbar_arrive(b_itemempty + 8 * b);
+      // FP8 reads the item's slot list for the scales until its last tile, so it hands the
+      // item slot back at the end of the item instead.
+      if (!FP8) mbar_arrive(b_itemempty + 8 * b);
       const int nv = I.n_valid;
       const int nt = (nv + kTileTokens - 1) / kTileTokens;
       const int cols = I.cols;
+      const int32_t* slots_b = reinterpret_cast<const int32_t*>(gbase + L.slots) + b * slot_cap;
+      const int32_t* ul_b =
+          UNION ? p.union_idx + static_cast<int64_t>(I.group) * p.union_g * p.topk : nullptr;
       // Column masks: bit c of colmask[u] set when query column c belongs to row u of the group.
       uint64_t colmask[8];
       uint64_t allcols = (cols >= 64) ? ~0ull : ((1ull << cols) - 1ull);
@@ -560,6 +644,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if ((bits >> u) & 1u) m |= colmask[u];
           vmask &= m;
         }
+        // FP8 caches: the slot's page scales -- K's multiplies the logit, V's the probability
+        // fed to P.V (the row sum keeps the unscaled probability).
+        float logit_scale = p.scale_log2, v_scale = 1.f;
+        if (FP8 && valid) {
+          const int64_t slot = UNION ? static_cast<int64_t>(ul_b[token])
+                                     : static_cast<int64_t>(slots_b[token]) / p.n_kvheads;
+          const int64_t si = (slot / p.page_size) * p.n_kvheads + I.kvh;
+          logit_scale *= __ldg(p.k_scale + si);
+          v_scale = __ldg(p.v_scale + si);
+        }
         bad |= !wait_bar(b_sfull + 8 * sb, sph, abort_flag, kSiteSFull);
         tc_fence_after();
         float x[NP];
@@ -571,7 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool need = false;
 #pragma unroll
         for (int c = 0; c < NP; ++c) {
-          x[c] = ((vmask >> c) & 1ull) ? x[c] * p.scale_log2 : NEG_INF;
+          x[c] = ((vmask >> c) & 1ull) ? x[c] * logit_scale : NEG_INF;
           need |= x[c] > m_used[c] + kRescaleThreshold;
         }
         // One barrier per tile decides, uniformly for the 128 threads, whether the max moves
@@ -640,9 +734,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < NP; ++c) {
           const float pv = x[c] == NEG_INF ? 0.f : fast_exp2(x[c] - m_used[c]);
           l_part[c] += pv;
-          const __nv_bfloat16 pb16 = __float2bfloat16_rn(pv);
-          *reinterpret_cast<__nv_bfloat16*>(prow + (c >> 3) * 1024 + (c & 7) * 128 +
-                                            ((tchunk ^ (c & 7)) << 4)) = pb16;
+          uint8_t* const dst = prow + (c >> 3) * 1024 + (c & 7) * 128 + ((tchunk ^ (c & 7)) << 4);
+          if (FP8)
+            *reinterpret_cast<__half*>(dst) = __float2half_rn(pv * v_scale);
+          else
+            *reinterpret_cast<__nv_bfloat16*>(dst) = __float2bfloat16_rn(pv);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -719,6 +815,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       js += nt;
+      if (FP8) mbar_arrive(b_itemempty + 8 * b);
     }
   }
 
@@ -768,10 +865,26 @@ cudaError_t make_cache_map(CUtensorMap* m, const void* cache, int64_t rows, int 
 
 namespace {
 
-template <int NP, bool UNION>
+// 2-D map over an e4m3 KV cache viewed as [rows, 256] bytes, box 128 x 1 (one 128-dim half row),
+// 128-byte swizzle.
+cudaError_t make_cache_map_e4m3(CUtensorMap* m, const void* cache, int64_t rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim)};
+  const cuuint32_t box[2] = {128, 1};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(cache), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int NP, bool UNION, bool FP8>
 cudaError_t launch_np(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
                       const Geometry& g, cudaStream_t stream) {
-  auto kern = sparse_prefill_kernel<NP, UNION>;
+  auto kern = sparse_prefill_kernel<NP, UNION, FP8>;
   // The shared-memory opt-in is set once per device and size, so calls made while a stream
   // is being captured into a CUDA graph only enqueue the launch.
   static std::atomic<int> opted_in[64];
@@ -793,16 +906,26 @@ cudaError_t launch_prefill(const PrefillParams& p, const Geometry& g, const void
                            const void* v_cache, int64_t tmap_rows, cudaStream_t stream) {
   if (g.n_items == 0) return cudaSuccess;
   CUtensorMap tk, tv;
-  cudaError_t e = make_cache_map(&tk, k_cache, tmap_rows, kHeadDim);
+  const bool fp8 = p.k_scale != nullptr;
+  cudaError_t e = fp8 ? make_cache_map_e4m3(&tk, k_cache, tmap_rows)
+                      : make_cache_map(&tk, k_cache, tmap_rows, kHeadDim);
   if (e != cudaSuccess) return e;
-  e = make_cache_map(&tv, v_cache, tmap_rows, kHeadDim);
+  e = fp8 ? make_cache_map_e4m3(&tv, v_cache, tmap_rows)
+          : make_cache_map(&tv, v_cache, tmap_rows, kHeadDim);
   if (e != cudaSuccess) return e;
   const bool u = p.union_g > 1;
+  if (fp8) {
+    switch (g.np) {
+      case 16: return u ? launch_np<16, true, true>(tk, tv, p, g, stream) : launch_np<16, false, true>(tk, tv, p, g, stream);
+      case 32: return u ? launch_np<32, true, true>(tk, tv, p, g, stream) : launch_np<32, false, true>(tk, tv, p, g, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (g.np) {
-    case 16: return u ? launch_np<16, true>(tk, tv, p, g, stream) : launch_np<16, false>(tk, tv, p, g, stream);
-    case 32: return u ? launch_np<32, true>(tk, tv, p, g, stream) : launch_np<32, false>(tk, tv, p, g, stream);
-    case 48: return u ? launch_np<48, true>(tk, tv, p, g, stream) : launch_np<48, false>(tk, tv, p, g, stream);
-    case 64: return u ? launch_np<64, true>(tk, tv, p, g, stream) : launch_np<64, false>(tk, tv, p, g, stream);
+    case 16: return u ? launch_np<16, true, false>(tk, tv, p, g, stream) : launch_np<16, false, false>(tk, tv, p, g, stream);
+    case 32: return u ? launch_np<32, true, false>(tk, tv, p, g, stream) : launch_np<32, false, false>(tk, tv, p, g, stream);
+    case 48: return u ? launch_np<48, true, false>(tk, tv, p, g, stream) : launch_np<48, false, false>(tk, tv, p, g, stream);
+    case 64: return u ? launch_np<64, true, false>(tk, tv, p, g, stream) : launch_np<64, false, false>(tk, tv, p, g, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -190,6 +190,32 @@ def make_union(seed: int = 3, n_rows: int = 8192, topk: int = 2048) -> Workload:
     return Workload("union_8k", q, k, v, idx, None, 1.0 / 16.0, pos)
 
 
+def quantize_e4m3(bits: np.ndarray, page_size: int):
+    """bf16 bit patterns [S, Hkv, D] -> (e4m3 codes [S, Hkv, D] uint8, fp32 scales
+    [ceil(S / page_size), Hkv]): one scale per page and KV head, amax / 448, values rounded to
+    the nearest e4m3 by torch's float8_e4m3fn cast (input preparation for the FP8 cache path)."""
+    import torch
+    x = torch.from_numpy(bf16_to_f32(bits))
+    S, H, D = x.shape
+    pages = -(-S // page_size)
+    pad = pages * page_size - S
+    xp = torch.cat([x, torch.zeros(pad, H, D)]) if pad else x
+    amax = xp.reshape(pages, page_size, H, D).abs().amax(dim=(1, 3))           # [pages, H]
+    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax)).float()
+    per_slot = scale.repeat_interleave(page_size, dim=0)[:S]                    # [S, H]
+    codes = (x / per_slot[:, :, None]).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes.numpy(), scale.numpy()
+
+
+def with_fp8_cache(w: Workload, page_size: int = 64) -> Workload:
+    """The same workload with K and V held as an e4m3 cache with per-page scales
+    (meta: k8, v8, k_scale, v_scale, page_size)."""
+    k8, ks = quantize_e4m3(w.k, page_size)
+    v8, vs = quantize_e4m3(w.v, page_size)
+    meta = dict(w.meta, fp8=True, k8=k8, v8=v8, k_scale=ks, v_scale=vs, fp8_page_size=page_size)
+    return Workload(w.name + "_fp8", w.q, w.k, w.v, w.indices, w.topk_len, w.scale, w.positions, meta)
+
+
 MLA_DQK, MLA_DV = 576, 512
 
 
