@@ -317,6 +317,8 @@ def run_gpu(args, rank, world, local_rank):
     n_pieces = min(len(valid) // 128, 4096)
     table = torch.from_numpy(valid[: n_pieces * 128].astype(np.int32).reshape(n_pieces, 128)).to(dev)
     k_flat = k.reshape(-1)
+    if k_flat.dtype != torch.bfloat16:   # e4m3 bytes: the probe reads 512-byte rows of the buffer
+        k_flat = k_flat.view(torch.bfloat16)
     k_rows = k_flat[: (k_flat.numel() // 256) * 256].view(-1, 256)
     ceilings = {}
     for eng in ("tma", "cpasync"):
