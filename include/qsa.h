@@ -279,6 +279,14 @@ qsa_status qsa_probe_gather_ceiling(const void* cache, int64_t n_rows, const int
                                     int64_t n_table_pieces, int32_t pieces_per_cta,
                                     int32_t engine, float* ms_out, void* stream);
 
+/* Failure-detection test hook (no counterpart on the pages): the next attention call
+ * (qsa_sparse_prefill*, qsa_sparse_mla_prefill) launches with its index warps withholding their
+ * items, so every other role's bounded wait (2 s) runs out.  The kernel records
+ * 0x100 | wait site in the device status word, abandons the call (its outputs are unspecified),
+ * frees its tensor memory and returns; the context stays usable and qsa_get_device_status then
+ * returns QSA_ERR_TIMEOUT.  One-shot, process wide. */
+void qsa_debug_stall_next_call(void);
+
 void qsa_get_counters(qsa_counters* out);   /* host pointer */
 void qsa_reset_counters(void);
 const char* qsa_status_string(qsa_status s);

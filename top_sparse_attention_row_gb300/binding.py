@@ -25,7 +25,7 @@ EXPORTED = ["qsa_sparse_prefill", "qsa_sparse_prefill_ex", "qsa_workspace_bytes"
             "qsa_sparse_prefill_noalloc", "qsa_probe_gather_ceiling",
             "qsa_sparse_prefill_paged", "qsa_sparse_mla_prefill", "qsa_select_mla_geometry",
             "qsa_page_mark", "qsa_page_split", "qsa_split_touched_pages",
-            "qsa_sparse_prefill_fp8"]
+            "qsa_sparse_prefill_fp8", "qsa_debug_stall_next_call"]
 
 # Size of the library-owned scratch array used by qsa_sparse_prefill_noalloc (include/qsa.h).
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -90,6 +90,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qsa_sparse_prefill_fp8.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, i64, i32, i32,
                                            i32, i32, f32, i32, i64, vp]
     lib.qsa_sparse_prefill_fp8.restype = ctypes.c_int
+    lib.qsa_debug_stall_next_call.argtypes = []
+    lib.qsa_debug_stall_next_call.restype = None
     lib.qsa_probe_gather_ceiling.argtypes = [vp, i64, vp, i64, i32, i32, ctypes.POINTER(f32), vp]
     lib.qsa_probe_gather_ceiling.restype = ctypes.c_int
     lib.qsa_workspace_bytes.argtypes = [i64, i32, i32]
@@ -441,6 +443,12 @@ def counters() -> dict:
 
 def reset_counters():
     load_library().qsa_reset_counters()
+
+
+def debug_stall_next_call():
+    """Arm the failure-detection hook (qsa_debug_stall_next_call): the next attention call's
+    bounded waits run out and it records a timeout in the device status word."""
+    load_library().qsa_debug_stall_next_call()
 
 
 def device_status(stream=None) -> int:

@@ -14,6 +14,7 @@ using qsa::Geometry;
 
 std::atomic<uint64_t> g_calls_per_token{0}, g_calls_union{0}, g_union_fallbacks{0},
     g_step_downs{0}, g_launches{0};
+std::atomic<int> g_stall_next{0};   // armed by qsa_debug_stall_next_call
 
 constexpr size_t kWsAlign = 256;
 
@@ -298,6 +299,7 @@ qsa_status run(const void* q, const void* k_cache, const void* v_cache, const in
   const int64_t tmap_rows = n_kv_slots > 0 ? n_kv_slots * n_kvheads : static_cast<int64_t>(INT32_MAX);
   p.pad_row = static_cast<int32_t>(tmap_rows);
   if (paged) p.pa = *paged;
+  p.stall_first_item = g_stall_next.exchange(0);
   if (fp8) {
     p.k_scale = fp8->k_scale;
     p.v_scale = fp8->v_scale;
@@ -385,6 +387,7 @@ qsa_status run_mla(const void* q, const void* kv_cache, const int32_t* indices,
   const int64_t tmap_rows = n_kv_slots > 0 ? n_kv_slots : static_cast<int64_t>(INT32_MAX);
   p.pad_row = static_cast<int32_t>(tmap_rows);
   if (paged) p.pa = *paged;
+  p.stall_first_item = g_stall_next.exchange(0);
 
   void* ws = nullptr;
   if (g.union_g > 1) {
@@ -618,6 +621,8 @@ qsa_status qsa_select_geometry(int32_t n_qheads, int32_t n_kvheads, int32_t unio
   to_public(g, out);
   return QSA_OK;
 }
+
+void qsa_debug_stall_next_call(void) { g_stall_next.store(1); }
 
 void qsa_get_counters(qsa_counters* out) {
   if (!out) return;

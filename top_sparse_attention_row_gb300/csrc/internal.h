@@ -72,6 +72,7 @@ struct PrefillParams {
   const float* k_scale;
   const float* v_scale;
   int32_t page_size;
+  int32_t stall_first_item;     // failure-detection test: the index warp withholds its items
 };
 
 struct Geometry {
@@ -145,6 +146,7 @@ struct MlaParams {
   int32_t tmem_cols;
   float scale_log2;
   PagedAddr pa;                 // page_table == nullptr = physical slots
+  int32_t stall_first_item;     // failure-detection test: the index warp withholds its items
 };
 
 struct MlaSmemLayout {

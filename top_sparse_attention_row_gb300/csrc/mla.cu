@@ -174,6 +174,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ index / Q loader
     uint32_t it = 0;
     for (int64_t item = blockIdx.x; item < n_items; item += stride, ++it) {
+      // failure-detection test hook: withhold the first item so every other wait runs out
+      if (p.stall_first_item) break;
       const uint32_t b = it & 1, ph = (it >> 1) & 1;
       if (!__all_sync(0xffffffffu, mla_wait(b_itemempty + 8 * b, ph ^ 1, abort_flag, status, kMItemEmpty)))
         break;
@@ -499,6 +501,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t item = blockIdx.x; item < n_items; item += stride, ++it) {
       const uint32_t b = it & 1, ph = (it >> 1) & 1;
       bad |= !mla_wait(b_itemfull + 8 * b, ph, abort_flag, status, kMItemFull);
+      // Uniform decision before the item record is read (see the d=256 kernel).
+      if (named_bar_any(3, 128, bad || *abort_flag)) break;
       const MlaItem I = info[b];
       mbar_arrive(b_itemempty + 8 * b);
       const int nv = I.n_valid;

@@ -252,6 +252,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ index / Q loader
     uint32_t it = 0;
     for (int64_t item = blockIdx.x; item < n_items; item += stride, ++it) {
+      // failure-detection test hook: withhold the first item so every other wait runs out
+      if (p.stall_first_item) break;
       const uint32_t b = it & 1, ph = (it >> 1) & 1;
       bool ok = wait_bar(b_itemempty + 8 * b, ph ^ 1, abort_flag, kSiteItemEmpty);
       if (!__all_sync(0xffffffffu, ok)) break;
@@ -593,6 +595,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int64_t item = blockIdx.x; item < n_items; item += stride, ++it) {
       const uint32_t b = it & 1, ph = (it >> 1) & 1;
       bad |= !wait_bar(b_itemfull + 8 * b, ph, abort_flag, kSiteItemFull);
+      // Uniform decision before the item record is read: if any softmax thread's wait gave up
+      // (or another role aborted), all 128 leave together.
+      if (named_bar_any(3, 128, bad || *abort_flag)) break;
       const ItemInfo I = info[b];
       // FP8 reads the item's slot list for the scales until its last tile, so it hands the
       // item slot back at the end of the item instead.
