@@ -285,9 +285,13 @@ __global__ void __launch_bounds__(kBmThreads)
   //    covers every slot, in which case the bitmaps are built once.
   const int64_t span = static_cast<int64_t>(W) * 32;
   const bool one_window = gmax >= 0 && gmax < span;
-  for (int pass = 0; pass < 2 && gmax >= 0; ++pass) {
+  // One window: rows are visited in order, so each row's place follows from the rows before it
+  // and a single pass both counts and emits.  Several windows: a counting pass first, because a
+  // row's slots from every window precede the next row's.
+  int placed = 0;
+  for (int pass = one_window ? 1 : 0; pass < 2 && gmax >= 0; ++pass) {
     int64_t wbase = 0;
-    if (pass == 1) {
+    if (pass == 1 && !one_window) {
       if (tid == 0) {
         int acc = 0;
         for (int t = 0; t < Gp; ++t) { row_base[t] = acc; acc += row_total[t]; }
@@ -298,7 +302,7 @@ __global__ void __launch_bounds__(kBmThreads)
       const int64_t need_words = (gmax - wbase) / 32 + 1;
       const int active = static_cast<int>(need_words < W ? need_words : W);
       const int wpt = (active + kBmThreads - 1) / kBmThreads;   // words per thread
-      if (!(pass == 1 && one_window)) {
+      {
         for (int i = tid; i < Gp * active; i += kBmThreads) bm[(i / active) * W + i % active] = 0u;
         __syncthreads();
         for (int e = tid; e < Gp * topk; e += kBmThreads) {
@@ -325,7 +329,7 @@ __global__ void __launch_bounds__(kBmThreads)
         if (pass == 0) {
           if (tid == 0) row_total[t] += total;
         } else {
-          int pos = row_base[t] + row_done[t] + off;
+          int pos = (one_window ? placed : row_base[t] + row_done[t]) + off;
           for (int w = w0; w < w1; ++w) {
             uint32_t earlier = 0u;
             for (int u = 0; u < t; ++u) earlier |= bm[u * W + w];
@@ -342,6 +346,7 @@ __global__ void __launch_bounds__(kBmThreads)
           }
           __syncthreads();
           if (tid == 0) row_done[t] += total;
+          placed += total;   // uniform: every thread holds the block total
         }
         __syncthreads();
       }
@@ -358,7 +363,11 @@ __global__ void __launch_bounds__(kBmThreads)
     }
   }
   int total = 0;
-  for (int t = 0; t < Gp; ++t) total += row_total[t];
+  if (one_window) {
+    total = placed;
+  } else {
+    for (int t = 0; t < Gp; ++t) total += row_total[t];
+  }
   if (tid == 0) union_len[group] = total;
   if (pad_outputs) {
     for (int64_t e = total + tid; e < cap; e += kBmThreads) {
@@ -401,8 +410,22 @@ cudaError_t launch_union_build(const int32_t* indices, const int32_t* topk_len, 
   if (paged != nullptr) pa = *paged;
   const int64_t n_groups = (n_rows + union_g - 1) / union_g;
   if (sorted_out == nullptr) {
-    const int W = union_bitmap_words(topk, union_g);
+    // Window: the widest that still lets several groups share an SM (the build is latency
+    // bound), no wider than the slot count when the caller gives one.
+    int W = union_bitmap_words(topk, union_g);
     if (W < kBmThreads) return cudaErrorInvalidValue;
+    for (int per_sm = 4; per_sm >= 2; --per_sm) {
+      const int64_t budget = (227 * 1024) / per_sm - 1024;
+      const int64_t w = (budget / 4 - static_cast<int64_t>(union_g) * topk) / union_g / kBmThreads * kBmThreads;
+      if (w >= 1024) {
+        if (w < W) W = static_cast<int>(w);
+        break;
+      }
+    }
+    if (n_kv_slots > 0) {
+      const int64_t need = ((n_kv_slots + 31) / 32 + kBmThreads - 1) / kBmThreads * kBmThreads;
+      if (need < W) W = static_cast<int>(need);
+    }
     const size_t smem = static_cast<size_t>(union_g) * (static_cast<size_t>(topk) + W) * 4;
     static std::atomic<int> bm_opted_in[64];
     int dev = 0;
