@@ -422,7 +422,8 @@ def run_gpu(args, rank, world, local_rank):
     if os.path.exists(tpath):
         with open(tpath) as f:
             tj = json.load(f)
-        key = f"{args.config}:union{args.union}" + (":paged" if paged else "")
+        key = (f"{args.config}:union{args.union}" + (":paged" if paged else "")
+               + (":fp8" if args.fp8 else ""))
         ent = tj.get(key)
         if ent and ent.get("kernel_sha") == kernel_sha(mla):
             traffic = ent.get("dram_bytes_per_launch")
