@@ -124,22 +124,34 @@ __device__ __forceinline__ void sts_v4(uint32_t addr, uint4 v) {
                : "memory");
 }
 
-// Pieces of an item in consumption order: K(0), K(1), V(0), K(2), V(1), ..., K(nt-1), V(nt-2),
-// V(nt-1); every entry is two pieces (dims 0-127, 128-255).
+// MMA issue order of an item with lookahead L (kLookahead): at step j the thread issues
+// S^T(j) = K(j).Q^T (j < nt) and then O^T += V(j-L)^T.P^T(j-L) (j >= L), so the softmax of
+// tile j has the issue time of L further QK^T groups and L-1 P.V groups before P.V(j) needs it.
+// Pieces (two per entry: dims 0-127, 128-255) enter the ring in exactly that order:
+//   K(0) .. K(L-1), then K(j), V(j-L) for L <= j < nt, then the remaining V.
+
+__device__ __forceinline__ int k_entry(int j) { return j + (j > kLookahead ? j - kLookahead : 0); }
+__device__ __forceinline__ int v_entry(int i, int nt) {
+  return (i + kLookahead + 1 < nt ? i + kLookahead + 1 : nt) + i;
+}
 __device__ __forceinline__ void piece_of(int q, int nt, int& tile, int& is_v, int& half) {
-  if (q < 2) {
-    tile = 0; is_v = 0; half = q;
-    return;
-  }
-  const int b = (q + 2) >> 2, r = (q + 2) & 3;
-  if (b < nt) {
-    if (r < 2) { tile = b; is_v = 0; half = r; } else { tile = b - 1; is_v = 1; half = r - 2; }
+  const int e = q >> 1;
+  half = q & 1;
+  if (nt <= kLookahead) {
+    is_v = e >= nt;
+    tile = is_v ? e - nt : e;
+  } else if (e < kLookahead) {
+    is_v = 0;
+    tile = e;
+  } else if (e < 2 * nt - kLookahead) {
+    const int d = e - kLookahead, j = kLookahead + (d >> 1);
+    is_v = d & 1;
+    tile = is_v ? j - kLookahead : j;
   } else {
-    tile = nt - 1; is_v = 1; half = r;
+    is_v = 1;
+    tile = e - nt;
   }
 }
-__device__ __forceinline__ int k_piece(int j) { return j == 0 ? 0 : 4 * j - 2; }
-__device__ __forceinline__ int v_piece(int j, int nt) { return j + 1 < nt ? 4 * j + 4 : 4 * nt - 2; }
 
 __device__ __forceinline__ void cp_async_16_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
@@ -185,9 +197,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // barrier addresses
   const uint32_t b_full = base + L.bars;
   const uint32_t b_empty = b_full + 8 * R;
-  const uint32_t b_sfull = b_empty + 8 * R;
-  const uint32_t b_sfree = b_sfull + 16;
-  const uint32_t b_pfull = b_sfree + 16;
+  const uint32_t b_sfull = b_empty + 8 * R;     // [kSBufs]
+  const uint32_t b_sfree = b_sfull + 8 * kSBufs;
+  const uint32_t b_pfull = b_sfree + 8 * kSBufs;
   const uint32_t b_pvdone = b_pfull + 16;
   const uint32_t b_itemfull = b_pvdone + 16;
   const uint32_t b_itemempty = b_itemfull + 16;
@@ -213,9 +225,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(b_empty + 8 * s, 1);
       if (FP8) mbar_init(b_land + 8 * s, 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kSBufs; ++b) {
       mbar_init(b_sfull + 8 * b, 1);
       mbar_init(b_sfree + 8 * b, 128);
+    }
+    for (int b = 0; b < 2; ++b) {
       mbar_init(b_pfull + 8 * b, 128);
       mbar_init(b_pvdone + 8 * b, 1);
       mbar_init(b_itemfull + 8 * b, 1);
@@ -242,8 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const uint32_t tm_s0 = tmem_base;              // S buffers: columns [0, NP), [NP, 2NP)
-  const uint32_t tm_o = tmem_base + 2 * NP;      // O^T halves: [2NP, 3NP), [3NP, 4NP)
+  const uint32_t tm_s0 = tmem_base;                 // S^T buffers: columns [b NP, (b+1) NP)
+  const uint32_t tm_o = tmem_base + kSBufs * NP;    // O^T halves: the next 2 NP columns
 
   const int64_t n_items = p.n_items;
   const int64_t stride = gridDim.x;
@@ -508,11 +522,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         aborted = true;
         break;
       }
-      for (int j = 0; j <= nt; ++j) {
+      for (int j = 0; j < nt + kLookahead; ++j) {
         if (j < nt) {
           // S^T(j) = K(j) . Q^T
-          const uint32_t s_lo = seq + k_piece(j), s_hi = s_lo + 1;
-          const uint32_t jsj = js + j, sb = jsj & 1, sph = (jsj >> 1) & 1;
+          const uint32_t s_lo = seq + 2 * k_entry(j), s_hi = s_lo + 1;
+          const uint32_t jsj = js + j, sb = jsj % kSBufs, sph = (jsj / kSBufs) & 1;
           bool ok = wait_bar(b_full + 8 * (s_lo % R), (s_lo / R) & 1, abort_flag, kSiteStageFull);
           ok = ok && wait_bar(b_full + 8 * (s_hi % R), (s_hi / R) & 1, abort_flag, kSiteStageFull);
           ok = ok && wait_bar(b_sfree + 8 * sb, sph ^ 1, abort_flag, kSiteSFree);
@@ -540,11 +554,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           __syncwarp();
         }
-        if (j > 0) {
-          // O^T += V(j-1)^T . P^T(j-1)
-          const int jp = j - 1;
+        if (j >= kLookahead && j - kLookahead < nt) {
+          // O^T += V(j-L)^T . P^T(j-L)
+          const int jp = j - kLookahead;
           const uint32_t jsp = js + jp, pb = jsp & 1, pph = (jsp >> 1) & 1;
-          const uint32_t s_vlo = seq + v_piece(jp, nt), s_vhi = s_vlo + 1;
+          const uint32_t s_vlo = seq + 2 * v_entry(jp, nt), s_vhi = s_vlo + 1;
           bool ok = wait_bar(b_pfull + 8 * pb, pph, abort_flag, kSitePFull);
           ok = ok && wait_bar(b_full + 8 * (s_vlo % R), (s_vlo / R) & 1, abort_flag, kSiteStageFull);
           ok = ok && wait_bar(b_full + 8 * (s_vhi % R), (s_vhi / R) & 1, abort_flag, kSiteStageFull);
@@ -636,7 +650,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (UNION && nt > 0) bits_next = t < nv ? ub[t] : 0u;
       bool quit = false;
       for (int j = 0; j < nt; ++j) {
-        const uint32_t jsj = js + j, sb = jsj & 1, sph = (jsj >> 1) & 1;
+        const uint32_t jsj = js + j, sb = jsj & 1, sph = (jsj >> 1) & 1;     // P buffer
+        const uint32_t ss = jsj % kSBufs, ssph = (jsj / kSBufs) & 1;       // S^T buffer
         const int token = j * kTileTokens + t;
         const bool valid = token < nv;
         uint64_t vmask = valid ? allcols : 0ull;
@@ -659,14 +674,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           logit_scale *= __ldg(p.k_scale + si);
           v_scale = __ldg(p.v_scale + si);
         }
-        bad |= !wait_bar(b_sfull + 8 * sb, sph, abort_flag, kSiteSFull);
+        bad |= !wait_bar(b_sfull + 8 * ss, ssph, abort_flag, kSiteSFull);
         tc_fence_after();
         float x[NP];
 #pragma unroll
-        for (int q = 0; q < NP / 16; ++q) tmem_ld16(tm_s0 + lane_off + sb * NP + 16 * q, x + 16 * q);
+        for (int q = 0; q < NP / 16; ++q) tmem_ld16(tm_s0 + lane_off + ss * NP + 16 * q, x + 16 * q);
         tc_wait_ld();
         tc_fence_before();
-        mbar_arrive(b_sfree + 8 * sb);
+        mbar_arrive(b_sfree + 8 * ss);
         bool need = false;
 #pragma unroll
         for (int c = 0; c < NP; ++c) {
