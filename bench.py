@@ -285,7 +285,7 @@ def run_gpu(args, rank, world, local_rank):
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    def call():
+    def call_on(q, k, v, idx, tl, d_meta, out, lse, ws):
         if mla:
             binding.sparse_mla_prefill(q, k, idx, tl, w.scale, out=out, lse=lse, union_g=args.union,
                                        stream=stream)
@@ -301,6 +301,9 @@ def run_gpu(args, rank, world, local_rank):
         else:
             binding.sparse_prefill(q, k, v, idx, tl, w.scale, out=out, lse=lse, union_g=args.union,
                                    workspace=ws, stream=stream)
+
+    def call():
+        call_on(q, k, v, idx, tl, d_meta, out, lse, ws)
 
     if mla:
         geo = binding.select_mla_geometry(w.n_qheads, args.union, w.topk, w.n_rows)
@@ -358,36 +361,59 @@ def run_gpu(args, rank, world, local_rank):
     # end to end: pinned host inputs -> device, call, result -> host, every step
     e_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     e_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size()
-              for t in (h_q, h_k, h_v, h_idx) + ((h_tl,) if h_tl is not None else ()) + h_meta)
+    h2d_bytes = sum(t.numel() * t.element_size()
+                    for t in (h_q, h_k, h_v, h_idx) + ((h_tl,) if h_tl is not None else ()) + h_meta)
     d2h = e_out.numel() * e_out.element_size() + e_lse.numel() * e_lse.element_size()
 
-    def e2e_step():
-        q.copy_(h_q, non_blocking=True)
-        k.copy_(h_k, non_blocking=True)
-        v.copy_(h_v, non_blocking=True)
-        idx.copy_(h_idx, non_blocking=True)
-        if tl is not None:
-            tl.copy_(h_tl, non_blocking=True)
-        for d, h in zip(d_meta, h_meta):
-            d.copy_(h, non_blocking=True)
-        call()
-        e_out.copy_(out, non_blocking=True)
-        e_lse.copy_(lse, non_blocking=True)
+    # Two device input sets: the copies of step i+1 run on a copy stream while step i computes
+    # (every step still copies all of its inputs in and its O / LSE out inside the timed region).
+    host_in = (h_q, h_k, h_v, h_idx, h_tl) + h_meta
+    sets = [(q, k, v, idx, tl) + d_meta,
+            tuple(None if t is None else torch.empty_like(t) for t in (q, k, v, idx, tl) + d_meta)]
+    outs = [(out, lse), (torch.empty_like(out), torch.empty_like(lse))]
+    wss = [ws, None if ws is None else torch.empty_like(ws)]
+    copy_stream = torch.cuda.Stream(device=dev)
+    copied = [torch.cuda.Event(), torch.cuda.Event()]
+    done = [torch.cuda.Event(), torch.cuda.Event()]
 
-    for _ in range(2):
-        e2e_step()
+    def h2d(si):
+        with torch.cuda.stream(copy_stream):
+            for d, h in zip(sets[si], host_in):
+                if d is not None:
+                    d.copy_(h, non_blocking=True)
+            copied[si].record(copy_stream)
+
+    def compute(si):
+        stream.wait_event(copied[si])
+        qq, kk, vv, ii, tt = sets[si][:5]
+        oo, ll = outs[si]
+        call_on(qq, kk, vv, ii, tt, sets[si][5:], oo, ll, wss[si])
+        done[si].record(stream)
+        e_out.copy_(oo, non_blocking=True)
+        e_lse.copy_(ll, non_blocking=True)
+
+    def e2e_run(n):
+        h2d(0)
+        for i in range(n):
+            if i + 1 < n:
+                # set (i+1) % 2 is free once the kernel of step i-1 has consumed it
+                if i >= 1:
+                    copy_stream.wait_event(done[(i + 1) % 2])
+                h2d((i + 1) % 2)
+            compute(i % 2)
+
+    e2e_run(3)
     torch.cuda.synchronize()
-    e_times = []
-    for _ in range(args.steps):
-        flush.zero_()
-        s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s_ev.record(stream)
-        e2e_step()
-        e_ev.record(stream)
-        torch.cuda.synchronize()
-        e_times.append(s_ev.elapsed_time(e_ev))
-    e_ms = sum(e_times) / len(e_times)
+    flush.zero_()
+    torch.cuda.synchronize()
+    s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s_ev.record(stream)
+    copy_stream.wait_event(s_ev)
+    e2e_run(args.steps)
+    stream.wait_stream(copy_stream)
+    e_ev.record(stream)
+    torch.cuda.synchronize()
+    e_ms = s_ev.elapsed_time(e_ev) / args.steps
 
     # max over ranks
     if world > 1:
@@ -462,7 +488,11 @@ def run_gpu(args, rank, world, local_rank):
                    "parallelism": f"{world} independent shard(s), no collective"},
         "roofline": roofline,
         "e2e": {"value": rows_total / (e_ms / 1e3), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms},
+                "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
+                "method": "public API per step: pinned-host inputs copied in, call, O and LSE "
+                          "copied out; step i+1's copies overlap step i on a second stream "
+                          "(two device input sets); no L2 flush between steps (each step's "
+                          "copies replace the inputs)"},
         "gpu_launches": launches,
         "clocks": clocks,
         "wall_s_timed_region": wall,
