@@ -184,6 +184,17 @@ qsa_status qsa_sparse_mla_prefill(const void* q, const void* kv_cache, const int
                                   int32_t n_heads, int32_t d_qk, int32_t d_v, int32_t topk,
                                   float scale, int32_t union_g, int64_t n_kv_slots, void* stream);
 
+/* MLA shape over a paged latent cache: indices are logical positions of each row's request,
+ * translated through page_table in the kernels exactly as in qsa_sparse_prefill_paged
+ * (kv_cache [n_pages * page_size, d_qk]); everything else as qsa_sparse_mla_prefill. */
+qsa_status qsa_sparse_mla_prefill_paged(const void* q, const void* kv_cache, const int32_t* indices,
+                                        const int32_t* topk_len, const int32_t* cu_seqlens_q,
+                                        const int32_t* kv_lens, const int32_t* page_table,
+                                        void* out, float* lse, int64_t n_rows, int32_t n_requests,
+                                        int32_t pages_per_req, int32_t page_size, int64_t n_pages,
+                                        int32_t n_heads, int32_t d_qk, int32_t d_v, int32_t topk,
+                                        float scale, int32_t union_g, void* stream);
+
 /* Host-only geometry selection for qsa_sparse_mla_prefill (stages = latent ring depth). */
 qsa_status qsa_select_mla_geometry(int32_t n_heads, int32_t union_g, int32_t topk, int32_t d_qk,
                                    int32_t d_v, int64_t n_rows, int32_t num_sms,
@@ -274,7 +285,7 @@ qsa_status qsa_select_geometry(int32_t n_qheads, int32_t n_kvheads, int32_t unio
  * 1 = TMA tile::gather4) and its ring shape, and nothing else.  Writes the elapsed GPU time in
  * milliseconds to *ms_out (host pointer) and synchronises `stream`.  The pages motivate
  * it: the gather is the share of the sparse kernel that grows on newer parts ("DSA prefill ...
- * triton_sparse_mla", Speed Tests), so the kernel is judged against the measured gather rate. */
+ * triton_sparse_mla", Speed Tests), so the kernel's gather rate is reported against this one. */
 qsa_status qsa_probe_gather_ceiling(const void* cache, int64_t n_rows, const int32_t* rows,
                                     int64_t n_table_pieces, int32_t pieces_per_cta,
                                     int32_t engine, float* ms_out, void* stream);

@@ -122,3 +122,51 @@ def test_mla_full_size_8k(B, G):
                                                                      8189, 8190, 8191]]))
     O, L = ref(w, rows=rows)
     assert_parity(out, lse, O, L, rows=rows, what=f"mla_8k G={G}")
+
+
+def paged_mla_case(seed=70, ps=64, kv_lens=(700, 1300, 400), rows=(30, 50, 20), topk=512, heads=8):
+    """Three requests whose latent rows live on shuffled pages of one cache (two spare pages),
+    rows at the end of each request selecting distinct causal positions of it; returns the
+    paged call's inputs."""
+    rng = np.random.default_rng(seed)
+    pages = [-(-L // ps) for L in kv_lens]
+    n_pages = sum(pages) + 2
+    perm = rng.permutation(n_pages)
+    cache = W.randn_bf16(rng, (n_pages * ps, 576))
+    table = np.full((len(kv_lens), max(pages) + 1), -1, dtype=np.int32)
+    off = 0
+    for i, n in enumerate(pages):
+        table[i, :n] = perm[off:off + n]
+        off += n
+    R = sum(rows)
+    q = W.randn_bf16(rng, (R, heads, 576))
+    logical = np.full((R, topk), -1, dtype=np.int32)
+    cu = np.concatenate([[0], np.cumsum(rows)]).astype(np.int32)
+    r = 0
+    for i, (L, n) in enumerate(zip(kv_lens, rows)):
+        for pos in range(L - n, L):
+            m = min(pos + 1, topk)
+            logical[r, :m] = rng.choice(pos + 1, size=m, replace=False)
+            r += 1
+    return q, cache, logical, cu, np.asarray(kv_lens, dtype=np.int32), table, ps, n_pages
+
+
+@pytest.mark.parametrize("G", [0, 2])
+def test_mla_paged_matches_oracle_and_plain_entry(B, G):
+    import torch
+    q, cache, logical, cu, kvl, table, ps, n_pages = paged_mla_case()
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+    dq, dkv = bf(q), bf(cache)
+    out, lse = B.sparse_mla_prefill_paged(dq, dkv, i32(logical), None, i32(cu), i32(kvl), i32(table),
+                                          ps, 1.0 / 24.0, n_pages=n_pages, union_g=G)
+    torch.cuda.synchronize()
+    assert B.device_status() == 0
+    phys = oracle.physical_indices(logical, cu, kvl, table, ps, n_pages)
+    O, L = oracle.sparse_mla_prefill(q, cache, phys, None, 1.0 / 24.0)
+    assert_parity(out, lse, O, L, what=f"mla paged G={G}")
+    out2, lse2 = B.sparse_mla_prefill(dq, dkv, i32(np.where(phys >= 0, phys, -1)), None, 1.0 / 24.0,
+                                      union_g=G)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse, lse2)

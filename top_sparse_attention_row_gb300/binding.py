@@ -25,7 +25,7 @@ EXPORTED = ["qsa_sparse_prefill", "qsa_sparse_prefill_ex", "qsa_workspace_bytes"
             "qsa_sparse_prefill_noalloc", "qsa_probe_gather_ceiling",
             "qsa_sparse_prefill_paged", "qsa_sparse_mla_prefill", "qsa_select_mla_geometry",
             "qsa_page_mark", "qsa_page_split", "qsa_split_touched_pages",
-            "qsa_sparse_prefill_fp8", "qsa_debug_stall_next_call"]
+            "qsa_sparse_prefill_fp8", "qsa_debug_stall_next_call", "qsa_sparse_mla_prefill_paged"]
 
 # Size of the library-owned scratch array used by qsa_sparse_prefill_noalloc (include/qsa.h).
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -92,6 +92,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qsa_sparse_prefill_fp8.restype = ctypes.c_int
     lib.qsa_debug_stall_next_call.argtypes = []
     lib.qsa_debug_stall_next_call.restype = None
+    lib.qsa_sparse_mla_prefill_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, i32,
+                                                 i32, i64, i32, i32, i32, i32, f32, i32, vp]
+    lib.qsa_sparse_mla_prefill_paged.restype = ctypes.c_int
     lib.qsa_probe_gather_ceiling.argtypes = [vp, i64, vp, i64, i32, i32, ctypes.POINTER(f32), vp]
     lib.qsa_probe_gather_ceiling.restype = ctypes.c_int
     lib.qsa_workspace_bytes.argtypes = [i64, i32, i32]
@@ -294,6 +297,38 @@ def sparse_mla_prefill(q, kv_cache, indices, topk_len, scale: float, *, out=None
                                     _ptr(lse), R, H, Dqk, Dv, topk, float(scale), int(union_g),
                                     int(n_kv_slots), _stream_ptr(stream))
     _check(st, "qsa_sparse_mla_prefill")
+    return out, lse
+
+
+def sparse_mla_prefill_paged(q, kv_cache, indices, topk_len, cu_seqlens_q, kv_lens, page_table,
+                             page_size: int, scale: float, *, n_pages: int = 0, out=None, lse=None,
+                             union_g: int = 0, want_lse: bool = True, stream=None):
+    """MLA shape over a paged latent cache (qsa_sparse_mla_prefill_paged): logical indices,
+    ragged row offsets and a page table as in sparse_prefill_paged."""
+    import torch
+    lib = load_library()
+    _require(q, torch.bfloat16, "q", 3)
+    _require(kv_cache, torch.bfloat16, "kv_cache", 2)
+    _require(indices, torch.int32, "indices", 2)
+    _require(topk_len, torch.int32, "topk_len", 1)
+    _require(cu_seqlens_q, torch.int32, "cu_seqlens_q", 1)
+    _require(kv_lens, torch.int32, "kv_lens", 1)
+    _require(page_table, torch.int32, "page_table", 2)
+    R, H, Dqk = q.shape
+    n_req = page_table.shape[0]
+    if cu_seqlens_q.shape[0] != n_req + 1 or (kv_lens is not None and kv_lens.shape[0] != n_req):
+        raise ValueError("cu_seqlens_q / kv_lens must match the page table's requests")
+    if out is None:
+        out = torch.empty((R, H, 512), dtype=torch.bfloat16, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty((R, H), dtype=torch.float32, device=q.device)
+    st = lib.qsa_sparse_mla_prefill_paged(_ptr(q), _ptr(kv_cache), _ptr(indices), _ptr(topk_len),
+                                          _ptr(cu_seqlens_q), _ptr(kv_lens), _ptr(page_table),
+                                          _ptr(out), _ptr(lse), R, n_req, page_table.shape[1],
+                                          int(page_size), int(n_pages), H, Dqk, 512,
+                                          indices.shape[1], float(scale), int(union_g),
+                                          _stream_ptr(stream))
+    _check(st, "qsa_sparse_mla_prefill_paged")
     return out, lse
 
 

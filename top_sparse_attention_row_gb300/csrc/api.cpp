@@ -435,6 +435,31 @@ qsa_status page_split_args(const void* src_pool, void* dst_pool, int64_t n_src_p
   return QSA_OK;
 }
 
+// Paged-call metadata -> PagedAddr and the physical slot count (0 = unchecked).
+qsa_status paged_args(const int32_t* cu_seqlens_q, const int32_t* kv_lens, const int32_t* page_table,
+                      int32_t n_requests, int32_t pages_per_req, int32_t page_size,
+                      int64_t n_pages, int32_t n_kvheads, qsa::PagedAddr* pa, int64_t* n_kv_slots) {
+  if (!cu_seqlens_q || !page_table) return QSA_ERR_INVALID_ARG;
+  if (n_requests < 1 || pages_per_req < 1 || page_size < 1 || n_pages < 0)
+    return QSA_ERR_INVALID_ARG;
+  *n_kv_slots = 0;
+  if (n_pages > 0) {
+    *n_kv_slots = n_pages * page_size;
+    if (n_kvheads > 0 && *n_kv_slots * n_kvheads >= INT32_MAX) return QSA_ERR_UNSUPPORTED;
+  }
+  pa->page_table = page_table;
+  pa->cu_seqlens_q = cu_seqlens_q;
+  pa->kv_lens = kv_lens;
+  pa->n_requests = n_requests;
+  pa->pages_per_req = pages_per_req;
+  pa->page_size = page_size;
+  pa->page_shift = -1;
+  for (int s = 0; s < 31; ++s)
+    if ((int32_t{1} << s) == page_size) pa->page_shift = s;
+  pa->n_pages = n_pages;
+  return QSA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -544,27 +569,29 @@ qsa_status qsa_sparse_prefill_paged(const void* q, const void* k_cache, const vo
                                     int32_t page_size, int64_t n_pages, int32_t n_qheads,
                                     int32_t n_kvheads, int32_t head_dim, int32_t topk, float scale,
                                     int32_t union_g, void* stream) {
-  if (!cu_seqlens_q || !page_table) return QSA_ERR_INVALID_ARG;
-  if (n_requests < 1 || pages_per_req < 1 || page_size < 1 || n_pages < 0)
-    return QSA_ERR_INVALID_ARG;
-  int64_t n_kv_slots = 0;
-  if (n_pages > 0) {
-    n_kv_slots = n_pages * page_size;
-    if (n_kvheads > 0 && n_kv_slots * n_kvheads >= INT32_MAX) return QSA_ERR_UNSUPPORTED;
-  }
   qsa::PagedAddr pa{};
-  pa.page_table = page_table;
-  pa.cu_seqlens_q = cu_seqlens_q;
-  pa.kv_lens = kv_lens;
-  pa.n_requests = n_requests;
-  pa.pages_per_req = pages_per_req;
-  pa.page_size = page_size;
-  pa.page_shift = -1;
-  for (int s = 0; s < 31; ++s)
-    if ((int32_t{1} << s) == page_size) pa.page_shift = s;
-  pa.n_pages = n_pages;
+  int64_t n_kv_slots = 0;
+  const qsa_status st = paged_args(cu_seqlens_q, kv_lens, page_table, n_requests, pages_per_req,
+                                   page_size, n_pages, n_kvheads, &pa, &n_kv_slots);
+  if (st != QSA_OK) return st;
   return run(q, k_cache, v_cache, indices, topk_len, out, lse, n_rows, n_qheads, n_kvheads,
              head_dim, topk, scale, union_g, n_kv_slots, nullptr, 0, nullptr, &pa, stream);
+}
+
+qsa_status qsa_sparse_mla_prefill_paged(const void* q, const void* kv_cache, const int32_t* indices,
+                                        const int32_t* topk_len, const int32_t* cu_seqlens_q,
+                                        const int32_t* kv_lens, const int32_t* page_table,
+                                        void* out, float* lse, int64_t n_rows, int32_t n_requests,
+                                        int32_t pages_per_req, int32_t page_size, int64_t n_pages,
+                                        int32_t n_heads, int32_t d_qk, int32_t d_v, int32_t topk,
+                                        float scale, int32_t union_g, void* stream) {
+  qsa::PagedAddr pa{};
+  int64_t n_kv_slots = 0;
+  const qsa_status st = paged_args(cu_seqlens_q, kv_lens, page_table, n_requests, pages_per_req,
+                                   page_size, n_pages, 1, &pa, &n_kv_slots);
+  if (st != QSA_OK) return st;
+  return run_mla(q, kv_cache, indices, topk_len, out, lse, n_rows, n_heads, d_qk, d_v, topk, scale,
+                 union_g, n_kv_slots, &pa, stream);
 }
 
 qsa_status qsa_sparse_prefill_ex(const void* q, const void* k_cache, const void* v_cache,
