@@ -110,7 +110,8 @@ qsa_status select(int32_t Hq, int32_t Hkv, int32_t union_g, int32_t topk, int32_
   g->stages = stages;
   g->grid = static_cast<int>(grid);
   g->smem_bytes = qsa::smem_layout(np, stages, slot_cap).total;
-  g->tmem_cols = pow2_at_least((qsa::kSBufs + 2) * np);   // S^T buffers + two O^T halves
+  // S^T buffers (lookahead + 1) + two O^T halves
+  g->tmem_cols = pow2_at_least((qsa::lookahead_for(G > 1) + 3) * np);
   g->slot_cap = slot_cap;
   g->n_items = n_items;
   g->n_groups = static_cast<int>(n_groups);

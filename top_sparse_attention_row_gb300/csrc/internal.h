@@ -23,11 +23,11 @@ constexpr int kProducerWarp0 = 6;            // first gather warp
 constexpr int kProducerWarps = 6;            // gather warps, each owning one ring stage
 constexpr int kThreads = 32 * (kProducerWarp0 + kProducerWarps);
 constexpr int kMinStages = 4;                // ring must hold V(j) and K(j+1) together
-// MMA issue lookahead of the d=256 kernel: QK^T(j+L) is issued before P.V(j).  L = 1 measured
-// fastest (L = 2 and 3 gave the softmax more slack but cost 1 % on every workload: the
-// softmax is not on the critical path, the gather is).  kSBufs = L + 1 S^T buffers.
-constexpr int kLookahead = 1;
-constexpr int kSBufs = kLookahead + 1;
+// MMA issue lookahead of the d=256 kernel: QK^T(j+L) is issued before P.V(j), with L + 1 S^T
+// buffers.  Measured on GB300: per-token tiles (N = 16) run fastest at L = 1 (L = 2 or 3 cost
+// 1 %); union tiles (N = 32, twice the softmax work per tile) gain 3 % at L = 2.
+__host__ __device__ constexpr int lookahead_for(bool union_mode) { return union_mode ? 2 : 1; }
+constexpr int kMaxSBufs = 3;
 constexpr int kMaxStages = 8;
 constexpr int kSmemLimit = 232448;           // 227 KiB opt-in dynamic shared memory
 constexpr int kUnionMaxSmem = 200 * 1024;    // union-build kernel shared-memory cap
@@ -109,9 +109,9 @@ __host__ __device__ inline SmemLayout smem_layout(int np, int stages, int slot_c
   L.pbuf = L.qbuf + L.q_bytes;          // one Q tile buffer
   L.slots = L.pbuf + 2 * L.p_bytes;
   L.bars = L.slots + 2 * slot_cap * 4;
-  // full[st], empty[st], s_full[kSBufs], s_free[kSBufs], p_full[2], pv_done[2], item_full[2],
-  // item_empty[2], q_empty, q_full, final, landed[st] (FP8 caches)
-  L.misc = L.bars + (3 * stages + 2 * kSBufs + 11) * 8;
+  // full[st], empty[st], s_full[kMaxSBufs], s_free[kMaxSBufs], p_full[2], pv_done[2],
+  // item_full[2], item_empty[2], q_empty, q_full, final, landed[st] (FP8 caches)
+  L.misc = L.bars + (3 * stages + 2 * kMaxSBufs + 11) * 8;
   // info[2][8] int32, red[2][4][np] float, tmem base, abort flag, vote[3]
   int misc_bytes = 2 * 8 * 4 + 2 * 4 * np * 4 + 32;
   L.total = L.misc + misc_bytes + 1024;   // + alignment slack for the 1024-aligned base

@@ -124,29 +124,32 @@ __device__ __forceinline__ void sts_v4(uint32_t addr, uint4 v) {
                : "memory");
 }
 
-// MMA issue order of an item with lookahead L (kLookahead): at step j the thread issues
+// MMA issue order of an item with lookahead L (lookahead_for): at step j the thread issues
 // S^T(j) = K(j).Q^T (j < nt) and then O^T += V(j-L)^T.P^T(j-L) (j >= L), so the softmax of
 // tile j has the issue time of L further QK^T groups and L-1 P.V groups before P.V(j) needs it.
 // Pieces (two per entry: dims 0-127, 128-255) enter the ring in exactly that order:
 //   K(0) .. K(L-1), then K(j), V(j-L) for L <= j < nt, then the remaining V.
 
-__device__ __forceinline__ int k_entry(int j) { return j + (j > kLookahead ? j - kLookahead : 0); }
+template <int L>
+__device__ __forceinline__ int k_entry(int j) { return j + (j > L ? j - L : 0); }
+template <int L>
 __device__ __forceinline__ int v_entry(int i, int nt) {
-  return (i + kLookahead + 1 < nt ? i + kLookahead + 1 : nt) + i;
+  return (i + L + 1 < nt ? i + L + 1 : nt) + i;
 }
+template <int L>
 __device__ __forceinline__ void piece_of(int q, int nt, int& tile, int& is_v, int& half) {
   const int e = q >> 1;
   half = q & 1;
-  if (nt <= kLookahead) {
+  if (nt <= L) {
     is_v = e >= nt;
     tile = is_v ? e - nt : e;
-  } else if (e < kLookahead) {
+  } else if (e < L) {
     is_v = 0;
     tile = e;
-  } else if (e < 2 * nt - kLookahead) {
-    const int d = e - kLookahead, j = kLookahead + (d >> 1);
+  } else if (e < 2 * nt - L) {
+    const int d = e - L, j = L + (d >> 1);
     is_v = d & 1;
-    tile = is_v ? j - kLookahead : j;
+    tile = is_v ? j - L : j;
   } else {
     is_v = 1;
     tile = e - nt;
@@ -157,7 +160,6 @@ __device__ __forceinline__ void cp_async_16_zfill(uint32_t dst, const void* src,
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 // Arrive (without a pending-count increment) on `bar` once all earlier cp.async of this thread
 // have completed.
 __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
@@ -190,6 +192,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t base = (raw_u32 + 1023u) & ~1023u;
   uint8_t* const gbase = smem_raw + (base - raw_u32);
 
+  constexpr int kLookahead = lookahead_for(UNION);
+  constexpr int kSBufs = kLookahead + 1;
   const int slot_cap = UNION ? 0 : p.slot_cap;
   const SmemLayout L = smem_layout(NP, p.stages, slot_cap);
   const int R = p.stages;
@@ -198,8 +202,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t b_full = base + L.bars;
   const uint32_t b_empty = b_full + 8 * R;
   const uint32_t b_sfull = b_empty + 8 * R;     // [kSBufs]
-  const uint32_t b_sfree = b_sfull + 8 * kSBufs;
-  const uint32_t b_pfull = b_sfree + 8 * kSBufs;
+  const uint32_t b_sfree = b_sfull + 8 * kMaxSBufs;
+  const uint32_t b_pfull = b_sfree + 8 * kMaxSBufs;
   const uint32_t b_pvdone = b_pfull + 16;
   const uint32_t b_itemfull = b_pvdone + 16;
   const uint32_t b_itemempty = b_itemfull + 16;
@@ -372,7 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t st = s % R;
         if (static_cast<int>(st) % W != pw) continue;
         int tile, is_v, half;
-        piece_of(q, nt, tile, is_v, half);
+        piece_of<kLookahead>(q, nt, tile, is_v, half);
         const int t0 = tile * kTileTokens;
         // union slots of the tile: lane holds tokens 4*lane .. 4*lane+3 (loaded before the
         // stage wait so the wait hides the load)
@@ -525,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < nt + kLookahead; ++j) {
         if (j < nt) {
           // S^T(j) = K(j) . Q^T
-          const uint32_t s_lo = seq + 2 * k_entry(j), s_hi = s_lo + 1;
+          const uint32_t s_lo = seq + 2 * k_entry<kLookahead>(j), s_hi = s_lo + 1;
           const uint32_t jsj = js + j, sb = jsj % kSBufs, sph = (jsj / kSBufs) & 1;
           bool ok = wait_bar(b_full + 8 * (s_lo % R), (s_lo / R) & 1, abort_flag, kSiteStageFull);
           ok = ok && wait_bar(b_full + 8 * (s_hi % R), (s_hi / R) & 1, abort_flag, kSiteStageFull);
@@ -558,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // O^T += V(j-L)^T . P^T(j-L)
           const int jp = j - kLookahead;
           const uint32_t jsp = js + jp, pb = jsp & 1, pph = (jsp >> 1) & 1;
-          const uint32_t s_vlo = seq + 2 * v_entry(jp, nt), s_vhi = s_vlo + 1;
+          const uint32_t s_vlo = seq + 2 * v_entry<kLookahead>(jp, nt), s_vhi = s_vlo + 1;
           bool ok = wait_bar(b_pfull + 8 * pb, pph, abort_flag, kSitePFull);
           ok = ok && wait_bar(b_full + 8 * (s_vlo % R), (s_vlo / R) & 1, abort_flag, kSiteStageFull);
           ok = ok && wait_bar(b_full + 8 * (s_vhi % R), (s_vhi / R) & 1, abort_flag, kSiteStageFull);
