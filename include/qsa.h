@@ -212,8 +212,8 @@ qsa_status qsa_select_mla_geometry(int32_t n_heads, int32_t union_g, int32_t top
  *     slots of the source pool; slots past the pool are ignored).  No atomics, no host read.
  *   qsa_page_split: copies every destination page whose source page is marked (mark NULL =
  *     every page).  Destination pages of unmarked source pages are left untouched.  The launch
- *     grid is n_src_pages * ratio CTAs whatever the mark holds, so a captured CUDA graph
- *     replays it; an unmarked page costs one byte load.
+ *     grid is one CTA per source page whatever the mark holds, so a captured CUDA graph replays
+ *     it; an unmarked page costs one byte load.
  *   qsa_split_touched_pages: mark + masked split in one call.
  * Requirements: src_pool and dst_pool 16-byte aligned (host pointer section_bytes, each entry a
  * positive multiple of 16, 1 <= n_sections <= 8), src_page_size a multiple of dst_page_size,

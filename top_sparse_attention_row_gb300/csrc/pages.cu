@@ -5,10 +5,10 @@
 //  * page_mark_kernel: one thread per index element; every valid token slot t sets
 //    mark[t / src_page_size] = 1.  Threads that mark the same page store the same byte, so no
 //    atomic is needed.
-//  * page_split_kernel: one CTA per destination page (a fixed grid of n_src_pages x ratio, so
-//    the launch shape does not depend on the indices and a captured graph replays it).  A CTA
-//    whose source page is unmarked returns after a one-byte load; otherwise it copies its
-//    sub-page of every section with 16-byte loads and stores.
+//  * page_split_kernel: one CTA per source page (a fixed grid of n_src_pages, so the launch
+//    shape does not depend on the indices and a captured graph replays it).  A CTA whose page is
+//    unmarked returns after a one-byte load; otherwise it copies every sub-page of every section
+//    with 16-byte loads and stores, four in flight per thread.
 // Page layout (both pools): a page of P tokens holds its sections one after another, section k
 // being P x section_bytes[k] bytes, token-major inside the section.  Destination page
 // p * ratio + i holds source tokens i * dst_page_size .. (i + 1) * dst_page_size - 1 of source
@@ -40,24 +40,31 @@ __global__ void __launch_bounds__(kSplitThreads)
     page_split_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
                       const uint8_t* __restrict__ mark, int32_t ratio, int32_t dst_page_size,
                       PageSections sec) {
-  const int64_t q = blockIdx.x;                       // destination page
-  const int64_t p = q / ratio;                        // its source page
-  const int32_t i = static_cast<int32_t>(q - p * ratio);
+  const int64_t p = blockIdx.x;                       // source page
   if (mark != nullptr && __ldg(mark + p) == 0) return;
-  const int64_t src_page_bytes = static_cast<int64_t>(ratio) * dst_page_size * sec.token_bytes;
   const int64_t dst_page_bytes = static_cast<int64_t>(dst_page_size) * sec.token_bytes;
-  const uint8_t* sp = src + p * src_page_bytes;
-  uint8_t* dp = dst + q * dst_page_bytes;
+  const uint8_t* sp = src + p * ratio * dst_page_bytes;
   int64_t src_off = 0, dst_off = 0;
   for (int k = 0; k < sec.n; ++k) {
-    const int64_t sb = sec.bytes[k];
-    // the sub-page's run of this section is contiguous in both pools
-    const uint4* s4 = reinterpret_cast<const uint4*>(sp + src_off + static_cast<int64_t>(i) * dst_page_size * sb);
-    uint4* d4 = reinterpret_cast<uint4*>(dp + dst_off);
-    const int64_t n16 = dst_page_size * sb / 16;
-    for (int64_t e = threadIdx.x; e < n16; e += kSplitThreads) d4[e] = __ldg(s4 + e);
-    src_off += static_cast<int64_t>(ratio) * dst_page_size * sb;
-    dst_off += static_cast<int64_t>(dst_page_size) * sb;
+    const int64_t run = static_cast<int64_t>(dst_page_size) * sec.bytes[k];   // one sub-page
+    const int64_t n16 = run / 16;
+    for (int i = 0; i < ratio; ++i) {
+      // sub-page i of section k: contiguous in both pools
+      const uint4* s4 = reinterpret_cast<const uint4*>(sp + src_off + i * run);
+      uint4* d4 = reinterpret_cast<uint4*>(dst + (p * ratio + i) * dst_page_bytes + dst_off);
+      int64_t e = threadIdx.x;
+      for (; e + 3 * kSplitThreads < n16; e += 4 * kSplitThreads) {
+        const uint4 a0 = __ldg(s4 + e), a1 = __ldg(s4 + e + kSplitThreads);
+        const uint4 a2 = __ldg(s4 + e + 2 * kSplitThreads), a3 = __ldg(s4 + e + 3 * kSplitThreads);
+        d4[e] = a0;
+        d4[e + kSplitThreads] = a1;
+        d4[e + 2 * kSplitThreads] = a2;
+        d4[e + 3 * kSplitThreads] = a3;
+      }
+      for (; e < n16; e += kSplitThreads) d4[e] = __ldg(s4 + e);
+    }
+    src_off += static_cast<int64_t>(ratio) * run;
+    dst_off += run;
   }
 }
 
@@ -79,7 +86,7 @@ cudaError_t launch_page_split(const void* src, void* dst, const uint8_t* mark, i
                               int32_t src_page_size, int32_t dst_page_size,
                               const PageSections& sec, cudaStream_t stream) {
   const int32_t ratio = src_page_size / dst_page_size;
-  const int64_t grid = n_src_pages * ratio;
+  const int64_t grid = n_src_pages;
   if (grid == 0) return cudaSuccess;
   page_split_kernel<<<static_cast<unsigned>(grid), kSplitThreads, 0, stream>>>(
       static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dst), mark, ratio, dst_page_size, sec);
