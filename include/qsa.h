@@ -31,6 +31,9 @@
  *  - A row with no valid slot gets O = 0 and LSE = -inf.  A slot listed twice in one row is
  *    weighted twice (per-token path).
  *  - Results are deterministic: no atomics take part in any reduction.
+ *  - Environment: QSA_LOG=1 prints one stderr line per attention call with the selected launch
+ *    geometry; QSA_GATHER=cpasync selects cp.async copies instead of TMA gather4 for the bf16
+ *    d=256 kernel (same results, bit for bit).
  */
 #ifndef QSA_H_
 #define QSA_H_

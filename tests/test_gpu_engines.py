@@ -75,3 +75,18 @@ def test_gather_ceiling_probe(B, engine):
     table = torch.randint(0, n_rows, (512, 128), generator=g, dtype=torch.int32).cuda()
     gbs = B.probe_gather_ceiling(cache, table, pieces_per_cta=64, engine=engine)
     assert np.isfinite(gbs) and gbs > 100.0
+
+
+def test_geometry_log_line(B):
+    """QSA_LOG=1 prints the selected geometry, one line per attention call."""
+    code = (f"import sys; sys.path.insert(0, {ROOT!r}); sys.path.insert(0, {os.path.join(ROOT, 'tests')!r})\n"
+            "import torch\nfrom helpers import to_device\n"
+            "from top_sparse_attention_row_gb300 import binding as B, workloads as W\n"
+            "w = W.make_tiny(); q, k, v, idx, tl = to_device(w)\n"
+            "B.sparse_prefill(q, k, v, idx, tl, w.scale); B.sparse_prefill(q, k, v, idx, tl, w.scale, union_g=2)\n"
+            "torch.cuda.synchronize()\n")
+    r = subprocess.run([sys.executable, "-c", code], env=dict(os.environ, QSA_LOG="1"),
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stderr.splitlines() if l.startswith("qsa: d=256")]
+    assert len(lines) == 2 and "union=1" in lines[0] and "union=2" in lines[1], r.stderr

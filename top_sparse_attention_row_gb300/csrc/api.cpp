@@ -3,6 +3,7 @@
 // before any CUDA call, so a bad call enqueues nothing.
 #include <atomic>
 #include <cmath>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 
@@ -216,6 +217,15 @@ bool gather_engine_is_tma() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// QSA_LOG=1: one stderr line per attention call with the geometry the selector chose.
+bool log_geometry() {
+  static const bool on = [] {
+    const char* e = std::getenv("QSA_LOG");
+    return e != nullptr && std::strcmp(e, "1") == 0;
+  }();
+  return on;
+}
+
 // Device checks: compute capability 10.3 and the SM count (cached per device).
 qsa_status device_sms(int32_t* sms) {
   static std::atomic<int32_t> cache[64];
@@ -272,6 +282,14 @@ qsa_status run(const void* q, const void* k_cache, const void* v_cache, const in
               &stepped, fp8 != nullptr);
   if (st != QSA_OK) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  if (log_geometry())
+    std::fprintf(stderr,
+                 "qsa: d=256 rows=%lld heads=%d/%d topk=%d union=%d%s -> N=%d cols=%d chunks=%d "
+                 "stages=%d grid=%d smem=%d tmem=%d items=%lld%s%s\n",
+                 static_cast<long long>(n_rows), n_qheads, n_kvheads, topk, g.union_g,
+                 fp8 ? " fp8" : (paged ? " paged" : ""), g.np, g.cols, g.head_chunks, g.stages,
+                 g.grid, g.smem_bytes, g.tmem_cols, static_cast<long long>(g.n_items),
+                 fell_back ? " (union fallback)" : "", stepped ? " (stepped down)" : "");
 
   qsa::PrefillParams p{};
   p.q = static_cast<const uint16_t*>(q);
@@ -364,6 +382,13 @@ qsa_status run_mla(const void* q, const void* kv_cache, const int32_t* indices,
   st = select_mla(n_heads, union_g, topk, d_qk, d_v, n_rows, sms, &g, &fell_back);
   if (st != QSA_OK) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  if (log_geometry())
+    std::fprintf(stderr,
+                 "qsa: mla rows=%lld heads=%d topk=%d union=%d%s -> N=%d cols=%d chunks=%d "
+                 "latent_stages=%d grid=%d smem=%d tmem=%d items=%lld%s\n",
+                 static_cast<long long>(n_rows), n_heads, topk, g.union_g, paged ? " paged" : "",
+                 g.np, g.cols, g.head_chunks, g.pair_stages, g.grid, g.smem_bytes, g.tmem_cols,
+                 static_cast<long long>(g.n_items), fell_back ? " (union fallback)" : "");
 
   qsa::MlaParams p{};
   p.q = static_cast<const uint16_t*>(q);
