@@ -84,7 +84,8 @@ qsa_status select(int32_t Hq, int32_t Hkv, int32_t union_g, int32_t topk, int32_
     slot_cap = 0;
   }
   int stages = 0;
-  for (int s = qsa::kMaxStages; s >= qsa::kMinStages; --s) {
+  // even stage counts: a piece pair's two stages share one empty barrier
+  for (int s = qsa::kMaxStages; s >= qsa::kMinStages; s -= 2) {
     if (qsa::smem_layout(np, s, slot_cap).total <= qsa::kSmemLimit) {
       stages = s;
       break;
@@ -92,7 +93,7 @@ qsa_status select(int32_t Hq, int32_t Hkv, int32_t union_g, int32_t topk, int32_
   }
   if (stages == 0) return QSA_ERR_UNSUPPORTED;   // per-token slot list too large for topk
   if (forced && forced->stages > 0) {
-    int want = forced->stages < qsa::kMinStages ? qsa::kMinStages : forced->stages;
+    int want = forced->stages < qsa::kMinStages ? qsa::kMinStages : forced->stages & ~1;
     if (want > stages) {
       *stepped = true;
       want = stages;

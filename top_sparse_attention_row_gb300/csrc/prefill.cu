@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < R; ++s) {
       // owner warp: expect_tx (TMA), one arrival after converting (FP8), or 32 lane arrivals
       mbar_init(b_full + 8 * s, (p.gather_tma || FP8) ? 1 : 32);
-      mbar_init(b_empty + 8 * s, 1);
+      mbar_init(b_empty + 8 * s, 1);   // stage pairs share empty[pair]: [0, R/2) are used
       if (FP8) mbar_init(b_land + 8 * s, 1);
     }
     for (int b = 0; b < kSBufs; ++b) {
@@ -389,7 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           uy.w = t + 3 < nv ? ul[t + 3] * p.n_kvheads + I.kvh : p.pad_row;
         }
         const uint32_t par = ((s / R) & 1) ^ 1;
-        if (!__all_sync(0xffffffffu, wait_bar(b_empty + 8 * st, par, abort_flag, kSiteStageEmpty))) {
+        const uint32_t empty_bar = b_empty + 8 * (st >> 1);   // the stage pair's barrier
+        if (!__all_sync(0xffffffffu, wait_bar(empty_bar, par, abort_flag, kSiteStageEmpty))) {
           aborted = true;
           break;
         }
@@ -551,8 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint64_t bq = sw128_desc(qaddr + (kk >> 2) * (NP * 128) + (kk & 3) * 32, 16, 1024);
               tc_mma(tm_s0 + sb * NP, a, bq, kIdescQK, kk > 0 ? 1u : 0u);
             }
-            tc_commit(b_empty + 8 * (s_lo % R));
-            tc_commit(b_empty + 8 * (s_hi % R));
+            tc_commit(b_empty + 8 * ((s_lo % R) >> 1));   // one commit frees the stage pair
             tc_commit(b_sfull + 8 * sb);
             if (j == nt - 1) tc_commit(b_qempty);
           }
@@ -584,8 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_mma(tm_o + hh * NP, a, bp, kIdescPV, (jp == 0 && kk == 0) ? 0u : 1u);
               }
             }
-            tc_commit(b_empty + 8 * (s_vlo % R));
-            tc_commit(b_empty + 8 * (s_vhi % R));
+            tc_commit(b_empty + 8 * ((s_vlo % R) >> 1));
             tc_commit(b_pvdone + 8 * pb);
           }
           __syncwarp();
