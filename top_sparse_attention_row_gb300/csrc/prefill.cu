@@ -16,15 +16,20 @@
 //    instead of padding the head dimension up to the MMA M.
 //      S^T[128 x N]  = K_tile[128 x 256] . Q^T            (A: K-major SW128, B: K-major SW128)
 //      O^T[256 x N] += V_tile^T[256 x 128] . P^T[128 x N]  (A: MN-major SW128, B: K-major SW128)
-//    Accumulators live in tensor memory: two S buffers and the two 128-row halves of O^T.
+//    Accumulators live in tensor memory: L + 1 S buffers (L = MMA lookahead: 1 per-token, 2
+//    union) and the two 128-row halves of O^T.
 //  * K/V rows are gathered into a ring of 32 KiB stages (128 slots x 128 dims, 128-byte
-//    swizzled rows) in exactly the order the MMA consumes them -- K(0), K(1), V(0), K(2), V(1),
-//    ..., V(nt-1), two half-row pieces each -- so the ring drains FIFO.  Each of six producer
-//    warps owns one stage and gathers whole pieces into it: per-SM gather bandwidth grows with
-//    the number of warps issuing copies concurrently.  Two gather engines: cp.async 16-byte
-//    copies (default; lanes arrive on the stage barrier as their copies land and the MMA
-//    thread fences them into the async proxy) and TMA tile::gather4 (4 slots x 128 B per
-//    instruction, out-of-bounds rows zero-filled).
+//    swizzled rows) in exactly the order the MMA consumes them -- with L = 1: K(0), K(1), V(0),
+//    K(2), V(1), ..., V(nt-1), two half-row pieces each -- so the ring drains FIFO; one commit
+//    releases a piece pair's two stages.  Each of six producer warps owns one stage and gathers
+//    whole pieces into it: per-SM gather bandwidth grows with the number of warps issuing
+//    copies concurrently.  Two gather engines: TMA tile::gather4 (default; 4 slots x 128 B per
+//    instruction, out-of-bounds rows zero-filled) and cp.async 16-byte copies (lanes arrive on
+//    the stage barrier as their copies land and the MMA thread fences them into the async
+//    proxy).
+//  * FP8 caches (template FP8): e4m3 half-rows land in the upper half of the stage and the
+//    owning producer rewrites the stage in place as the fp16 tile; the MMAs run fp16 operands,
+//    the K page scale multiplies the logit and the V page scale the probability fed to P.V.
 //  * Online softmax in registers, one thread per slot (tensor-memory lane).  The running max
 //    is only raised when a tile's logits exceed it by more than 2^8 (log2 domain), so the
 //    O^T rescale through tensor memory is rare; the result is exact either way because O and
