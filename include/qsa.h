@@ -285,7 +285,7 @@ qsa_status qsa_select_geometry(int32_t n_qheads, int32_t n_kvheads, int32_t unio
  * in `rows` ([n_table_pieces, 128] int32 row numbers < n_rows of a [n_rows, 256] bf16 cache,
  * 16-byte aligned), 128 rows (32 KiB) per piece, `pieces_per_cta` pieces on every SM, into shared
  * memory with one of the attention kernel's gather engines (engine 0 = cp.async 16-byte copies,
- * 1 = TMA tile::gather4) and its ring shape, and nothing else.  Writes the elapsed GPU time in
+ * 1 = TMA tile::gather4, 2 = both, on alternate stages) and its ring shape, and nothing else.  Writes the elapsed GPU time in
  * milliseconds to *ms_out (host pointer) and synchronises `stream`.  The pages motivate
  * it: the gather is the share of the sparse kernel that grows on newer parts ("DSA prefill ...
  * triton_sparse_mla", Speed Tests), so the kernel's gather rate is reported against this one. */

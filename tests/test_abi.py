@@ -112,7 +112,7 @@ def test_entry_validation_before_any_cuda_call(lib):
     assert pg(fake, fake, fake, fake, None, fake, None, fake, fake, None, 0, 2, 4, 64, 0, 6, 1, 256, 64, 0.0625, 0, None) == 0
     pr = lib.qsa_probe_gather_ceiling
     ms = ctypes.c_float(0.0)
-    assert pr(fake, 1000, fake, 4, 10, 2, ctypes.byref(ms), None) == 1      # unknown engine
+    assert pr(fake, 1000, fake, 4, 10, 3, ctypes.byref(ms), None) == 1      # unknown engine
     assert pr(fake + 8, 1000, fake, 4, 10, 1, ctypes.byref(ms), None) == 1  # misaligned cache
     assert pr(fake, 1000, fake, 0, 10, 0, ctypes.byref(ms), None) == 1      # empty row table
 

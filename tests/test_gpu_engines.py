@@ -66,7 +66,7 @@ def test_cpasync_engine_matches_tma_bitwise(B, tmp_path):
         assert_parity(out, lse, O, L)
 
 
-@pytest.mark.parametrize("engine", ["tma", "cpasync"])
+@pytest.mark.parametrize("engine", ["tma", "cpasync", "mixed"])
 def test_gather_ceiling_probe(B, engine):
     import torch
     g = torch.Generator().manual_seed(7)

@@ -431,7 +431,7 @@ def union_build(indices, topk_len, union_g: int, n_kv_slots: int = 0, want_sorte
     return srt, uidx, ubits, ulen
 
 
-GATHER_ENGINES = {"cpasync": 0, "tma": 1}
+GATHER_ENGINES = {"cpasync": 0, "tma": 1, "mixed": 2}
 
 
 def probe_gather_ceiling(cache_rows, row_table, pieces_per_cta: int = 1500, engine: str = "tma",

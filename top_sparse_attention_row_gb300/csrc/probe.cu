@@ -49,7 +49,9 @@ __global__ void __launch_bounds__(32 * kProbeWarps, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kProbeStages; ++s) {
-      mbar_init(full + 8 * s, use_tma ? 1 : 32);
+      // engine 2 (mixed): even stages TMA, odd stages cp.async
+      const bool stage_tma = use_tma == 1 || (use_tma == 2 && (s & 1) == 0);
+      mbar_init(full + 8 * s, stage_tma ? 1 : 32);
       mbar_init(empty + 8 * s, 1);
     }
     abort_flag = 0;
@@ -59,13 +61,14 @@ __global__ void __launch_bounds__(32 * kProbeWarps, 1)
   volatile int* ab = &abort_flag;
   if (warp < kProbeStages) {
     const int st = warp;
+    const bool warp_tma = use_tma == 1 || (use_tma == 2 && (st & 1) == 0);
     int last = -1;   // newest piece this warp issued
     for (int p = st; p < pieces_per_cta; p += kProbeStages) {
       const uint32_t par = ((p / kProbeStages) & 1) ^ 1;
       if (!__all_sync(0xffffffffu, probe_wait(empty + 8 * st, par, ab, status))) break;
       const int32_t* prow = rows + ((blockIdx.x * 131 + p) % n_table_pieces) * kTileTokens;
       const uint32_t dst = base + st * kStageBytes;
-      if (use_tma) {
+      if (warp_tma) {
         // lane: rows 4*lane .. 4*lane+3, two gather4 ops (dims 0-63 and 64-127)
         const int4 y = *reinterpret_cast<const int4*>(prow + 4 * lane);
         if (lane == 0) mbar_arrive_expect_tx(full + 8 * st, kStageBytes);
@@ -87,7 +90,7 @@ __global__ void __launch_bounds__(32 * kProbeWarps, 1)
       asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(full + 8 * st)
                    : "memory");
     }
-    if (!use_tma) {
+    if (!warp_tma) {
       asm volatile("cp.async.wait_all;" ::: "memory");
     } else if (*ab && last >= 0 && lane == 0) {
       // after an abort the consumer may not have waited for this stage: let the newest copy
@@ -117,7 +120,7 @@ extern "C" qsa_status qsa_probe_gather_ceiling(const void* cache, int64_t n_rows
                                                int32_t pieces_per_cta, int32_t engine,
                                                float* ms_out, void* stream_v) {
   if (!cache || !rows || !ms_out || n_rows <= 0 || n_table_pieces <= 0 || pieces_per_cta <= 0 ||
-      (engine != 0 && engine != 1) || (reinterpret_cast<uintptr_t>(cache) & 15u) != 0)
+      engine < 0 || engine > 2 || (reinterpret_cast<uintptr_t>(cache) & 15u) != 0)
     return QSA_ERR_INVALID_ARG;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
