@@ -201,6 +201,39 @@ __device__ __forceinline__ int block_reduce_min(int v, int* scratch) {
   return r;
 }
 
+// Exclusive prefixes over the block of eight per-thread counts at once (entries t >= n are 0):
+// off[t] = sum of c[t] over lower threads, tot[t] = block sum.  One barrier pair for all eight.
+__device__ __forceinline__ void block_exclusive_scan8(const int (&c)[8], int (&off)[8], int (&tot)[8],
+                                                      int (*scratch)[8]) {
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int incl[8];
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    incl[t] = c[t];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl[t], o);
+      if (lane >= o) incl[t] += y;
+    }
+  }
+  __syncthreads();
+  if (lane == 31) {
+#pragma unroll
+    for (int t = 0; t < 8; ++t) scratch[w][t] = incl[t];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    int before = 0, sum = 0;
+    for (int i = 0; i < kBmThreads / 32; ++i) {
+      if (i < w) before += scratch[i][t];
+      sum += scratch[i][t];
+    }
+    off[t] = before + incl[t] - c[t];
+    tot[t] = sum;
+  }
+}
+
 // Exclusive prefix of v over the block; *total gets the block sum.
 __device__ __forceinline__ int block_exclusive_scan(int v, int* scratch, int* total) {
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -235,6 +268,7 @@ __global__ void __launch_bounds__(kBmThreads)
   __shared__ int scratch[kBmThreads / 32];
   __shared__ int row_total[8], row_base[8], row_done[8];
   __shared__ int32_t row_req[8], row_kvlen[8];
+  __shared__ int vscratch[kBmThreads / 32][8];
 
   const int64_t group = blockIdx.x;
   const int64_t r0 = group * G;
@@ -285,13 +319,68 @@ __global__ void __launch_bounds__(kBmThreads)
   //    covers every slot, in which case the bitmaps are built once.
   const int64_t span = static_cast<int64_t>(W) * 32;
   const bool one_window = gmax >= 0 && gmax < span;
-  // One window: rows are visited in order, so each row's place follows from the rows before it
-  // and a single pass both counts and emits.  Several windows: a counting pass first, because a
+  // One window: the bitmaps are built once, one vector scan gives every (thread, row) count its
+  // place, and a single pass emits all rows.  Several windows: a counting pass first, because a
   // row's slots from every window precede the next row's.
   int placed = 0;
-  for (int pass = one_window ? 1 : 0; pass < 2 && gmax >= 0; ++pass) {
+  if (one_window) {
+    const int active = gmax / 32 + 1;
+    for (int i = tid; i < Gp * active; i += kBmThreads) bm[(i / active) * W + i % active] = 0u;
+    __syncthreads();
+    for (int e = tid; e < Gp * topk; e += kBmThreads) {
+      const int32_t x = ent[e];
+      if (x >= 0) atomicOr(&bm[(e / topk) * W + (x >> 5)], 1u << (x & 31));
+    }
+    __syncthreads();
+    const int wpt = (active + kBmThreads - 1) / kBmThreads;   // words per thread
+    const int w0 = tid * wpt, w1 = min(w0 + wpt, active);
+    int cnt[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) cnt[t] = 0;
+    for (int w = w0; w < w1; ++w) {
+      uint32_t earlier = 0u;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        if (t < Gp) {
+          const uint32_t m = bm[t * W + w];
+          cnt[t] += __popc(m & ~earlier);
+          earlier |= m;
+        }
+      }
+    }
+    int off[8], tot[8];
+    block_exclusive_scan8(cnt, off, tot, vscratch);
+    int pos[8], acc = 0;
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      pos[t] = acc + off[t];
+      acc += t < Gp ? tot[t] : 0;
+    }
+    for (int w = w0; w < w1; ++w) {
+      uint32_t words[8], earlier = 0u;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) words[t] = t < Gp ? bm[t * W + w] : 0u;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        uint32_t m = words[t] & ~earlier;
+        earlier |= words[t];
+        while (m) {
+          const int b = __ffs(m) - 1;
+          m &= m - 1u;
+          uint32_t owners = 0u;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) owners |= ((words[u] >> b) & 1u) << u;
+          out_idx[pos[t]] = 32 * w + b;
+          out_bits[pos[t]] = static_cast<uint8_t>(owners);
+          ++pos[t];
+        }
+      }
+    }
+    placed = acc;
+  }
+  for (int pass = 0; pass < 2 && gmax >= 0 && !one_window; ++pass) {
     int64_t wbase = 0;
-    if (pass == 1 && !one_window) {
+    if (pass == 1) {
       if (tid == 0) {
         int acc = 0;
         for (int t = 0; t < Gp; ++t) { row_base[t] = acc; acc += row_total[t]; }
@@ -329,7 +418,7 @@ __global__ void __launch_bounds__(kBmThreads)
         if (pass == 0) {
           if (tid == 0) row_total[t] += total;
         } else {
-          int pos = (one_window ? placed : row_base[t] + row_done[t]) + off;
+          int pos = row_base[t] + row_done[t] + off;
           for (int w = w0; w < w1; ++w) {
             uint32_t earlier = 0u;
             for (int u = 0; u < t; ++u) earlier |= bm[u * W + w];
@@ -346,11 +435,9 @@ __global__ void __launch_bounds__(kBmThreads)
           }
           __syncthreads();
           if (tid == 0) row_done[t] += total;
-          placed += total;   // uniform: every thread holds the block total
         }
         __syncthreads();
       }
-      if (one_window) break;
       // next window starts at the smallest slot past this one
       int my_next = INT_MAX;
       for (int e = tid; e < Gp * topk; e += kBmThreads) {
