@@ -293,6 +293,21 @@ qsa_status qsa_probe_gather_ceiling(const void* cache, int64_t n_rows, const int
                                     int64_t n_table_pieces, int32_t pieces_per_cta,
                                     int32_t engine, float* ms_out, void* stream);
 
+/* Gather / tensor-pipe contention probe (measurement helper, no counterpart on the pages): the
+ * gather of qsa_probe_gather_ceiling (same arguments; pieces_per_cta may be 0) while one more warp
+ * per SM keeps the tensor pipe busy with batches of 16 tcgen05.mma M128 x mma_n x K16 (bf16 in,
+ * fp32 out; mma_n a multiple of 16, at most 64), one commit per batch, two batches in flight.
+ * mma_mode 1 reads A from shared memory (as the attention kernel's operands do), 2 from tensor
+ * memory.  The MMAs run until the gather ends (at most mma_batches batches), or exactly
+ * mma_batches batches when pieces_per_cta is 0.  Writes the kernel's elapsed milliseconds to
+ * *ms_out and the tensor pipe's mean nanoseconds per MMA on one SM to *mma_ns_out (host
+ * pointers); synchronises `stream`.  QSA_ERR_INVALID_ARG on a bad argument, QSA_ERR_TIMEOUT if a
+ * bounded wait (1 s) ran out. */
+qsa_status qsa_probe_gather_mma(const void* cache, int64_t n_rows, const int32_t* rows,
+                                int64_t n_table_pieces, int32_t pieces_per_cta, int32_t engine,
+                                int32_t mma_mode, int32_t mma_n, int32_t mma_batches,
+                                float* ms_out, float* mma_ns_out, void* stream);
+
 /* Failure-detection test hook (no counterpart on the pages): the next attention call
  * (qsa_sparse_prefill*, qsa_sparse_mla_prefill) launches with its index warps withholding their
  * items, so every other role's bounded wait (2 s) runs out.  The kernel records

@@ -115,6 +115,15 @@ def test_entry_validation_before_any_cuda_call(lib):
     assert pr(fake, 1000, fake, 4, 10, 3, ctypes.byref(ms), None) == 1      # unknown engine
     assert pr(fake + 8, 1000, fake, 4, 10, 1, ctypes.byref(ms), None) == 1  # misaligned cache
     assert pr(fake, 1000, fake, 0, 10, 0, ctypes.byref(ms), None) == 1      # empty row table
+    pm = lib.qsa_probe_gather_mma
+    ns = ctypes.c_float(0.0)
+    #         cache rows  table pieces ppc eng mode  n  batches
+    assert pm(fake, 1000, fake, 4, 10, 1, 3, 16, 10, ctypes.byref(ms), ctypes.byref(ns), None) == 1  # mode
+    assert pm(fake, 1000, fake, 4, 10, 1, 1, 24, 10, ctypes.byref(ms), ctypes.byref(ns), None) == 1  # N % 16
+    assert pm(fake, 1000, fake, 4, 10, 1, 2, 128, 10, ctypes.byref(ms), ctypes.byref(ns), None) == 1  # N > 64
+    assert pm(fake, 1000, fake, 4, 0, 1, 1, 16, 0, ctypes.byref(ms), ctypes.byref(ns), None) == 1   # no batches
+    assert pm(fake, 1000, fake, 4, -1, 1, 1, 16, 10, ctypes.byref(ms), ctypes.byref(ns), None) == 1  # ppc < 0
+    assert pm(fake, 1000, fake, 4, 10, 1, 1, 16, 10, ctypes.byref(ms), None, None) == 1              # no output
 
 
 def test_workspace_bytes(lib):
