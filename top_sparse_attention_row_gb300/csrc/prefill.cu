@@ -357,8 +357,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Producer warp w owns the ring stages st with st % W == w and gathers every piece that
     // lands on them, whole (64 cp.async of 2 slots x 16 chunks, or 64 TMA gather4), in order.
     // One owner per stage: no two warps ever wait on different phases of one stage, and a
-    // warp issues a whole 32 KiB piece back to back, which measured 1.7x the rate of six
-    // warps sharing every piece.
+    // warp issues a whole 32 KiB piece back to back.  Measured alternatives were slower: six
+    // warps sharing every piece (1.3x the time), and two warps per piece with three, five or
+    // six warp pairs (3-8 % slower: more warps spinning on stage barriers, fewer registers).
     const int pw = warp - kProducerWarp0;
     constexpr int W = kProducerWarps;
     const bool tma = p.gather_tma != 0;

@@ -294,22 +294,38 @@ __global__ void __launch_bounds__(kBmThreads)
   }
 
   // 1. valid slots of the group's rows (topk_len, negative, >= n_kv_slots filtered; logical
-  //    positions translated through the page table) and their max
+  //    positions translated through the page table) and their max.  Each thread has eight
+  //    index loads in flight before it uses any: the build is bound by load latency.
   int my_max = -1;
-  for (int e = tid; e < Gp * topk; e += kBmThreads) {
-    const int u = e / topk, j = e - u * topk;
-    const int64_t r = r0 + u;
-    int Lr = topk;
-    if (topk_len) Lr = min(max(topk_len[r], 0), topk);
-    int32_t x = -1;
-    if (j < Lr) x = indices[r * topk + j];
-    if (paged) {
-      const int64_t slot = paged_slot(pa, row_req[u], row_kvlen[u], x);
-      x = slot > static_cast<int64_t>(INT32_MAX) ? -1 : static_cast<int32_t>(slot);
+  constexpr int kLoadsInFlight = 8;
+  const int n_ent = Gp * topk;
+  for (int e0 = 0; e0 < n_ent; e0 += kLoadsInFlight * kBmThreads) {
+    int32_t xs[kLoadsInFlight];
+#pragma unroll
+    for (int k = 0; k < kLoadsInFlight; ++k) {
+      const int e = e0 + k * kBmThreads + tid;
+      xs[k] = -1;
+      if (e < n_ent) {
+        const int u = e / topk, j = e - u * topk;
+        const int64_t r = r0 + u;
+        const int Lr = topk_len ? min(max(__ldg(topk_len + r), 0), topk) : topk;
+        if (j < Lr) xs[k] = __ldg(indices + r * topk + j);
+      }
     }
-    if (x < 0 || (n_kv_slots > 0 && x >= n_kv_slots)) x = -1;
-    ent[e] = x;
-    my_max = max(my_max, x);
+#pragma unroll
+    for (int k = 0; k < kLoadsInFlight; ++k) {
+      const int e = e0 + k * kBmThreads + tid;
+      if (e >= n_ent) break;
+      int32_t x = xs[k];
+      if (paged) {
+        const int u = e / topk;
+        const int64_t slot = paged_slot(pa, row_req[u], row_kvlen[u], x);
+        x = slot > static_cast<int64_t>(INT32_MAX) ? -1 : static_cast<int32_t>(slot);
+      }
+      if (x < 0 || (n_kv_slots > 0 && x >= n_kv_slots)) x = -1;
+      ent[e] = x;
+      my_max = max(my_max, x);
+    }
   }
   const int gmax = block_reduce_max(my_max, scratch);
   if (tid < 8) { row_total[tid] = 0; row_done[tid] = 0; }
