@@ -299,17 +299,26 @@ __global__ void __launch_bounds__(kBmThreads)
   int my_max = -1;
   constexpr int kLoadsInFlight = 8;
   const int n_ent = Gp * topk;
+  // (row, position) of element e = e0 + k * kBmThreads + tid, stepped without a division
+  int eu = tid / topk, ej = tid - eu * topk;
   for (int e0 = 0; e0 < n_ent; e0 += kLoadsInFlight * kBmThreads) {
     int32_t xs[kLoadsInFlight];
+    int us[kLoadsInFlight];
 #pragma unroll
     for (int k = 0; k < kLoadsInFlight; ++k) {
       const int e = e0 + k * kBmThreads + tid;
+      us[k] = eu;
       xs[k] = -1;
       if (e < n_ent) {
-        const int u = e / topk, j = e - u * topk;
-        const int64_t r = r0 + u;
+        const int64_t r = r0 + eu;
         const int Lr = topk_len ? min(max(__ldg(topk_len + r), 0), topk) : topk;
-        if (j < Lr) xs[k] = __ldg(indices + r * topk + j);
+        if (ej < Lr) xs[k] = __ldg(indices + r * topk + ej);
+      }
+      ej += kBmThreads;
+      if (ej >= topk) {          // a row boundary was crossed (at most once when topk >= 256)
+        const int q = ej / topk;
+        eu += q;
+        ej -= q * topk;
       }
     }
 #pragma unroll
@@ -318,7 +327,7 @@ __global__ void __launch_bounds__(kBmThreads)
       if (e >= n_ent) break;
       int32_t x = xs[k];
       if (paged) {
-        const int u = e / topk;
+        const int u = us[k];
         const int64_t slot = paged_slot(pa, row_req[u], row_kvlen[u], x);
         x = slot > static_cast<int64_t>(INT32_MAX) ? -1 : static_cast<int32_t>(slot);
       }
