@@ -289,13 +289,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         y2 = t + 2 < nv ? v.z : p.pad_row;
         y3 = t + 3 < nv ? v.w : p.pad_row;
       };
+      // A tile's rows are read once, one tile ahead of their use, so the (global, in union mode)
+      // load latency overlaps the previous tile's pieces.
+      int n0 = 0, n1 = 0, n2 = 0, n3 = 0;
+      if (nt > 0) rows_of(0, n0, n1, n2, n3);
       if (pw < kMlaPairOwners) {
+        int y0 = 0, y1 = 0, y2 = 0, y3 = 0;
         for (int q = 0; q < kMlaPairs * nt; ++q) {
           const uint32_t s = lseq + q;
           const uint32_t st = s % RP;
           const int tile = q / kMlaPairs, c = q % kMlaPairs;
-          int y0, y1, y2, y3;
-          rows_of(tile, y0, y1, y2, y3);
+          if (c == 0) {
+            y0 = n0; y1 = n1; y2 = n2; y3 = n3;
+            if (tile + 1 < nt) rows_of(tile + 1, n0, n1, n2, n3);
+          }
           if (!__all_sync(0xffffffffu, mla_wait(b_lempty + 8 * st, ((s / RP) & 1) ^ 1, abort_flag,
                                                 status, kMLatEmpty))) {
             aborted = true;
@@ -314,8 +321,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if (pw == kMlaRopeOwner) {
         for (int j = 0; j < nt; ++j) {
           const uint32_t s = rseq + j;
-          int y0, y1, y2, y3;
-          rows_of(j, y0, y1, y2, y3);
+          const int y0 = n0, y1 = n1, y2 = n2, y3 = n3;
+          if (j + 1 < nt) rows_of(j + 1, n0, n1, n2, n3);
           if (!__all_sync(0xffffffffu, mla_wait(b_rempty, (s & 1) ^ 1, abort_flag, status, kMRopeEmpty))) {
             aborted = true;
             break;

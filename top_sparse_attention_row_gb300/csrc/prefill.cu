@@ -377,23 +377,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t* sl = reinterpret_cast<const int32_t*>(gbase + L.slots) + b * slot_cap;
       const int32_t* ul =
           UNION ? p.union_idx + static_cast<int64_t>(I.group) * p.union_g * p.topk : nullptr;
-      for (int q = 0; q < 4 * nt; ++q) {
+      const int n_pieces = 4 * nt;
+      auto mine = [&](int q) { return static_cast<int>((seq + q) % R) % W == pw; };
+      // union slots of a piece's tile (global memory): lane holds tokens 4*lane .. 4*lane+3
+      auto union_rows = [&](int q) {
+        int tile, is_v, half;
+        piece_of<kLookahead>(q, nt, tile, is_v, half);
+        const int t = tile * kTileTokens + 4 * lane;
+        int4 y;
+        y.x = t + 0 < nv ? ul[t + 0] * p.n_kvheads + I.kvh : p.pad_row;
+        y.y = t + 1 < nv ? ul[t + 1] * p.n_kvheads + I.kvh : p.pad_row;
+        y.z = t + 2 < nv ? ul[t + 2] * p.n_kvheads + I.kvh : p.pad_row;
+        y.w = t + 3 < nv ? ul[t + 3] * p.n_kvheads + I.kvh : p.pad_row;
+        return y;
+      };
+      int q0 = 0;
+      while (q0 < n_pieces && !mine(q0)) ++q0;
+      // The union slots of the warp's next piece are loaded one piece ahead, so their latency
+      // overlaps the wait for the current piece's stage and its issue.
+      int4 uy_next = make_int4(0, 0, 0, 0);
+      if (UNION && q0 < n_pieces) uy_next = union_rows(q0);
+      for (int q = q0, qn = 0; q < n_pieces; q = qn) {
+        qn = q + 1;
+        while (qn < n_pieces && !mine(qn)) ++qn;
+        const int4 uy = uy_next;
+        if (UNION && qn < n_pieces) uy_next = union_rows(qn);
         const uint32_t s = seq + q;
         const uint32_t st = s % R;
-        if (static_cast<int>(st) % W != pw) continue;
         int tile, is_v, half;
         piece_of<kLookahead>(q, nt, tile, is_v, half);
         const int t0 = tile * kTileTokens;
-        // union slots of the tile: lane holds tokens 4*lane .. 4*lane+3 (loaded before the
-        // stage wait so the wait hides the load)
-        int4 uy = make_int4(0, 0, 0, 0);
-        if (UNION) {
-          const int t = t0 + 4 * lane;
-          uy.x = t + 0 < nv ? ul[t + 0] * p.n_kvheads + I.kvh : p.pad_row;
-          uy.y = t + 1 < nv ? ul[t + 1] * p.n_kvheads + I.kvh : p.pad_row;
-          uy.z = t + 2 < nv ? ul[t + 2] * p.n_kvheads + I.kvh : p.pad_row;
-          uy.w = t + 3 < nv ? ul[t + 3] * p.n_kvheads + I.kvh : p.pad_row;
-        }
         const uint32_t par = ((s / R) & 1) ^ 1;
         const uint32_t empty_bar = b_empty + 8 * (st >> 1);   // the stage pair's barrier
         if (!__all_sync(0xffffffffu, wait_bar(empty_bar, par, abort_flag, kSiteStageEmpty))) {
