@@ -378,7 +378,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t* ul =
           UNION ? p.union_idx + static_cast<int64_t>(I.group) * p.union_g * p.topk : nullptr;
       const int n_pieces = 4 * nt;
-      auto mine = [&](int q) { return static_cast<int>((seq + q) % R) % W == pw; };
+      // This warp's pieces are those on its stages pw and pw + W: two arithmetic progressions
+      // of step R, merged in order.  Stepping straight to them, rather than testing every
+      // piece of the item, measured 1-2 % faster on GB300 (group6_32k 2.237 -> 2.205 ms).
+      const int sq = static_cast<int>(seq % static_cast<uint32_t>(R));
+      int qa = pw < R ? (pw - sq + R) % R : n_pieces;
+      int qb = pw + W < R ? (pw + W - sq + R) % R : n_pieces;
+      auto next_piece = [&]() {
+        int q;
+        if (qa <= qb) {
+          q = qa;
+          qa += R;
+        } else {
+          q = qb;
+          qb += R;
+        }
+        return q;
+      };
       // union slots of a piece's tile (global memory): lane holds tokens 4*lane .. 4*lane+3
       auto union_rows = [&](int q) {
         int tile, is_v, half;
@@ -391,15 +407,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         y.w = t + 3 < nv ? ul[t + 3] * p.n_kvheads + I.kvh : p.pad_row;
         return y;
       };
-      int q0 = 0;
-      while (q0 < n_pieces && !mine(q0)) ++q0;
+      const int q0 = next_piece();
       // The union slots of the warp's next piece are loaded one piece ahead, so their latency
       // overlaps the wait for the current piece's stage and its issue.
       int4 uy_next = make_int4(0, 0, 0, 0);
       if (UNION && q0 < n_pieces) uy_next = union_rows(q0);
       for (int q = q0, qn = 0; q < n_pieces; q = qn) {
-        qn = q + 1;
-        while (qn < n_pieces && !mine(qn)) ++qn;
+        qn = next_piece();
         const int4 uy = uy_next;
         if (UNION && qn < n_pieces) uy_next = union_rows(qn);
         const uint32_t s = seq + q;
