@@ -656,53 +656,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) rbuf[warp * NP + c] = v;
       }
       named_bar_sync(1, 128);
-      float inv_l[NP];
-      float my_l = 0.f, my_m = NEG_INF;
-#pragma unroll
-      for (int c = 0; c < NP; ++c) {
-        const float l = (rbuf[c] + rbuf[NP + c]) + (rbuf[2 * NP + c] + rbuf[3 * NP + c]);
-        inv_l[c] = l > 0.f ? 1.f / l : 0.f;
-        if (c == t) {
-          my_l = l;
-          my_m = m_used[c];
-        }
-      }
-      rb ^= 1;
-      if (nt > 0) {
-        const uint32_t jl = js + nt - 1;
-        bad |= !mla_wait(b_pvdone + 8 * (jl & 1), (jl >> 1) & 1, abort_flag, status, kMPvDone);
-        tc_fence_after();
-      }
+      // Thread t < cols finishes column t once (row sum, 1 / l, LSE, output offset) into the
+      // other reduction buffer, whose last readers passed the barrier above.
+      float* const inv_s = red + (rb ^ 1) * 4 * NP;
+      int64_t* const off_s = reinterpret_cast<int64_t*>(inv_s + NP);
       const int64_t H = p.n_heads;
-#pragma unroll 1
-      for (int oc = 0; oc < kMlaPairs; ++oc) {
-        float o[NP];
-        if (nt > 0) {
+      if (t < cols) {
+        const float l = (rbuf[t] + rbuf[NP + t]) + (rbuf[2 * NP + t] + rbuf[3 * NP + t]);
+        float my_m = NEG_INF;
 #pragma unroll
-          for (int q = 0; q < NP / 16; ++q) tmem_ld16(tm_o + lane_off + oc * NP + 16 * q, o + 16 * q);
-          tc_wait_ld();
-        } else {
-#pragma unroll
-          for (int c = 0; c < NP; ++c) o[c] = 0.f;
-        }
-        const int d = oc * 128 + t;
-#pragma unroll
-        for (int c = 0; c < NP; ++c) {
-          if (c < cols) {
-            int64_t row, head;
-            if (UNION) {
-              row = I.row0 + c / p.n_heads;
-              head = c % p.n_heads;
-            } else {
-              row = I.row0;
-              head = static_cast<int64_t>(I.chunk) * p.chunk_cols + c;
-            }
-            reinterpret_cast<__nv_bfloat16*>(p.out)[(row * H + head) * kMlaDv + d] =
-                __float2bfloat16_rn(o[c] * inv_l[c]);
-          }
-        }
-      }
-      if (p.lse != nullptr && t < cols) {
+        for (int c = 0; c < NP; ++c)
+          if (c == t) my_m = m_used[c];
         int64_t row, head;
         if (UNION) {
           row = I.row0 + t / p.n_heads;
@@ -711,7 +675,38 @@ __global__ void __launch_bounds__(kThreads, 1)
           row = I.row0;
           head = static_cast<int64_t>(I.chunk) * p.chunk_cols + t;
         }
-        p.lse[row * H + head] = my_l > 0.f ? (my_m + log2f(my_l)) * kMlaLn2 : NEG_INF;
+        inv_s[t] = l > 0.f ? 1.f / l : 0.f;
+        off_s[t] = (row * H + head) * kMlaDv;
+        if (p.lse != nullptr) p.lse[row * H + head] = l > 0.f ? (my_m + log2f(l)) * kMlaLn2 : NEG_INF;
+      }
+      named_bar_sync(1, 128);
+      rb ^= 1;
+      if (nt > 0) {
+        const uint32_t jl = js + nt - 1;
+        bad |= !mla_wait(b_pvdone + 8 * (jl & 1), (jl >> 1) & 1, abort_flag, status, kMPvDone);
+        tc_fence_after();
+      }
+      __nv_bfloat16* const outp = reinterpret_cast<__nv_bfloat16*>(p.out);
+#pragma unroll 1
+      for (int oc = 0; oc < kMlaPairs; ++oc) {
+        const int d = oc * 128 + t;
+#pragma unroll
+        for (int q = 0; q < NP / 16; ++q) {
+          if (16 * q >= cols) break;
+          float o[16];
+          if (nt > 0) {
+            tmem_ld16(tm_o + lane_off + oc * NP + 16 * q, o);
+            tc_wait_ld();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] = 0.f;
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int c = 16 * q + i;
+            if (c < cols) outp[off_s[c] + d] = __float2bfloat16_rn(o[i] * inv_s[c]);
+          }
+        }
       }
       tc_fence_before();
       js += nt;
