@@ -843,24 +843,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
       }
       __nv_bfloat16* const outp = reinterpret_cast<__nv_bfloat16*>(p.out);
+      // 16 columns at a time, both 128-dim halves loaded before one wait
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int d = hh * 128 + t;
+      for (int q = 0; q < NP / 16; ++q) {
+        if (16 * q >= cols) break;
+        float o[2][16];
+        if (nt > 0) {
+          tmem_ld16(tm_o + lane_off + 16 * q, o[0]);
+          tmem_ld16(tm_o + lane_off + NP + 16 * q, o[1]);
+          tc_wait_ld();
+        } else {
 #pragma unroll
-        for (int q = 0; q < NP / 16; ++q) {
-          if (16 * q >= cols) break;
-          float o[16];
-          if (nt > 0) {
-            tmem_ld16(tm_o + lane_off + hh * NP + 16 * q, o);
-            tc_wait_ld();
-          } else {
+          for (int i = 0; i < 16; ++i) o[0][i] = o[1][i] = 0.f;
+        }
 #pragma unroll
-            for (int i = 0; i < 16; ++i) o[i] = 0.f;
-          }
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int c = 16 * q + i;
-            if (c < cols) outp[off_s[c] + d] = __float2bfloat16_rn(o[i] * inv_s[c]);
+        for (int i = 0; i < 16; ++i) {
+          const int c = 16 * q + i;
+          if (c < cols) {
+            const float il = inv_s[c];
+            __nv_bfloat16* const dst = outp + off_s[c] + t;
+            dst[0] = __float2bfloat16_rn(o[0][i] * il);
+            dst[128] = __float2bfloat16_rn(o[1][i] * il);
           }
         }
       }
