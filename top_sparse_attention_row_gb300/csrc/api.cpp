@@ -29,7 +29,7 @@ int pow2_at_least(int v) {
 }
 
 struct WsLayout {
-  size_t idx, bits, len, total;
+  size_t idx, bits, len, ctr, total;
 };
 WsLayout ws_layout(int64_t n_rows, int32_t topk, int32_t G) {
   WsLayout w{};
@@ -39,7 +39,8 @@ WsLayout ws_layout(int64_t n_rows, int32_t topk, int32_t G) {
   w.idx = 0;
   w.bits = round_up(static_cast<int64_t>(cap * 4), kWsAlign);
   w.len = w.bits + round_up(static_cast<int64_t>(cap), kWsAlign);
-  w.total = w.len + round_up(n_groups * 4, kWsAlign);
+  w.ctr = w.len + round_up(n_groups * 4, kWsAlign);   // the attention kernel's item counter
+  w.total = w.ctr + kWsAlign;
   return w;
 }
 
@@ -343,11 +344,12 @@ qsa_status run(const void* q, const void* k_cache, const void* v_cache, const in
     p.union_idx = reinterpret_cast<int32_t*>(b + w.idx);
     p.union_bits = b + w.bits;
     p.union_len = reinterpret_cast<int32_t*>(b + w.len);
+    p.item_counter = reinterpret_cast<int32_t*>(b + w.ctr);
     cudaError_t e = qsa::launch_union_build(indices, topk_len, n_rows, topk, g.union_g, n_kv_slots,
                                             nullptr, const_cast<int32_t*>(p.union_idx),
                                             const_cast<uint8_t*>(p.union_bits),
                                             const_cast<int32_t*>(p.union_len), false, paged,
-                                            stream);
+                                            stream, p.item_counter);
     if (e != cudaSuccess) {
       if (own_ws) cudaFreeAsync(ws, stream);
       return QSA_ERR_CUDA;

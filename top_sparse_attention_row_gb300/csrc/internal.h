@@ -82,6 +82,9 @@ struct PrefillParams {
   const float* v_scale;
   int32_t page_size;
   int32_t stall_first_item;     // failure-detection test: the index warp withholds its items
+  // Union mode: items are handed out through this counter (zeroed by the union build) in
+  // reverse order, longest groups first; nullptr = static round robin over the grid.
+  int32_t* item_counter;
 };
 
 struct Geometry {
@@ -214,7 +217,7 @@ cudaError_t launch_union_build(const int32_t* indices, const int32_t* topk_len, 
                                int32_t topk, int32_t union_g, int64_t n_kv_slots,
                                int32_t* sorted_out, int32_t* union_idx, uint8_t* union_bits,
                                int32_t* union_len, bool pad_outputs, const PagedAddr* paged,
-                               cudaStream_t stream);
+                               cudaStream_t stream, int32_t* item_counter = nullptr);
 size_t union_build_smem_bytes(int32_t topk, int32_t union_g);   // hot-path (bitmap) kernel
 size_t union_sort_smem_bytes(int32_t topk, int32_t union_g);    // sorted-rows (bitonic) kernel
 cudaError_t read_and_clear_device_status(cudaStream_t stream, int32_t* status);

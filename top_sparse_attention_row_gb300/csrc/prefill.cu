@@ -273,13 +273,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kIndexWarp) {
     // ------------------------------------------------------------ index / Q loader
+    // Items: a static round robin over the grid, or (union mode) taken from a global counter in
+    // reverse order -- the later row groups of a prefill have the longest union lists, so the
+    // long items go first and the short ones even out the CTAs' finishing times.  After the
+    // last item the warp publishes an item record with n_valid = -1, which ends every role.
+    auto next_item = [&](int64_t cur) -> int64_t {
+      if (p.item_counter == nullptr) return cur + stride;
+      int32_t k = 0;
+      if (lane == 0) k = atomicAdd(p.item_counter, 1);
+      k = __shfl_sync(0xffffffffu, k, 0);
+      return k < n_items ? n_items - 1 - k : n_items;
+    };
     uint32_t it = 0;
-    for (int64_t item = blockIdx.x; item < n_items; item += stride, ++it) {
+    for (int64_t item = p.item_counter == nullptr ? static_cast<int64_t>(blockIdx.x) : next_item(0);;
+         item = next_item(item), ++it) {
       // failure-detection test hook: withhold the first item so every other wait runs out
       if (p.stall_first_item) break;
       const uint32_t b = it & 1, ph = (it >> 1) & 1;
       bool ok = wait_bar(b_itemempty + 8 * b, ph ^ 1, abort_flag, kSiteItemEmpty);
       if (!__all_sync(0xffffffffu, ok)) break;
+      if (item >= n_items) {
+        if (lane == 0) {
+          info[b].n_valid = -1;
+          mbar_arrive(b_itemfull + 8 * b);
+        }
+        break;
+      }
       int32_t group, kvh, chunk;
       decode_item(p, item, group, kvh, chunk);
       int32_t cols, row0, rows_in_group;
@@ -365,13 +384,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool tma = p.gather_tma != 0;
     uint32_t seq = 0, it = 0, issued = 0;
     bool aborted = false;
-    for (int64_t item = blockIdx.x; item < n_items && !aborted; item += stride, ++it) {
+    for (;; ++it) {
       const uint32_t b = it & 1, ph = (it >> 1) & 1;
       if (!__all_sync(0xffffffffu, wait_bar(b_itemfull + 8 * b, ph, abort_flag, kSiteItemFull))) {
         aborted = true;
         break;
       }
       const ItemInfo I = info[b];
+      if (I.n_valid < 0) break;                // no more items
       const int nv = I.n_valid;
       const int nt = (nv + kTileTokens - 1) / kTileTokens;
       const int32_t* sl = reinterpret_cast<const int32_t*>(gbase + L.slots) + b * slot_cap;
@@ -545,13 +565,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       : idesc_bf16_f32(128, NP, true, false);
     uint32_t seq = 0, js = 0, it = 0;
     bool aborted = false;
-    for (int64_t item = blockIdx.x; item < n_items && !aborted; item += stride, ++it) {
+    for (;; ++it) {
       const uint32_t b = it & 1, ph = (it >> 1) & 1;
       if (!__all_sync(0xffffffffu, wait_bar(b_itemfull + 8 * b, ph, abort_flag, kSiteItemFull))) {
         aborted = true;
         break;
       }
       const int nv = info[b].n_valid;
+      if (nv < 0) break;                        // no more items
       const int nt = (nv + kTileTokens - 1) / kTileTokens;
       __syncwarp();
       if (lane == 0) mbar_arrive(b_itemempty + 8 * b);
@@ -642,13 +663,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t js = 0, it = 0, rb = 0;
     bool bad = false;
     const float NEG_INF = -INFINITY;
-    for (int64_t item = blockIdx.x; item < n_items; item += stride, ++it) {
+    for (;; ++it) {
       const uint32_t b = it & 1, ph = (it >> 1) & 1;
       bad |= !wait_bar(b_itemfull + 8 * b, ph, abort_flag, kSiteItemFull);
       // Uniform decision before the item record is read: if any softmax thread's wait gave up
       // (or another role aborted), all 128 leave together.
       if (named_bar_any(3, 128, bad || *abort_flag)) break;
       const ItemInfo I = info[b];
+      if (I.n_valid < 0) break;                // no more items (same record for all 128)
       // FP8 reads the item's slot list for the scales until its last tile, so it hands the
       // item slot back at the end of the item instead.
       if (!FP8) mbar_arrive(b_itemempty + 8 * b);

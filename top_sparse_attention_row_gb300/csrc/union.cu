@@ -261,7 +261,8 @@ __global__ void __launch_bounds__(kBmThreads)
     union_bitmap_kernel(const int32_t* __restrict__ indices, const int32_t* __restrict__ topk_len,
                         int64_t n_rows, int32_t topk, int32_t G, int32_t W, int64_t n_kv_slots,
                         int32_t* __restrict__ union_idx, uint8_t* __restrict__ union_bits,
-                        int32_t* __restrict__ union_len, int32_t pad_outputs, PagedAddr pa) {
+                        int32_t* __restrict__ union_len, int32_t pad_outputs, PagedAddr pa,
+                        int32_t* __restrict__ item_counter) {
   extern __shared__ uint32_t sm_words[];
   int32_t* ent = reinterpret_cast<int32_t*>(sm_words);    // [G][topk]: valid slot or -1
   uint32_t* bm = sm_words + G * topk;                      // [G][W] bitmaps of one window
@@ -274,6 +275,8 @@ __global__ void __launch_bounds__(kBmThreads)
   const int64_t r0 = group * G;
   const int Gp = static_cast<int>(n_rows - r0 < G ? n_rows - r0 : G);
   const int tid = threadIdx.x;
+  // the attention kernel that follows on the stream hands out its items through this counter
+  if (item_counter != nullptr && group == 0 && tid == 0) *item_counter = 0;
   const int64_t cap = static_cast<int64_t>(G) * topk;
   int32_t* out_idx = union_idx + group * cap;
   uint8_t* out_bits = union_bits + group * cap;
@@ -514,10 +517,11 @@ cudaError_t launch_union_build(const int32_t* indices, const int32_t* topk_len, 
                                int32_t topk, int32_t union_g, int64_t n_kv_slots,
                                int32_t* sorted_out, int32_t* union_idx, uint8_t* union_bits,
                                int32_t* union_len, bool pad_outputs, const PagedAddr* paged,
-                               cudaStream_t stream) {
+                               cudaStream_t stream, int32_t* item_counter) {
   if (n_rows == 0) return cudaSuccess;
   // The sorted-rows kernel takes physical slots only.
   if (paged != nullptr && sorted_out != nullptr) return cudaErrorInvalidValue;
+  if (item_counter != nullptr && sorted_out != nullptr) return cudaErrorInvalidValue;
   PagedAddr pa{};
   if (paged != nullptr) pa = *paged;
   const int64_t n_groups = (n_rows + union_g - 1) / union_g;
@@ -551,7 +555,7 @@ cudaError_t launch_union_build(const int32_t* indices, const int32_t* topk_len, 
     }
     union_bitmap_kernel<<<static_cast<unsigned>(n_groups), kBmThreads, smem, stream>>>(
         indices, topk_len, n_rows, topk, union_g, W, n_kv_slots, union_idx, union_bits, union_len,
-        pad_outputs ? 1 : 0, pa);
+        pad_outputs ? 1 : 0, pa, item_counter);
     return cudaGetLastError();
   }
   const int Kp = next_pow2(topk);
