@@ -426,11 +426,12 @@ qsa_status run_mla(const void* q, const void* kv_cache, const int32_t* indices,
     p.union_idx = reinterpret_cast<int32_t*>(b + w.idx);
     p.union_bits = b + w.bits;
     p.union_len = reinterpret_cast<int32_t*>(b + w.len);
+    p.item_counter = reinterpret_cast<int32_t*>(b + w.ctr);
     cudaError_t e = qsa::launch_union_build(indices, topk_len, n_rows, topk, g.union_g, n_kv_slots,
                                             nullptr, const_cast<int32_t*>(p.union_idx),
                                             const_cast<uint8_t*>(p.union_bits),
                                             const_cast<int32_t*>(p.union_len), false, paged,
-                                            stream);
+                                            stream, p.item_counter);
     if (e != cudaSuccess) {
       cudaFreeAsync(ws, stream);
       return QSA_ERR_CUDA;

@@ -159,6 +159,7 @@ struct MlaParams {
   float scale_log2;
   PagedAddr pa;                 // page_table == nullptr = physical slots
   int32_t stall_first_item;     // failure-detection test: the index warp withholds its items
+  int32_t* item_counter;        // union mode: longest-first item counter (as PrefillParams)
 };
 
 struct MlaSmemLayout {

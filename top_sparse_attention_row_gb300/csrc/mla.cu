@@ -174,13 +174,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kIndexWarp) {
     // ------------------------------------------------------------ index / Q loader
+    // Items as in the d=256 kernel: static round robin, or (union mode) longest-first from a
+    // global counter; a record with n_valid = -1 ends every role.
+    auto next_item = [&](int64_t cur) -> int64_t {
+      if (p.item_counter == nullptr) return cur + stride;
+      int32_t k = 0;
+      if (lane == 0) k = atomicAdd(p.item_counter, 1);
+      k = __shfl_sync(0xffffffffu, k, 0);
+      return k < n_items ? n_items - 1 - k : n_items;
+    };
     uint32_t it = 0;
-    for (int64_t item = blockIdx.x; item < n_items; item += stride, ++it) {
+    for (int64_t item = p.item_counter == nullptr ? static_cast<int64_t>(blockIdx.x) : next_item(0);;
+         item = next_item(item), ++it) {
       // failure-detection test hook: withhold the first item so every other wait runs out
       if (p.stall_first_item) break;
       const uint32_t b = it & 1, ph = (it >> 1) & 1;
       if (!__all_sync(0xffffffffu, mla_wait(b_itemempty + 8 * b, ph ^ 1, abort_flag, status, kMItemEmpty)))
         break;
+      if (item >= n_items) {
+        if (lane == 0) {
+          info[b].n_valid = -1;
+          mbar_arrive(b_itemfull + 8 * b);
+        }
+        break;
+      }
       const int32_t chunk = static_cast<int32_t>(item / p.n_groups);
       const int32_t group = static_cast<int32_t>(item - static_cast<int64_t>(chunk) * p.n_groups);
       int32_t cols, row0, rows_in_group;
@@ -260,13 +277,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t lseq = 0, rseq = 0, it = 0;
     uint32_t l_issued = 0, r_issued = 0;
     bool aborted = false;
-    for (int64_t item = blockIdx.x; item < n_items && !aborted; item += stride, ++it) {
+    for (;; ++it) {
       const uint32_t b = it & 1, ph = (it >> 1) & 1;
       if (!__all_sync(0xffffffffu, mla_wait(b_itemfull + 8 * b, ph, abort_flag, status, kMItemFull))) {
         aborted = true;
         break;
       }
       const MlaItem I = info[b];
+      if (I.n_valid < 0) break;                // no more items
       const int nv = I.n_valid;
       const int nt = (nv + kTileTokens - 1) / kTileTokens;
       const int32_t* sl = reinterpret_cast<const int32_t*>(gbase + L.slots) + b * slot_cap;
@@ -386,13 +404,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_mma(tm_o + c * NP, a, bp, kIdescPV, (first && kk == 0) ? 0u : 1u);
       }
     };
-    for (int64_t item = blockIdx.x; item < n_items; item += stride, ++it) {
+    for (;; ++it) {
       const uint32_t b = it & 1, ph = (it >> 1) & 1;
       if (!__all_sync(0xffffffffu, mla_wait(b_itemfull + 8 * b, ph, abort_flag, status, kMItemFull))) {
         aborted = true;
         break;
       }
       const int nv = info[b].n_valid;
+      if (nv < 0) break;                        // no more items
       const int nt = (nv + kTileTokens - 1) / kTileTokens;
       __syncwarp();
       if (lane == 0) mbar_arrive(b_itemempty + 8 * b);
@@ -512,12 +531,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t js = 0, it = 0, rb = 0;
     bool bad = false;
     const float NEG_INF = -INFINITY;
-    for (int64_t item = blockIdx.x; item < n_items; item += stride, ++it) {
+    for (;; ++it) {
       const uint32_t b = it & 1, ph = (it >> 1) & 1;
       bad |= !mla_wait(b_itemfull + 8 * b, ph, abort_flag, status, kMItemFull);
       // Uniform decision before the item record is read (see the d=256 kernel).
       if (named_bar_any(3, 128, bad || *abort_flag)) break;
       const MlaItem I = info[b];
+      if (I.n_valid < 0) break;                // no more items (same record for all 128)
       mbar_arrive(b_itemempty + 8 * b);
       const int nv = I.n_valid;
       const int nt = (nv + kTileTokens - 1) / kTileTokens;
