@@ -176,6 +176,41 @@ struct ItemInfo {   // written by the index warp, read by every role
   int32_t n_valid, group, kvh, chunk, cols, row0, rows_in_group, pad;
 };
 
+// One butterfly step of a warp reduce-scatter: lanes with bit `o` set keep the upper half of
+// their N values, the others the lower half, and each adds (or maxes in) its partner's copy of
+// the half it keeps.
+template <int N, bool MAX>
+__device__ __forceinline__ void reduce_scatter_step(float* v, bool upper, int o) {
+#pragma unroll
+  for (int i = 0; i < N / 2; ++i) {
+    const float send = upper ? v[i] : v[i + N / 2];
+    const float keep = upper ? v[i + N / 2] : v[i];
+    const float r = __shfl_xor_sync(0xffffffffu, send, o);
+    v[i] = MAX ? fmaxf(keep, r) : keep + r;
+  }
+}
+
+// Warp-wide sum (or max) of each of NP = 16 or 32 per-lane columns in NP - 1 shuffles instead of
+// 5 NP: afterwards v[0] of lane l holds column warp_column<NP>(l) reduced over all 32 lanes
+// (for NP = 16 lanes l and l ^ 1 hold the same column).  v is overwritten.
+template <int NP>
+__device__ __forceinline__ int warp_column(int lane) { return NP == 32 ? lane : lane >> 1; }
+template <int NP, bool MAX>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[NP], int lane) {
+  static_assert(NP == 16 || NP == 32, "reduce-scatter covers 16 or 32 columns");
+  reduce_scatter_step<NP, MAX>(v, (lane & 16) != 0, 16);
+  reduce_scatter_step<NP / 2, MAX>(v, (lane & 8) != 0, 8);
+  reduce_scatter_step<NP / 4, MAX>(v, (lane & 4) != 0, 4);
+  reduce_scatter_step<NP / 8, MAX>(v, (lane & 2) != 0, 2);
+  if constexpr (NP == 32) {
+    reduce_scatter_step<2, MAX>(v, (lane & 1) != 0, 1);
+  } else {
+    const float r = __shfl_xor_sync(0xffffffffu, v[0], 1);
+    v[0] = MAX ? fmaxf(v[0], r) : v[0] + r;
+  }
+  return v[0];
+}
+
 __device__ __forceinline__ void decode_item(const PrefillParams& p, int64_t item, int32_t& group,
                                             int32_t& kvh, int32_t& chunk) {
   const int64_t per_kv = static_cast<int64_t>(p.head_chunks) * p.n_groups;
@@ -762,12 +797,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (f & 1) {
           float* rbuf = red + rb * 4 * NP;
+          if constexpr (NP == 16 || NP == 32) {
+            float v[NP];
 #pragma unroll
-          for (int c = 0; c < NP; ++c) {
-            float v = x[c];
+            for (int c = 0; c < NP; ++c) v[c] = x[c];
+            const float m = warp_reduce_scatter<NP, true>(v, lane);
+            if (NP == 32 || (lane & 1) == 0) rbuf[warp * NP + warp_column<NP>(lane)] = m;
+          } else {
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-            if (lane == 0) rbuf[warp * NP + c] = v;
+            for (int c = 0; c < NP; ++c) {
+              float v = x[c];
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+              if (lane == 0) rbuf[warp * NP + c] = v;
+            }
           }
           named_bar_sync(1, 128);
           float alpha[NP];
@@ -825,12 +868,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (quit) break;
       // ---- epilogue: row sums, O / l, LSE
       float* rbuf = red + rb * 4 * NP;
+      if constexpr (NP == 16 || NP == 32) {
+        const float l = warp_reduce_scatter<NP, false>(l_part, lane);   // l_part is done with
+        if (NP == 32 || (lane & 1) == 0) rbuf[warp * NP + warp_column<NP>(lane)] = l;
+      } else {
 #pragma unroll
-      for (int c = 0; c < NP; ++c) {
-        float v = l_part[c];
+        for (int c = 0; c < NP; ++c) {
+          float v = l_part[c];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) rbuf[warp * NP + c] = v;
+          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          if (lane == 0) rbuf[warp * NP + c] = v;
+        }
       }
       named_bar_sync(1, 128);
       // Thread t < cols finishes column t once: its row sum, 1 / l, LSE and output offset go to
