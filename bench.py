@@ -344,6 +344,9 @@ def run_gpu(args, rank, world, local_rank):
     t_wall = time.perf_counter()
     for i in range(args.steps):
         flush.zero_()
+        # ~0.5 ms of GPU spin after the flush: the host enqueues the call meanwhile, so the
+        # events time the device work and not the host's launch path (that is in e2e)
+        torch.cuda._sleep(1 << 20)
         starts[i].record(stream)
         call()
         ends[i].record(stream)

@@ -88,7 +88,10 @@ typedef struct qsa_counters {
  *            requires each row's valid slots to be distinct (a repeated slot is used once).
  *   Slots must be < n_slots of the caches (not checked: the signature carries no slot
  *   count; use qsa_sparse_prefill_ex with n_kv_slots to have them treated as padding).
- *   Union mode allocates its workspace on `stream` (cudaMallocAsync / cudaFreeAsync). */
+ *   Union mode allocates its workspace on `stream` (cudaMallocFromPoolAsync / cudaFreeAsync) from
+ *   a stream-ordered memory pool the library creates per device, whose release threshold is
+ *   unbounded: freed workspaces stay in that pool for later calls (until the process exits), so
+ *   steady-state calls make no driver allocation. */
 qsa_status qsa_sparse_prefill(const void* q, const void* k_cache, const void* v_cache,
                               const int32_t* indices, const int32_t* topk_len,
                               void* out, float* lse,
@@ -180,8 +183,8 @@ qsa_status qsa_sparse_prefill_fp8(const void* q, const void* k_cache, const void
  *   qsa_sparse_prefill; a union needs union_g * n_heads <= 32, otherwise the per-token path
  *   runs and counts a fallback.  n_kv_slots: 0 = unchecked, > 0 = slots >= n_kv_slots are
  *   padding.  q, kv_cache and out must be 16-byte aligned.  Union workspace is allocated on
- *   `stream` (cudaMallocAsync / cudaFreeAsync).  Errors, streams and determinism are as for
- *   qsa_sparse_prefill. */
+ *   `stream` from the library's pool (as for qsa_sparse_prefill).  Errors, streams and
+ *   determinism are as for qsa_sparse_prefill. */
 qsa_status qsa_sparse_mla_prefill(const void* q, const void* kv_cache, const int32_t* indices,
                                   const int32_t* topk_len, void* out, float* lse, int64_t n_rows,
                                   int32_t n_heads, int32_t d_qk, int32_t d_v, int32_t topk,

@@ -6,6 +6,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 
 #include "internal.h"
 
@@ -26,6 +27,34 @@ int pow2_at_least(int v) {
   int p = 32;
   while (p < v) p <<= 1;
   return p;
+}
+
+// Per-call union workspaces come from a library-owned stream-ordered memory pool per device
+// whose release threshold is unbounded: a freed workspace stays in the pool for the next call
+// instead of going back to the driver at the next synchronisation, so steady-state calls make
+// no driver allocation (the pool holds the largest workspace in use until the process exits).
+// Falls back to the device's default pool if a pool cannot be created.
+cudaError_t ws_alloc(void** ptr, size_t bytes, cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaMallocAsync(ptr, bytes, stream);
+  static std::once_flag once[64];
+  static cudaMemPool_t pools[64];
+  static bool have[64];
+  std::call_once(once[dev], [dev] {
+    cudaMemPoolProps props{};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    if (cudaMemPoolCreate(&pools[dev], &props) == cudaSuccess) {
+      uint64_t threshold = UINT64_MAX;
+      have[dev] = cudaMemPoolSetAttribute(pools[dev], cudaMemPoolAttrReleaseThreshold,
+                                          &threshold) == cudaSuccess;
+    }
+  });
+  return have[dev] ? cudaMallocFromPoolAsync(ptr, bytes, pools[dev], stream)
+                   : cudaMallocAsync(ptr, bytes, stream);
 }
 
 struct WsLayout {
@@ -337,7 +366,7 @@ qsa_status run(const void* q, const void* k_cache, const void* v_cache, const in
         return QSA_ERR_WORKSPACE;
       ws = workspace;
     } else {
-      if (cudaMallocAsync(&ws, w.total, stream) != cudaSuccess) return QSA_ERR_CUDA;
+      if (ws_alloc(&ws, w.total, stream) != cudaSuccess) return QSA_ERR_CUDA;
       own_ws = true;
     }
     uint8_t* b = static_cast<uint8_t*>(ws);
@@ -421,7 +450,7 @@ qsa_status run_mla(const void* q, const void* kv_cache, const int32_t* indices,
   void* ws = nullptr;
   if (g.union_g > 1) {
     const WsLayout w = ws_layout(n_rows, topk, g.union_g);
-    if (cudaMallocAsync(&ws, w.total, stream) != cudaSuccess) return QSA_ERR_CUDA;
+    if (ws_alloc(&ws, w.total, stream) != cudaSuccess) return QSA_ERR_CUDA;
     uint8_t* b = static_cast<uint8_t*>(ws);
     p.union_idx = reinterpret_cast<int32_t*>(b + w.idx);
     p.union_bits = b + w.bits;
