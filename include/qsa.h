@@ -261,7 +261,9 @@ qsa_status qsa_sparse_prefill_noalloc(const void* q, const void* k_cache, const 
                                       int32_t head_dim, int32_t topk, float scale,
                                       int32_t union_g, void* stream);
 
-/* Bytes of union-mode workspace for a call (0 when union_g <= 1). */
+/* Bytes of union-mode workspace for a call (0 when union_g <= 1): the groups' slot lists,
+ * ownership bytes and list lengths, and the counter the attention kernel hands its items out
+ * through (zeroed by the union build of the same call). */
 size_t qsa_workspace_bytes(int64_t n_rows, int32_t topk, int32_t union_g);
 
 /* Union build on its own ("DSA prefill ... triton_sparse_mla", Modifications and Accuracy
