@@ -80,10 +80,43 @@ def test_fp8_mixed_paged_and_edges(B):
     assert_parity(out, lse, O, L, what="fp8 mixed")
 
 
-def test_fp8_full_size_group6(B):
-    """The group-6 workload with an e4m3 cache (pages of 64), sampled rows against the oracle."""
-    w = W.with_fp8_cache(W.make("group6_32k"), 64)
+@pytest.mark.parametrize("G", [0, 4])
+def test_fp8_full_size(B, oracle_pool, G):
+    """The group-6 workload (per-token) and the union workload (G = 4) with e4m3 caches (pages of
+    64), every row against the FP8 oracle."""
+    name = "group6_32k" if G == 0 else "union_8k"
+    w = W.with_fp8_cache(W.make(name), 64)
+    out, lse = run(B, w, union_g=G)
+    oracle_pool.check_all_rows((name, "fp8:64"), "fp8", out, lse, f"fp8 {name} G={G}")
+
+
+@pytest.mark.parametrize("c", [4096.0, 3.0e4, 1.0e-6])
+def test_fp8_large_and_small_v_scales(B, c):
+    """V page scales multiplied by c: O scales by c exactly and LSE is unchanged.  With c = 3e4 a
+    probability times its V scale passes the fp16 range unless the kernel normalises the scales
+    per item; with c = 1e-6 it would fall into fp16 subnormals."""
+    from helpers import compare, O_ATOL, LSE_RTOL
+    w = W.with_fp8_cache(W.make_chunk(n_rows=64, context=3000, n_qheads=6, n_kvheads=1, topk=2051,
+                                      seed=77, name="vscale"), 64)
+    w.meta["v_scale"] = (w.meta["v_scale"] * np.float32(c)).astype(np.float32)
     out, lse = run(B, w)
-    rows = np.arange(0, w.n_rows, 331)
-    O, L = ref(w, rows=rows)
-    assert_parity(out, lse, O, L, rows=rows, what="fp8 group6")
+    O, L = ref(w)
+    dO, dL, mism = compare(out.float() / c, lse, O / c, L)
+    assert mism == 0 and dO <= O_ATOL and dL <= LSE_RTOL, (c, dO, dL, mism)
+
+
+def test_fp8_mixed_page_scale_magnitudes(B):
+    """Per-page V scales spread over four decades and K scales over one, union and per-token:
+    errors stay within 2e-2 of the largest output magnitude."""
+    from helpers import compare, LSE_RTOL
+    rng = np.random.default_rng(78)
+    for G in (0, 2):
+        w = W.with_fp8_cache(W.make_union(n_rows=300, topk=384), 16)
+        m = w.meta
+        m["v_scale"] = (m["v_scale"] * 10.0 ** rng.uniform(-2, 2, m["v_scale"].shape)).astype(np.float32)
+        m["k_scale"] = (m["k_scale"] * 10.0 ** rng.uniform(-0.5, 0.5, m["k_scale"].shape)).astype(np.float32)
+        out, lse = run(B, w, union_g=G)
+        O, L = ref(w)
+        dO, dL, mism = compare(out, lse, O, L)
+        bound = 2e-2 * max(1.0, float(np.abs(O).max()))
+        assert mism == 0 and dO <= bound and dL <= LSE_RTOL, (G, dO, bound, dL, mism)

@@ -70,6 +70,20 @@ __device__ __noinline__ bool mla_wait_slow(uint32_t bar, uint32_t parity, volati
   }
 }
 
+// Bounded wait that ignores the abort flag: after an abort, lets copies and MMAs already issued
+// complete before shared or tensor memory is given up.
+__device__ __noinline__ bool mla_drain(uint32_t bar, uint32_t parity, int32_t* status,
+                                       unsigned long long limit) {
+  const unsigned long long t0 = mla_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (mla_ns() - t0 > limit) {
+      atomicCAS(status, 0, 0x100 | kMDrain);
+      return false;
+    }
+  }
+  return true;
+}
+
 __device__ __forceinline__ bool mla_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                          int32_t* status, int32_t site) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -361,9 +375,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Drain: let the newest copy of every stage this warp shared in land (bounded).
       if (pw < kMlaPairOwners) {
         for (uint32_t s = l_issued > static_cast<uint32_t>(RP) ? l_issued - RP : 0; s < l_issued; ++s)
-          mla_wait_slow(b_lfull + 8 * (s % RP), (s / RP) & 1, abort_flag, status, kMDrain, kMlaDrainNs);
+          mla_drain(b_lfull + 8 * (s % RP), (s / RP) & 1, status, kMlaDrainNs);
       } else if (pw == kMlaRopeOwner && r_issued > 0) {
-        mla_wait_slow(b_rfull, (r_issued - 1) & 1, abort_flag, status, kMDrain, kMlaDrainNs);
+        mla_drain(b_rfull, (r_issued - 1) & 1, status, kMlaDrainNs);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -521,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Every MMA this thread issued has completed once `fin` flips.
     if (lane == 0) {
       tc_commit(b_fin);
-      mla_wait_slow(b_fin, 0, abort_flag, status, kMDrain, aborted ? kMlaDrainNs : kMlaWaitNs);
+      mla_drain(b_fin, 0, status, aborted ? kMlaDrainNs : kMlaWaitNs);
     }
     __syncwarp();
   } else if (warp < kSoftmaxWarps) {

@@ -64,11 +64,14 @@ extern "C" qsa_status qsa_sparse_prefill_noalloc(
                                       n_rows < 0 ? 0 : n_rows, 1, &g);
   if (st != QSA_OK) return st;
   if (g.union_g > 1 &&
-      qsa_workspace_bytes(n_rows, topk, g.union_g) > qsa::kNoAllocScratchBytes)
+      qsa_union_workspace_bytes(n_rows, topk, g.union_g) > qsa::kNoAllocScratchBytes)
     return QSA_ERR_WORKSPACE;   // call needs more scratch than the fixed array holds
   void* scratch = nullptr;
   if (!q || !k_cache || !v_cache || !indices || !out) return QSA_ERR_INVALID_ARG;
-  if (n_rows > 0 && qsa::scratch_address(&scratch) != cudaSuccess) return QSA_ERR_CUDA;
+  // Only union calls use the array: a per-token call never looks its address up, so it
+  // neither loads the array's module nor needs to come before a stream capture.
+  if (n_rows > 0 && g.union_g > 1 && qsa::scratch_address(&scratch) != cudaSuccess)
+    return QSA_ERR_CUDA;
   return qsa_sparse_prefill_ex(q, k_cache, v_cache, indices, topk_len, out, lse, n_rows,
                                n_qheads, n_kvheads, head_dim, topk, scale, union_g, 0, scratch,
                                qsa::kNoAllocScratchBytes, nullptr, stream);

@@ -88,6 +88,19 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile i
   }
 }
 
+// Bounded wait that ignores the abort flag: after an abort, lets copies and MMAs already issued
+// complete before shared or tensor memory is given up.
+__device__ __noinline__ bool drain_bar(uint32_t bar, uint32_t parity, unsigned long long limit) {
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > limit) {
+      atomicCAS(&g_device_status, 0, 0x100 | kSiteDrain);
+      return false;
+    }
+  }
+  return true;
+}
+
 // Bounded wait for phase `parity` of mbarrier `bar`.  False on timeout or abort.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                          int32_t site) {
@@ -235,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kLookahead = lookahead_for(UNION);
   constexpr int kSBufs = kLookahead + 1;
   const int slot_cap = UNION ? 0 : p.slot_cap;
-  const SmemLayout L = smem_layout(NP, p.stages, slot_cap);
+  const SmemLayout L = smem_layout(NP, p.stages, slot_cap, FP8);
   const int R = p.stages;
 
   // barrier addresses
@@ -258,6 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                           2 * 4 * NP * sizeof(float));
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* const vote = reinterpret_cast<int*>(tmem_slot + 2);   // [3]
+  float* const vred = reinterpret_cast<float*>(tmem_slot + 8);   // [4] FP8: per-warp V-scale max
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -450,17 +464,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return q;
       };
+      // tensor-map row of union slot t; a slot whose row would pass the map (or int32) becomes
+      // padding, as in the per-token compaction
+      auto union_row = [&](int t) -> int32_t {
+        if (t >= nv) return p.pad_row;
+        const int64_t y = static_cast<int64_t>(ul[t]) * p.n_kvheads + I.kvh;
+        return y < static_cast<int64_t>(p.pad_row) ? static_cast<int32_t>(y) : p.pad_row;
+      };
       // union slots of a piece's tile (global memory): lane holds tokens 4*lane .. 4*lane+3
       auto union_rows = [&](int q) {
         int tile, is_v, half;
         piece_of<kLookahead>(q, nt, tile, is_v, half);
         const int t = tile * kTileTokens + 4 * lane;
-        int4 y;
-        y.x = t + 0 < nv ? ul[t + 0] * p.n_kvheads + I.kvh : p.pad_row;
-        y.y = t + 1 < nv ? ul[t + 1] * p.n_kvheads + I.kvh : p.pad_row;
-        y.z = t + 2 < nv ? ul[t + 2] * p.n_kvheads + I.kvh : p.pad_row;
-        y.w = t + 3 < nv ? ul[t + 3] * p.n_kvheads + I.kvh : p.pad_row;
-        return y;
+        return make_int4(union_row(t), union_row(t + 1), union_row(t + 2), union_row(t + 3));
       };
       const int q0 = next_piece();
       // The union slots of the warp's next piece are loaded one piece ahead, so their latency
@@ -590,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t landed = FP8 ? b_land : b_full;
       for (uint32_t s = issued > static_cast<uint32_t>(R) ? issued - R : 0; s < issued; ++s)
         if (static_cast<int>(s % R) % W == pw)
-          wait_slow(landed + 8 * (s % R), (s / R) & 1, abort_flag, kSiteDrain, kDrainLimitNs);
+          drain_bar(landed + 8 * (s % R), (s / R) & 1, kDrainLimitNs);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
@@ -600,6 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       : idesc_bf16_f32(128, NP, true, false);
     uint32_t seq = 0, js = 0, it = 0;
     bool aborted = false;
+    const bool cp_engine = !FP8 && p.gather_tma == 0;
     for (;; ++it) {
       const uint32_t b = it & 1, ph = (it >> 1) & 1;
       if (!__all_sync(0xffffffffu, wait_bar(b_itemfull + 8 * b, ph, abort_flag, kSiteItemFull))) {
@@ -629,7 +646,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          fence_proxy_async_smem();   // cp.async stage writes -> tensor-core (async proxy) reads
+          // cp.async stage writes -> tensor-core (async proxy) reads; TMA writes are already in
+          // the async proxy, and the FP8 rewrite fences on the writer side
+          if (cp_engine) fence_proxy_async_smem();
           if (lane == 0) {
             const uint32_t klo = base + L.ring + (s_lo % R) * kStageBytes;
             const uint32_t khi = base + L.ring + (s_hi % R) * kStageBytes;
@@ -660,7 +679,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          fence_proxy_async_smem();   // cp.async stage writes -> tensor-core (async proxy) reads
+          // cp.async stage writes -> tensor-core (async proxy) reads; TMA writes are already in
+          // the async proxy, and the FP8 rewrite fences on the writer side
+          if (cp_engine) fence_proxy_async_smem();
           if (lane == 0) {
             const uint32_t pbase = base + L.pbuf + pb * L.p_bytes;
 #pragma unroll
@@ -688,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Every MMA this thread issued has completed once `fin` flips.
     if (lane == 0) {
       tc_commit(b_fin);
-      wait_slow(b_fin, 0, abort_flag, kSiteDrain, aborted ? kDrainLimitNs : kWaitLimitNs);
+      drain_bar(b_fin, 0, aborted ? kDrainLimitNs : kWaitLimitNs);
     }
     __syncwarp();
   } else {
@@ -739,6 +760,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_used[c] = NEG_INF;
         l_part[c] = 0.f;
       }
+      // FP8 caches: P is stored in fp16 as p * v_scale with p <= 2^8 (the lazy rescale
+      // threshold), so a large V page scale could overflow fp16.  The item's V scales are
+      // normalised by 2^-v_exp, v_exp the binary exponent of their largest magnitude (every
+      // stored P then stays below 2^8), and the epilogue multiplies O back by 2^v_exp -- both
+      // exact power-of-two scalings.
+      int v_exp = 0;
+      float v_norm = 1.f;
+      if (FP8) {
+        float vmax = 0.f;
+        for (int j = 0; j < nt; ++j) {
+          const int token = j * kTileTokens + t;
+          if (token < nv) {
+            const int64_t slot = UNION ? static_cast<int64_t>(ul_b[token])
+                                       : static_cast<int64_t>(slots_b[token]) / p.n_kvheads;
+            vmax = fmaxf(vmax, fabsf(__ldg(p.v_scale + (slot / p.page_size) * p.n_kvheads + I.kvh)));
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
+        if (lane == 0) vred[warp] = vmax;
+        named_bar_sync(1, 128);
+        vmax = fmaxf(fmaxf(vred[0], vred[1]), fmaxf(vred[2], vred[3]));
+        frexpf(vmax, &v_exp);            // vmax < 2^v_exp
+        v_exp = max(-126, min(v_exp, 126));
+        v_norm = ldexpf(1.f, -v_exp);
+      }
       uint32_t bits_next = 0;
       if (UNION && nt > 0) bits_next = t < nv ? ub[t] : 0u;
       bool quit = false;
@@ -765,7 +812,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      : static_cast<int64_t>(slots_b[token]) / p.n_kvheads;
           const int64_t si = (slot / p.page_size) * p.n_kvheads + I.kvh;
           logit_scale *= __ldg(p.k_scale + si);
-          v_scale = __ldg(p.v_scale + si);
+          v_scale = __ldg(p.v_scale + si) * v_norm;
         }
         bad |= !wait_bar(b_sfull + 8 * ss, ssph, abort_flag, kSiteSFull);
         tc_fence_after();
@@ -901,7 +948,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           row = I.row0;
           head = static_cast<int64_t>(I.kvh) * p.group + I.chunk * p.chunk_cols + t;
         }
-        inv_s[t] = l > 0.f ? 1.f / l : 0.f;
+        inv_s[t] = l > 0.f ? (FP8 ? ldexpf(1.f / l, v_exp) : 1.f / l) : 0.f;
         off_s[t] = (row * Hq + head) * kHeadDim;
         if (p.lse != nullptr) p.lse[row * Hq + head] = l > 0.f ? (my_m + log2f(l)) * kLn2 : NEG_INF;
       }
