@@ -30,3 +30,12 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def oracle_pool():
+    """Spawned worker processes that run the oracle on every row of a full-size call."""
+    from oracle_pool import OraclePool
+    pool = OraclePool()
+    yield pool
+    pool.close()

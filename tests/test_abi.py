@@ -115,19 +115,12 @@ def test_entry_validation_before_any_cuda_call(lib):
     assert pr(fake, 1000, fake, 4, 10, 3, ctypes.byref(ms), None) == 1      # unknown engine
     assert pr(fake + 8, 1000, fake, 4, 10, 1, ctypes.byref(ms), None) == 1  # misaligned cache
     assert pr(fake, 1000, fake, 0, 10, 0, ctypes.byref(ms), None) == 1      # empty row table
-    pm = lib.qsa_probe_gather_mma
-    ns = ctypes.c_float(0.0)
-    #         cache rows  table pieces ppc eng mode  n  batches
-    assert pm(fake, 1000, fake, 4, 10, 1, 3, 16, 10, ctypes.byref(ms), ctypes.byref(ns), None) == 1  # mode
-    assert pm(fake, 1000, fake, 4, 10, 1, 1, 24, 10, ctypes.byref(ms), ctypes.byref(ns), None) == 1  # N % 16
-    assert pm(fake, 1000, fake, 4, 10, 1, 2, 128, 10, ctypes.byref(ms), ctypes.byref(ns), None) == 1  # N > 64
-    assert pm(fake, 1000, fake, 4, 0, 1, 1, 16, 0, ctypes.byref(ms), ctypes.byref(ns), None) == 1   # no batches
-    assert pm(fake, 1000, fake, 4, -1, 1, 1, 16, 10, ctypes.byref(ms), ctypes.byref(ns), None) == 1  # ppc < 0
-    assert pm(fake, 1000, fake, 4, 10, 1, 1, 16, 10, ctypes.byref(ms), None, None) == 1              # no output
 
 
 def test_workspace_bytes(lib):
     from top_sparse_attention_row_gb300 import binding as B
+    for args in ((8192, 2048, 4), (1023, 16, 3), (5, 7, 8), (100, 2048, 1), (0, 16, 4)):
+        assert lib.qsa_union_workspace_bytes(*args) == lib.qsa_workspace_bytes(*args)
     assert B.workspace_bytes(8192, 2048, 1) == 0
     n = B.workspace_bytes(8192, 2048, 4)
     groups = 2048
@@ -204,3 +197,32 @@ def test_fp8_entry_validation(lib):
     assert f(fake, fake + 8, fake, fake, fake, 64, fake, None, fake, None, 10, 6, 1, 256, 2051, 0.0625, 0, 0, None) == 1
     assert f(fake, fake, fake, fake, fake, 64, fake, None, fake, None, 10, 6, 1, 128, 2051, 0.0625, 0, 0, None) == 2
     assert f(fake, fake, fake, fake, fake, 64, fake, None, fake, None, 0, 6, 1, 256, 2051, 0.0625, 0, 0, None) == 0
+
+
+def _params(name):
+    src = open(os.path.join(ROOT, "include", "qsa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    m = re.search(r"\b" + name + r"\s*\(([^)]*)\)\s*;", src)
+    assert m, name
+    return [re.split(r"[\s*]+", p.strip())[-1] for p in m.group(1).split(",") if p.strip()]
+
+
+def test_boundary_entry_points_and_argument_lists(lib):
+    """Every call of the boundary is exported under its name, and the attention entry keeps the
+    argument list of the operation: q, caches, indices, topk_len, outputs, sizes, scale, union size
+    and stream, in that order; the extended entry adds the slot count, the caller workspace and a
+    forced geometry before the stream."""
+    for name in ("qsa_sparse_prefill", "qsa_sparse_prefill_ex", "qsa_union_workspace_bytes",
+                 "qsa_union_build", "qsa_select_geometry", "qsa_get_counters", "qsa_reset_counters",
+                 "qsa_status_string", "qsa_version", "qsa_get_device_status"):
+        assert hasattr(lib, name), name
+    main = ["q", "k_cache", "v_cache", "indices", "topk_len", "out", "lse", "n_rows", "n_qheads",
+            "n_kvheads", "head_dim", "topk", "scale", "union_g", "stream"]
+    assert _params("qsa_sparse_prefill") == main
+    assert _params("qsa_sparse_prefill_ex") == main[:-1] + ["n_kv_slots", "workspace",
+                                                            "workspace_bytes", "forced", "stream"]
+    assert _params("qsa_union_workspace_bytes") == ["n_rows", "topk", "union_g"]
+    # the selector also takes the KV head count (work items are row groups x KV heads) and the SM
+    # count (so host-only callers choose it; <= 0 asks the current device)
+    assert _params("qsa_select_geometry") == ["n_qheads", "n_kvheads", "union_g", "topk",
+                                              "head_dim", "n_rows", "num_sms", "out"]

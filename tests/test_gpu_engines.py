@@ -90,16 +90,3 @@ def test_geometry_log_line(B):
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [l for l in r.stderr.splitlines() if l.startswith("qsa: d=256")]
     assert len(lines) == 2 and "union=1" in lines[0] and "union=2" in lines[1], r.stderr
-
-
-@pytest.mark.parametrize("mma_a", ["smem", "tmem"])
-def test_gather_mma_contention_probe(B, mma_a):
-    import torch
-    g = torch.Generator().manual_seed(8)
-    n_rows = 1 << 15
-    cache = torch.randn(n_rows, 256, generator=g).to(torch.bfloat16).cuda()
-    table = torch.randint(0, n_rows, (512, 128), generator=g, dtype=torch.int32).cuda()
-    alone = B.probe_gather_mma(cache, table, 0, mma_a=mma_a, mma_n=16, mma_batches=500)
-    assert alone["gbs"] is None and np.isfinite(alone["mma_ns"]) and alone["mma_ns"] > 0.0
-    both = B.probe_gather_mma(cache, table, 64, mma_a=mma_a, mma_n=32)
-    assert np.isfinite(both["gbs"]) and both["gbs"] > 100.0 and both["mma_ns"] > 0.0

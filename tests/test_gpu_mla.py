@@ -113,15 +113,12 @@ def test_mla_edge_rows(B):
 
 
 @pytest.mark.parametrize("G", [0, 2, 4])
-def test_mla_full_size_8k(B, G):
+def test_mla_full_size_8k(B, oracle_pool, G):
     """The 8192-token MLA prefill (8 heads, topk 2048, random walk) as the benchmark runs it,
-    against the oracle on sampled rows (first tile rows, walk rows, group tails)."""
+    every row against the oracle."""
     w = W.make("mla_8k")
     out, lse = run(B, w, union_g=G)
-    rows = np.unique(np.concatenate([np.arange(0, w.n_rows, 409), [1, 2, 3, 2047, 2048, 2049,
-                                                                     8189, 8190, 8191]]))
-    O, L = ref(w, rows=rows)
-    assert_parity(out, lse, O, L, rows=rows, what=f"mla_8k G={G}")
+    oracle_pool.check_all_rows(("mla_8k", ""), "mla", out, lse, f"mla_8k G={G}")
 
 
 def paged_mla_case(seed=70, ps=64, kv_lens=(700, 1300, 400), rows=(30, 50, 20), topk=512, heads=8):

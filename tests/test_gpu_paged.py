@@ -140,10 +140,10 @@ def test_paged_many_requests(B):
     assert_parity(out, lse, O, L, what="300 requests")
 
 
-def test_paged_full_size_mixed_batch(B):
+def test_paged_full_size_mixed_batch(B, oracle_pool):
     """The chunked mixed batch (4 requests, 14848 rows, 2024 pages of 64) through the paged
-    entry: bit-identical to the plain entry on the translated slots, and sampled rows against
-    the paged oracle."""
+    entry: bit-identical to the plain entry on the translated slots, and every row against the
+    paged oracle."""
     import torch
     w = W.make("mixed_paged")
     m = w.meta
@@ -154,8 +154,4 @@ def test_paged_full_size_mixed_batch(B):
     torch.cuda.synchronize()
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
     assert torch.equal(lse, lse2)
-    rows = np.unique(np.concatenate([np.arange(0, w.n_rows, 997), m["cu_seqlens_q"][1:-1],
-                                     m["cu_seqlens_q"][1:] - 1]))
-    O, L = paged_oracle(w, m["logical_indices"], m["cu_seqlens_q"], m["kv_lens_array"],
-                        m["page_table"], m["page_size"], m["n_pages"], rows=rows)
-    assert_parity(out, lse, O, L, rows=rows, what="full mixed batch, paged entry")
+    oracle_pool.check_all_rows(("mixed_paged", ""), "paged", out, lse, "full mixed batch, paged entry")

@@ -153,7 +153,7 @@ def test_counters_and_step_down(B):
     q, k, v, idx, tl = to_device(w)
     B.reset_counters()
     B.sparse_prefill(q, k, v, idx, tl, w.scale)
-    out, lse = B.sparse_prefill(q, k, v, idx, tl, w.scale, forced={"stages": 8, "grid": 7})
+    out, lse = B.sparse_prefill(q, k, v, idx, tl, w.scale, forced={"stages": 16, "grid": 7})
     torch.cuda.synchronize()
     c = B.counters()
     assert c["calls_per_token"] == 2 and c["step_downs"] == 1 and c["kernel_launches"] == 2

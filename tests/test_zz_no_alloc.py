@@ -5,6 +5,10 @@ Its union-mode scratch is a fixed array the library owns, so two calls in a row 
 memory; each must match the allocating entry point within the parity bounds.  This file is
 named to be collected last, so a run that stops at the first failure has already run every
 other test; it also passes on its own in a fresh process."""
+import os
+import subprocess
+import sys
+
 import numpy as np
 import pytest
 
@@ -60,3 +64,26 @@ def test_noalloc_refuses_calls_beyond_its_scratch(B):
     with pytest.raises(RuntimeError, match="WORKSPACE"):
         B.sparse_prefill_noalloc(q, kv, kv, idx, None, 0.0625, union_g=2)
     assert B.counters()["kernel_launches"] == 0       # refused before anything was enqueued
+
+
+def test_noalloc_per_token_first_in_a_fresh_process(B):
+    """A per-token call that comes first in a process needs no scratch: it runs without looking
+    the array up, and a union call after it still matches the allocating entry."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = (
+        "import sys, torch\n"
+        f"sys.path[:0] = [{root!r}, {os.path.join(root, 'tests')!r}]\n"
+        "from top_sparse_attention_row_gb300 import binding as B, workloads as W\n"
+        "from helpers import to_device, compare\n"
+        "B.load_library()\n"
+        "w = W.make_tiny(); q, k, v, idx, tl = to_device(w)\n"
+        "for G in (0, 2):\n"
+        "    o, l = B.sparse_prefill_noalloc(q, k, v, idx, tl, w.scale, union_g=G)\n"
+        "    ro, rl = B.sparse_prefill(q, k, v, idx, tl, w.scale, union_g=G)\n"
+        "    torch.cuda.synchronize()\n"
+        "    dO, dL, mism = compare(o, l, ro.float().cpu().numpy(), rl.cpu().numpy())\n"
+        "    assert mism == 0 and dO <= 2e-2 and dL <= 1e-3, (G, dO, dL, mism)\n"
+        "assert B.device_status() == 0\n"
+        "print('ok')\n")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stderr[-2000:]
