@@ -49,7 +49,7 @@ typedef enum qsa_status {
   QSA_OK = 0,
   QSA_ERR_INVALID_ARG = 1,   /* null required pointer, bad size, misaligned pointer */
   QSA_ERR_UNSUPPORTED = 2,   /* head_dim != 256, device is not sm_103, shape beyond limits */
-  QSA_ERR_WORKSPACE = 3,     /* caller workspace smaller than qsa_workspace_bytes() */
+  QSA_ERR_WORKSPACE = 3,     /* caller workspace smaller than qsa_union_workspace_bytes() */
   QSA_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
   QSA_ERR_TIMEOUT = 5        /* a kernel wait ran past its limit (see qsa_get_device_status) */
 } qsa_status;
@@ -103,7 +103,7 @@ qsa_status qsa_sparse_prefill(const void* q, const void* k_cache, const void* v_
  *   n_kv_slots: 0 = unchecked; > 0 = slots >= n_kv_slots are padding (and gathers are
  *               bounds-checked against it).
  *   workspace / workspace_bytes: caller scratch for union mode (NULL = allocate on stream);
- *               must hold qsa_workspace_bytes(n_rows, topk, effective union_g) bytes and be
+ *               must hold qsa_union_workspace_bytes(n_rows, topk, effective union_g) bytes and be
  *               256-byte aligned.  Unused by the per-token path.
  *   forced:     host pointer, NULL = selector; fields > 0 override stages and grid (an
  *               oversized stage count is stepped down to fit and counted). */
@@ -243,11 +243,12 @@ qsa_status qsa_split_touched_pages(const int32_t* indices, int64_t n_indices, co
  * hosts that give kernels no allocator.  Union-mode scratch lives in a fixed array of
  * QSA_NOALLOC_SCRATCH_BYTES in device global memory that the library owns; every GPU on which
  * the library is loaded holds that array until the process exits.
- *   - A call whose union workspace (qsa_workspace_bytes) exceeds QSA_NOALLOC_SCRATCH_BYTES is
+ *   - A call whose union workspace (qsa_union_workspace_bytes) exceeds QSA_NOALLOC_SCRATCH_BYTES is
  *     rejected with QSA_ERR_WORKSPACE before anything is enqueued.  The per-token path needs
  *     no scratch and has no such limit.
- *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress,
- *     with that device current); make that first call before any stream capture.
+ *   - The first union call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first union call before any
+ *     stream capture.  Per-token calls never touch the array.
  *   - Every call uses the same array, which keeps the previous call's contents; nothing in it
  *     needs to start at zero (each call writes every entry it later reads).  Calls whose work
  *     overlaps on the GPU (different streams, or different host threads) race on the array:
@@ -263,12 +264,17 @@ qsa_status qsa_sparse_prefill_noalloc(const void* q, const void* k_cache, const 
 
 /* Bytes of union-mode workspace for a call (0 when union_g <= 1): the groups' slot lists,
  * ownership bytes and list lengths, and the counter the attention kernel hands its items out
- * through (zeroed by the union build of the same call). */
+ * through (zeroed by the union build of the same call).  The workspace is what union mode
+ * allocates per call ("DSA prefill ... triton_sparse_mla", Modifications: the union lists and
+ * ownership bits are built per step before the attention kernel reads them).
+ * qsa_workspace_bytes is the same function under its earlier name. */
+size_t qsa_union_workspace_bytes(int64_t n_rows, int32_t topk, int32_t union_g);
 size_t qsa_workspace_bytes(int64_t n_rows, int32_t topk, int32_t union_g);
 
 /* Union build on its own ("DSA prefill ... triton_sparse_mla", Modifications and Accuracy
- * Tests: each row sorted on its own; a row emits a slot no earlier row of its group
- * selected and ORs in the bit of every row that did; each slot once, -1 dropped).
+ * Tests: every row's selection is sorted by itself; a slot enters the group's list through
+ * the first row holding it, its bits mark every row of the group that selected it, it is
+ * listed once, and -1 padding is left out).
  *   sorted_out [n_rows, topk] (nullable): each row's valid slots ascending, then -1.
  *   union_idx  [n_groups, union_g*topk]: group list, canonical order (row 0's emitted slots
  *              ascending, then row 1's, ...), -1 padded.
@@ -297,21 +303,6 @@ qsa_status qsa_select_geometry(int32_t n_qheads, int32_t n_kvheads, int32_t unio
 qsa_status qsa_probe_gather_ceiling(const void* cache, int64_t n_rows, const int32_t* rows,
                                     int64_t n_table_pieces, int32_t pieces_per_cta,
                                     int32_t engine, float* ms_out, void* stream);
-
-/* Gather / tensor-pipe contention probe (measurement helper, no counterpart on the pages): the
- * gather of qsa_probe_gather_ceiling (same arguments; pieces_per_cta may be 0) while one more warp
- * per SM keeps the tensor pipe busy with batches of 16 tcgen05.mma M128 x mma_n x K16 (bf16 in,
- * fp32 out; mma_n a multiple of 16, at most 64), one commit per batch, two batches in flight.
- * mma_mode 1 reads A from shared memory (as the attention kernel's operands do), 2 from tensor
- * memory.  The MMAs run until the gather ends (at most mma_batches batches), or exactly
- * mma_batches batches when pieces_per_cta is 0.  Writes the kernel's elapsed milliseconds to
- * *ms_out and the tensor pipe's mean nanoseconds per MMA on one SM to *mma_ns_out (host
- * pointers); synchronises `stream`.  QSA_ERR_INVALID_ARG on a bad argument, QSA_ERR_TIMEOUT if a
- * bounded wait (1 s) ran out. */
-qsa_status qsa_probe_gather_mma(const void* cache, int64_t n_rows, const int32_t* rows,
-                                int64_t n_table_pieces, int32_t pieces_per_cta, int32_t engine,
-                                int32_t mma_mode, int32_t mma_n, int32_t mma_batches,
-                                float* ms_out, float* mma_ns_out, void* stream);
 
 /* Failure-detection test hook (no counterpart on the pages): the next attention call
  * (qsa_sparse_prefill*, qsa_sparse_mla_prefill) launches with its index warps withholding their

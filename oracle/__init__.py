@@ -20,10 +20,10 @@ Functions and the passages they follow:
   ... triton_sparse_mla" (Motivation: online softmax in registers; Robustness:
   -1 marks an invalid slot, topk_length from metadata).
 * ``union.sorted_rows`` / ``union.union_build`` -- the G-token union with its
-  ownership bitmask ("DSA prefill ... triton_sparse_mla", Modifications: rows
-  sorted on their own, a token emits a row if no earlier token of the group
-  selected it and ORs in the bit of every token that did; Accuracy Tests: the
-  dedup contract -- each row once, bits = OR of owners, -1 dropped).
+  ownership bitmask ("DSA prefill ... triton_sparse_mla", Modifications: each
+  row's selection is sorted by itself, a slot joins the list through the first
+  row holding it and carries one bit per owning row; Accuracy Tests: the dedup
+  contract -- listed once, bits = OR of owners, -1 dropped).
 * ``union.union_attention`` -- attention of each token of a group over the
   union list restricted to its own ownership bit (same page: the bitmask
   restores each token's own softmax support, identical to per-token).

@@ -3,11 +3,12 @@
 TEST INFRASTRUCTURE ONLY (see the package docstring).
 
 Follows "DSA prefill ... triton_sparse_mla", Modifications: G adjacent query
-rows share one gathered index set; each row's selection is sorted on its own;
-a row emits a slot if no earlier row of its group selected it, and ORs in the
-bit of every row that did.  Accuracy Tests on the same page fix the contract:
-each slot appears once in a group's list, its bits are the OR of its owners,
--1 padding is dropped.
+rows share one gathered index set.  Every row's selection is sorted by itself;
+a slot enters the group's list through the first row that selected it, and its
+ownership bits record every row of the group whose selection holds it.  The
+Accuracy Tests section of that page states the resulting contract: a slot is
+listed once per group, its bits are the OR over the rows that own it, and -1
+padding never appears.
 
 Readings (the page prints no layout):
 * groups are G consecutive rows of the flat row array; the last group may

@@ -19,14 +19,14 @@ STATUS_NAMES = {0: "QSA_OK", 1: "QSA_ERR_INVALID_ARG", 2: "QSA_ERR_UNSUPPORTED",
                 3: "QSA_ERR_WORKSPACE", 4: "QSA_ERR_CUDA", 5: "QSA_ERR_TIMEOUT"}
 
 # Every symbol include/qsa.h declares (checked by the CPU test suite).
-EXPORTED = ["qsa_sparse_prefill", "qsa_sparse_prefill_ex", "qsa_workspace_bytes",
+EXPORTED = ["qsa_sparse_prefill", "qsa_sparse_prefill_ex", "qsa_union_workspace_bytes",
+            "qsa_workspace_bytes",
             "qsa_union_build", "qsa_select_geometry", "qsa_get_counters", "qsa_reset_counters",
             "qsa_status_string", "qsa_version", "qsa_get_device_status",
             "qsa_sparse_prefill_noalloc", "qsa_probe_gather_ceiling",
             "qsa_sparse_prefill_paged", "qsa_sparse_mla_prefill", "qsa_select_mla_geometry",
             "qsa_page_mark", "qsa_page_split", "qsa_split_touched_pages",
-            "qsa_sparse_prefill_fp8", "qsa_debug_stall_next_call", "qsa_sparse_mla_prefill_paged",
-            "qsa_probe_gather_mma"]
+            "qsa_sparse_prefill_fp8", "qsa_debug_stall_next_call", "qsa_sparse_mla_prefill_paged"]
 
 # Size of the library-owned scratch array used by qsa_sparse_prefill_noalloc (include/qsa.h).
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -98,11 +98,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qsa_sparse_mla_prefill_paged.restype = ctypes.c_int
     lib.qsa_probe_gather_ceiling.argtypes = [vp, i64, vp, i64, i32, i32, ctypes.POINTER(f32), vp]
     lib.qsa_probe_gather_ceiling.restype = ctypes.c_int
-    lib.qsa_probe_gather_mma.argtypes = [vp, i64, vp, i64, i32, i32, i32, i32, i32,
-                                         ctypes.POINTER(f32), ctypes.POINTER(f32), vp]
-    lib.qsa_probe_gather_mma.restype = ctypes.c_int
-    lib.qsa_workspace_bytes.argtypes = [i64, i32, i32]
-    lib.qsa_workspace_bytes.restype = sz
+    for name in ("qsa_union_workspace_bytes", "qsa_workspace_bytes"):
+        getattr(lib, name).argtypes = [i64, i32, i32]
+        getattr(lib, name).restype = sz
     lib.qsa_union_build.argtypes = [vp, vp, i64, i32, i32, i64, vp, vp, vp, vp, vp]
     lib.qsa_union_build.restype = ctypes.c_int
     lib.qsa_select_geometry.argtypes = [i32, i32, i32, i32, i32, i64, i32, ctypes.POINTER(Geometry)]
@@ -456,31 +454,11 @@ def probe_gather_ceiling(cache_rows, row_table, pieces_per_cta: int = 1500, engi
     return sms * pieces_per_cta * 32768 / (ms.value * 1e-3) / 1e9
 
 
-def probe_gather_mma(cache_rows, row_table, pieces_per_cta: int = 1500, engine: str = "tma",
-                     mma_a: str = "smem", mma_n: int = 16, mma_batches: int = 1 << 20,
-                     stream=None) -> dict:
-    """Gather / tensor-pipe contention probe (qsa_probe_gather_mma): the gather-ceiling probe with
-    one warp per SM issuing tcgen05.mma M128 x mma_n x K16 batches for as long as the gather runs
-    (or exactly mma_batches batches when pieces_per_cta is 0).  mma_a: "smem" or "tmem" (where A
-    is read from).  Returns {"gbs": gather GB/s over all SMs (None without a gather),
-    "ms": kernel time, "mma_ns": tensor-pipe ns per MMA on one SM}."""
-    import torch
-    lib = load_library()
-    _require(cache_rows, torch.bfloat16, "cache_rows", 2)
-    _require(row_table, torch.int32, "row_table", 2)
-    ms, ns = ctypes.c_float(0.0), ctypes.c_float(0.0)
-    st = lib.qsa_probe_gather_mma(_ptr(cache_rows), cache_rows.shape[0], _ptr(row_table),
-                                  row_table.shape[0], int(pieces_per_cta), GATHER_ENGINES[engine],
-                                  {"smem": 1, "tmem": 2}[mma_a], int(mma_n), int(mma_batches),
-                                  ctypes.byref(ms), ctypes.byref(ns), _stream_ptr(stream))
-    _check(st, "qsa_probe_gather_mma")
-    sms = torch.cuda.get_device_properties(cache_rows.device).multi_processor_count
-    gbs = sms * pieces_per_cta * 32768 / (ms.value * 1e-3) / 1e9 if pieces_per_cta else None
-    return {"gbs": gbs, "ms": ms.value, "mma_ns": ns.value}
+def union_workspace_bytes(n_rows: int, topk: int, union_g: int) -> int:
+    return int(load_library().qsa_union_workspace_bytes(n_rows, topk, union_g))
 
 
-def workspace_bytes(n_rows: int, topk: int, union_g: int) -> int:
-    return int(load_library().qsa_workspace_bytes(n_rows, topk, union_g))
+workspace_bytes = union_workspace_bytes
 
 
 def select_geometry(n_qheads, n_kvheads, union_g, topk, head_dim, n_rows, num_sms=0) -> dict:

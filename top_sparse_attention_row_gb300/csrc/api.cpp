@@ -73,9 +73,9 @@ WsLayout ws_layout(int64_t n_rows, int32_t topk, int32_t G) {
   return w;
 }
 
-// Pure host selection.  `forced` may override stages / grid; an oversized stage count steps
-// down to the largest that fits ("DSA prefill ... triton_sparse_mla", Robustness: the launcher
-// steps the shared-memory tile down instead of failing).
+// Pure host selection.  `forced` may override stages / grid; a stage count that does not fit
+// is reduced to the largest that does, rather than refused ("DSA prefill ...
+// triton_sparse_mla", Robustness: shared-memory limits are met by a smaller tile).
 qsa_status select(int32_t Hq, int32_t Hkv, int32_t union_g, int32_t topk, int32_t head_dim,
                   int64_t n_rows, int32_t num_sms, const qsa_geometry* forced, Geometry* g,
                   bool* fell_back, bool* stepped, bool fp8 = false) {
@@ -93,7 +93,7 @@ qsa_status select(int32_t Hq, int32_t Hkv, int32_t union_g, int32_t topk, int32_
   if (G > 1) {
     const int np_u = static_cast<int>(round_up(G * group, 16));
     const bool legal = G * group <= max_np &&
-                       qsa::smem_layout(np_u, qsa::kMinStages, 0).total <= qsa::kSmemLimit &&
+                       qsa::smem_layout(np_u, qsa::kMinStages, 0, fp8).total <= qsa::kSmemLimit &&
                        qsa::union_build_smem_bytes(topk, G) <= static_cast<size_t>(qsa::kUnionMaxSmem) &&
                        static_cast<int64_t>(G) * topk <= INT32_MAX / 2;
     if (!legal) {
@@ -116,7 +116,7 @@ qsa_status select(int32_t Hq, int32_t Hkv, int32_t union_g, int32_t topk, int32_
   int stages = 0;
   // even stage counts: a piece pair's two stages share one empty barrier
   for (int s = qsa::kMaxStages; s >= qsa::kMinStages; s -= 2) {
-    if (qsa::smem_layout(np, s, slot_cap).total <= qsa::kSmemLimit) {
+    if (qsa::smem_layout(np, s, slot_cap, fp8).total <= qsa::kSmemLimit) {
       stages = s;
       break;
     }
@@ -141,7 +141,7 @@ qsa_status select(int32_t Hq, int32_t Hkv, int32_t union_g, int32_t topk, int32_
   g->union_g = G;
   g->stages = stages;
   g->grid = static_cast<int>(grid);
-  g->smem_bytes = qsa::smem_layout(np, stages, slot_cap).total;
+  g->smem_bytes = qsa::smem_layout(np, stages, slot_cap, fp8).total;
   // S^T buffers (lookahead + 1) + two O^T halves
   g->tmem_cols = pow2_at_least((qsa::lookahead_for(G > 1) + 3) * np);
   g->slot_cap = slot_cap;
@@ -664,9 +664,13 @@ qsa_status qsa_sparse_prefill_ex(const void* q, const void* k_cache, const void*
              stream);
 }
 
-size_t qsa_workspace_bytes(int64_t n_rows, int32_t topk, int32_t union_g) {
+size_t qsa_union_workspace_bytes(int64_t n_rows, int32_t topk, int32_t union_g) {
   if (topk <= 0 || n_rows <= 0 || union_g <= 1 || union_g > 8) return 0;
   return ws_layout(n_rows, topk, union_g).total;
+}
+
+size_t qsa_workspace_bytes(int64_t n_rows, int32_t topk, int32_t union_g) {
+  return qsa_union_workspace_bytes(n_rows, topk, union_g);
 }
 
 qsa_status qsa_union_build(const int32_t* indices, const int32_t* topk_len, int64_t n_rows,

@@ -1,10 +1,10 @@
 // G-token union of selected slots with per-row ownership bits, one CTA per group.
 //
 // "DSA prefill ... triton_sparse_mla", Modifications: G adjacent query rows share one gathered
-// index set; each row's selection is sorted on its own, then every entry is searched
-// (lower_bound) in the other rows' sorted lists; a row emits a slot no earlier row of the group
-// selected and ORs in the bit of every row that did.  Accuracy Tests on the same page give the
-// contract: each slot once, bits = OR of owners, -1 dropped.
+// index set.  Each row's selection is sorted by itself and its entries are looked up (a
+// lower_bound search) in the other rows' sorted lists; a slot enters the group's list through
+// the first row holding it and carries one ownership bit per row that selected it.  Accuracy
+// Tests on the same page give the contract: listed once, bits = OR of owners, -1 dropped.
 //
 // Two kernels produce the same lists, bits and lengths:
 //  * union_bitmap_kernel (the hot path): slot numbers are small integers, so each row's valid
