@@ -186,7 +186,8 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
 __device__ __forceinline__ void cp_async_wait_0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 struct ItemInfo {   // written by the index warp, read by every role
-  int32_t n_valid, group, kvh, chunk, cols, row0, rows_in_group, pad;
+  int32_t n_valid, group, kvh, chunk, cols, row0, rows_in_group;
+  float v_scale_max;   // FP8 caches: largest |V page scale| over the item's slots
 };
 
 // One butterfly step of a warp reduce-scatter: lanes with bit `o` set keep the upper half of
@@ -271,7 +272,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                           2 * 4 * NP * sizeof(float));
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* const vote = reinterpret_cast<int*>(tmem_slot + 2);   // [3]
-  float* const vred = reinterpret_cast<float*>(tmem_slot + 8);   // [4] FP8: per-warp V-scale max
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -392,6 +392,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         nv = p.union_len[group];
       }
+      // FP8 caches: the largest |V page scale| of the item's slots, for the softmax's per-item
+      // normalisation; eight loads per lane in flight, one item ahead of the softmax.
+      float vmax = 0.f;
+      if (FP8) {
+        const int32_t* sl_b = reinterpret_cast<const int32_t*>(gbase + L.slots) + b * slot_cap;
+        const int32_t* ul_b =
+            UNION ? p.union_idx + static_cast<int64_t>(group) * p.union_g * p.topk : nullptr;
+        for (int t0 = 0; t0 < nv; t0 += 256) {
+          float sc[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int t = t0 + 32 * u + lane;
+            sc[u] = 0.f;
+            if (t < nv) {
+              const int64_t slot = UNION ? static_cast<int64_t>(ul_b[t])
+                                         : static_cast<int64_t>(sl_b[t]) / p.n_kvheads;
+              sc[u] = fabsf(__ldg(p.v_scale + (slot / p.page_size) * p.n_kvheads + kvh));
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) vmax = fmaxf(vmax, sc[u]);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
+      }
       if (lane == 0) {
         ItemInfo& I = info[b];
         I.n_valid = nv;
@@ -401,6 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         I.cols = cols;
         I.row0 = row0;
         I.rows_in_group = rows_in_group;
+        I.v_scale_max = vmax;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(b_itemfull + 8 * b);
@@ -768,21 +794,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int v_exp = 0;
       float v_norm = 1.f;
       if (FP8) {
-        float vmax = 0.f;
-        for (int j = 0; j < nt; ++j) {
-          const int token = j * kTileTokens + t;
-          if (token < nv) {
-            const int64_t slot = UNION ? static_cast<int64_t>(ul_b[token])
-                                       : static_cast<int64_t>(slots_b[token]) / p.n_kvheads;
-            vmax = fmaxf(vmax, fabsf(__ldg(p.v_scale + (slot / p.page_size) * p.n_kvheads + I.kvh)));
-          }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
-        if (lane == 0) vred[warp] = vmax;
-        named_bar_sync(1, 128);
-        vmax = fmaxf(fmaxf(vred[0], vred[1]), fmaxf(vred[2], vred[3]));
-        frexpf(vmax, &v_exp);            // vmax < 2^v_exp
+        frexpf(I.v_scale_max, &v_exp);   // (computed by the index warp) < 2^v_exp
         v_exp = max(-126, min(v_exp, 126));
         v_norm = ldexpf(1.f, -v_exp);
       }
