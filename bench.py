@@ -218,6 +218,172 @@ def max_over_ranks(values, device):
     return [float(x) for x in t.tolist()]
 
 
+def config_of(name, w, stats, union, paged, fp8, fp8_page_size, world):
+    """The workload description shared, key for key, by the GPU arm and the reference arm."""
+    return {"workload": DESCRIPTIONS.get(name, name), "name": name,
+            "rows": w.n_rows, "n_qheads": w.n_qheads, "n_kvheads": w.n_kvheads,
+            "head_dim": int(w.q.shape[2]), "topk": w.topk, "union_g": union,
+            "valid_slots": stats["valid_slots"],
+            "indices": ("logical positions + page table, translated in the kernels "
+                        "(qsa_sparse_prefill_paged)" if paged else "physical slots"),
+            "kv_cache": (f"e4m3 with fp32 scales per {fp8_page_size}-slot page and KV head, "
+                         "dequantised in the gather (qsa_sparse_prefill_fp8)" if fp8 else "bf16"),
+            "l2": "flushed before every timed GPU step (512 MiB memset outside the events)",
+            "parallelism": f"{world} independent shard(s), no collective"}
+
+
+class Prepared:
+    """One workload's inputs on the host (pinned) and the device, and the library call."""
+
+    def __init__(self, binding, W, name, *, fp8=False, paged=False, union=0, dev, seed_kw=None,
+                 fp8_page_size=64, stream):
+        import torch
+        w = W.make(name, **(seed_kw or {}))
+        if fp8:
+            if w.meta.get("mla") or paged:
+                raise SystemExit("--fp8 applies to the plain d=256 workloads")
+            w = W.with_fp8_cache(w, fp8_page_size)
+        self.w, self.name, self.fp8, self.paged, self.union = w, name, fp8, paged, union
+        self.mla = bool(w.meta.get("mla"))
+        if self.mla and paged:
+            raise SystemExit("--paged applies to the d=256 workloads")
+        if paged and "page_table" not in w.meta:
+            raise SystemExit(f"--paged needs a paged workload; {name} has no page table")
+        self.stats = workload_stats(w)
+        self.binding, self.stream = binding, stream
+
+        def bf(bits):
+            return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+        self.h_q = bf(w.q).pin_memory()
+        if self.mla:   # one latent cache [S, 576]; V is its first 512 dims, not a separate tensor
+            self.h_k = bf(w.k.reshape(w.k.shape[0], -1)).pin_memory()
+            self.h_v = self.h_k[:0]
+        elif fp8:   # e4m3 caches; their page scales travel with the metadata below
+            self.h_k = torch.from_numpy(w.meta["k8"]).pin_memory()
+            self.h_v = torch.from_numpy(w.meta["v8"]).pin_memory()
+        else:
+            self.h_k, self.h_v = bf(w.k).pin_memory(), bf(w.v).pin_memory()
+        self.h_idx = torch.from_numpy(w.meta["logical_indices"] if paged else w.indices).pin_memory()
+        self.h_tl = None if w.topk_len is None else torch.from_numpy(w.topk_len).pin_memory()
+        self.h_meta = ()
+        if fp8:
+            self.h_meta = tuple(torch.from_numpy(np.ascontiguousarray(w.meta[k], dtype=np.float32))
+                                .pin_memory() for k in ("k_scale", "v_scale"))
+        if paged:   # ragged row offsets, per-request KV lengths and the page table
+            self.h_meta = tuple(torch.from_numpy(np.ascontiguousarray(w.meta[k], dtype=np.int32))
+                                .pin_memory() for k in ("cu_seqlens_q", "kv_lens_array", "page_table"))
+        self.host_in = (self.h_q, self.h_k, self.h_v, self.h_idx, self.h_tl) + self.h_meta
+        self.dev_in = tuple(None if t is None else t.to(dev) for t in self.host_in)
+        q = self.dev_in[0]
+        self.out = (torch.empty((w.n_rows, w.n_qheads, w.meta["d_v"]), dtype=torch.bfloat16, device=dev)
+                    if self.mla else torch.empty_like(q))
+        self.lse = torch.empty((w.n_rows, w.n_qheads), dtype=torch.float32, device=dev)
+        self.ws = None
+        if union > 1 and not (self.mla or fp8 or paged):
+            nb = binding.union_workspace_bytes(w.n_rows, w.topk, union)
+            self.ws = torch.empty(max(nb, 256), dtype=torch.uint8, device=dev)
+        if self.mla:
+            self.geo = binding.select_mla_geometry(w.n_qheads, union, w.topk, w.n_rows)
+        else:
+            self.geo = binding.select_geometry(w.n_qheads, w.n_kvheads, union, w.topk, w.head_dim,
+                                               w.n_rows)
+
+    def call_on(self, dev_in, out, lse, ws):
+        b, w, u, st = self.binding, self.w, self.union, self.stream
+        q, k, v, idx, tl = dev_in[:5]
+        meta = dev_in[5:]
+        if self.mla:
+            b.sparse_mla_prefill(q, k, idx, tl, w.scale, out=out, lse=lse, union_g=u, stream=st)
+        elif self.fp8:
+            ks, vs = meta
+            b.sparse_prefill_fp8(q, k, v, ks, vs, w.meta["fp8_page_size"], idx, tl, w.scale, out=out,
+                                 lse=lse, union_g=u, stream=st)
+        elif self.paged:
+            cu, kvl, pt = meta
+            b.sparse_prefill_paged(q, k, v, idx, tl, cu, kvl, pt, w.meta["page_size"], w.scale,
+                                   n_pages=w.meta["n_pages"], out=out, lse=lse, union_g=u, stream=st)
+        else:
+            b.sparse_prefill(q, k, v, idx, tl, w.scale, out=out, lse=lse, union_g=u, workspace=ws,
+                             stream=st)
+
+    def call(self):
+        self.call_on(self.dev_in, self.out, self.lse, self.ws)
+
+    def issued_mma_flops(self):
+        """FLOPs the tensor cores execute, head padding included: every 128-slot tile of a work
+        item runs QK^T (K = d_qk) and P.V (d_v output dims) at N = the padded query columns.
+        Union tiles follow the union lists' lengths, read back from a union build."""
+        import torch
+        w, g = self.w, self.geo
+        np_, chunks = g["n_pad"], g["head_chunks"]
+        d_qk = int(w.q.shape[2])
+        d_v = w.meta["d_v"] if self.mla else d_qk
+        per_tile = 2 * 128 * np_ * (d_qk + d_v)
+        if g["union_g"] > 1:
+            phys = torch.from_numpy(np.ascontiguousarray(w.indices, dtype=np.int32)).to(self.out.device)
+            _, _, _, ulen = self.binding.union_build(phys, self.dev_in[4], g["union_g"],
+                                                     want_sorted=False)
+            tiles = int(((ulen.cpu().numpy().astype(np.int64) + 127) // 128).sum())
+        else:
+            tiles = int(((w.valid_counts().astype(np.int64) + 127) // 128).sum())
+        kv = 1 if self.mla else w.n_kvheads
+        return tiles * kv * chunks * per_tile
+
+
+def device_times(prep, steps, warmup, flush, stream):
+    """W untimed calls, then `steps` calls each bracketed by CUDA events on the launching stream,
+    with L2 flushed before each (outside the events) and ~0.5 ms of GPU spin after the flush so
+    the host has enqueued the call before the start event runs."""
+    import torch
+    for _ in range(warmup):
+        prep.call()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        torch.cuda._sleep(1 << 20)
+        starts[i].record(stream)
+        prep.call()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in zip(starts, ends)]
+
+
+def roofline_of(prep, ms, peaks, peak_src, ceiling, issued):
+    stats = prep.stats
+    kernel_s = ms / 1e3
+    t_tc = stats["flops"] / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = stats["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    bound = "tensor" if t_tc >= t_hbm else "hbm"
+    if bound == "tensor":
+        achieved, peak, unit = stats["flops"] / kernel_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    else:
+        achieved, peak, unit = stats["bytes"] / kernel_s / 1e9, peaks["hbm_gbs"], "GB/s"
+    r = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+         "peak_source": f"{peak_src} (MEASURED_PEAKS.json bf16 burst / hbm copy)",
+         "algorithmic_flops": stats["flops"], "algorithmic_bytes": stats["bytes"],
+         "roofline_us": max(t_tc, t_hbm) * 1e6,
+         "issued_mma_flops": issued, "issued_tflops": issued / kernel_s / 1e12,
+         "issued_frac": issued / kernel_s / 1e12 / peaks["bf16_tflops"],
+         "gathered_bytes": stats["gathered"], "kernel_ms": ms}
+    if ceiling and prep.union <= 1 and not prep.mla:
+        r["gather_gbs"] = stats["gathered"] / kernel_s / 1e9
+        r["gather_ceiling_gbs"] = ceiling
+        r["frac_of_gather_ceiling"] = r["gather_gbs"] / ceiling
+    return r
+
+
+# workloads measured beside the headline one, each device-timed in its own launch configuration
+SUB_CONFIGS = [
+    ("tiny", {}), ("group12_128k", {}), ("group12_128k_12q1kv", {}),
+    ("union_8k", {"union": 1}), ("union_8k", {"union": 2}), ("union_8k", {"union": 4}),
+    ("mixed_paged", {"paged": True}), ("mla_8k", {"union": 0}), ("mla_8k", {"union": 2}),
+    ("mla_8k", {"union": 4}), ("group6_32k", {"fp8": True}), ("union_8k", {"union": 4, "fp8": True}),
+]
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -229,90 +395,23 @@ def run_gpu(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     seed_kw = {} if world == 1 else {"seed": 1000 + rank}
-    w = W.make(args.config, **seed_kw)
-    if args.fp8:
-        if w.meta.get("mla") or args.paged:
-            raise SystemExit("--fp8 applies to the plain d=256 workloads")
-        w = W.with_fp8_cache(w, args.fp8_page_size)
-    stats = workload_stats(w)
 
-    # CPU baseline pool (spawned before any GPU work of this process matters; spawn is safe).
-    cpu = None
+    # CPU baseline pool (spawned, so safe whatever this process has done on the GPU).
     pool = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cores = os.cpu_count() or 1
         pool = oracle_pool(args.config, seed_kw, cores, args.fp8_page_size if args.fp8 else 0)
 
-    def bf(bits):
-        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
-
-    mla = bool(w.meta.get("mla"))
-    if mla and args.paged:
-        raise SystemExit("--paged applies to the d=256 workloads")
-    h_q = bf(w.q).pin_memory()
-    if mla:   # one latent cache [S, 576]; V is its first 512 dims, not a separate tensor
-        h_k = bf(w.k.reshape(w.k.shape[0], -1)).pin_memory()
-        h_v = h_k[:0]
-    elif args.fp8:   # e4m3 caches; their page scales travel with the metadata below
-        h_k = torch.from_numpy(w.meta["k8"]).pin_memory()
-        h_v = torch.from_numpy(w.meta["v8"]).pin_memory()
-    else:
-        h_k, h_v = bf(w.k).pin_memory(), bf(w.v).pin_memory()
-    paged = args.paged
-    if paged and "page_table" not in w.meta:
-        raise SystemExit(f"--paged needs a paged workload; {args.config} has no page table")
-    h_idx = torch.from_numpy(w.meta["logical_indices"] if paged else w.indices).pin_memory()
-    h_tl = None if w.topk_len is None else torch.from_numpy(w.topk_len).pin_memory()
-    # paged calls: ragged row offsets, per-request KV lengths and the page table
-    h_meta = ()
-    if args.fp8:
-        h_meta = tuple(torch.from_numpy(np.ascontiguousarray(w.meta[key], dtype=np.float32)).pin_memory()
-                       for key in ("k_scale", "v_scale"))
-    if paged:
-        h_meta = tuple(torch.from_numpy(np.ascontiguousarray(w.meta[key], dtype=np.int32)).pin_memory()
-                       for key in ("cu_seqlens_q", "kv_lens_array", "page_table"))
-    q, k, v = h_q.to(dev), h_k.to(dev), h_v.to(dev)
-    idx = h_idx.to(dev)
-    tl = None if h_tl is None else h_tl.to(dev)
-    d_meta = tuple(t.to(dev) for t in h_meta)
-    out = (torch.empty((w.n_rows, w.n_qheads, w.meta["d_v"]), dtype=torch.bfloat16, device=dev)
-           if mla else torch.empty_like(q))
-    lse = torch.empty((w.n_rows, w.n_qheads), dtype=torch.float32, device=dev)
-    ws = None
-    if args.union > 1:
-        nb = binding.workspace_bytes(w.n_rows, w.topk, args.union)
-        ws = torch.empty(max(nb, 256), dtype=torch.uint8, device=dev)
-    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
+    prep = Prepared(binding, W, args.config, fp8=args.fp8, paged=args.paged, union=args.union,
+                    dev=dev, seed_kw=seed_kw, fp8_page_size=args.fp8_page_size, stream=stream)
+    w, stats, mla = prep.w, prep.stats, prep.mla
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
-    def call_on(q, k, v, idx, tl, d_meta, out, lse, ws):
-        if mla:
-            binding.sparse_mla_prefill(q, k, idx, tl, w.scale, out=out, lse=lse, union_g=args.union,
-                                       stream=stream)
-        elif args.fp8:
-            ks, vs = d_meta
-            binding.sparse_prefill_fp8(q, k, v, ks, vs, w.meta["fp8_page_size"], idx, tl, w.scale,
-                                       out=out, lse=lse, union_g=args.union, stream=stream)
-        elif paged:
-            cu, kvl, pt = d_meta
-            binding.sparse_prefill_paged(q, k, v, idx, tl, cu, kvl, pt, w.meta["page_size"], w.scale,
-                                         n_pages=w.meta["n_pages"], out=out, lse=lse,
-                                         union_g=args.union, stream=stream)
-        else:
-            binding.sparse_prefill(q, k, v, idx, tl, w.scale, out=out, lse=lse, union_g=args.union,
-                                   workspace=ws, stream=stream)
-
-    def call():
-        call_on(q, k, v, idx, tl, d_meta, out, lse, ws)
-
-    if mla:
-        geo = binding.select_mla_geometry(w.n_qheads, args.union, w.topk, w.n_rows)
-    else:
-        geo = binding.select_geometry(w.n_qheads, w.n_kvheads, args.union, w.topk, w.head_dim,
-                                      w.n_rows)
     # gather ceiling on this workload's own K cache and selected rows (KV head 0), through a
     # view of the cache as 512-byte rows (for the 1152-byte MLA rows: the row holding each
     # selected slot's first bytes)
+    k = prep.dev_in[1]
     valid = w.indices[w.indices >= 0].astype(np.int64)
     valid = valid * w.n_kvheads if not mla else (valid * w.q.shape[2]) // 256
     if args.fp8:   # 256-byte e4m3 rows: the 512-byte probe row holding each slot's row
@@ -328,35 +427,25 @@ def run_gpu(args, rank, world, local_rank):
         binding.probe_gather_ceiling(k_rows, table, pieces_per_cta=200, engine=eng)
         ceilings[eng] = max(binding.probe_gather_ceiling(k_rows, table, engine=eng) for _ in range(3))
     ceiling_gbs = max(ceilings.values())
+
     for _ in range(args.warmup):
-        call()
+        prep.call()
     torch.cuda.synchronize()
     if binding.device_status(stream) != 0:
         raise RuntimeError("device wait timed out during warm-up")
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     c0 = binding.counters()["kernel_launches"]
     sampler = ClockSampler(local_rank) if rank == 0 else None
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
-    for i in range(args.steps):
-        flush.zero_()
-        # ~0.5 ms of GPU spin after the flush: the host enqueues the call meanwhile, so the
-        # events time the device work and not the host's launch path (that is in e2e)
-        torch.cuda._sleep(1 << 20)
-        starts[i].record(stream)
-        call()
-        ends[i].record(stream)
-    torch.cuda.synchronize()
+    times = device_times(prep, args.steps, 0, flush, stream)
     if world > 1:
         dist.barrier()
     wall = time.perf_counter() - t_wall
     clocks = sampler.stop() if sampler else None
     launches = binding.counters()["kernel_launches"] - c0
-    times = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms = sum(times) / len(times)
     if binding.device_status(stream) != 0:
         raise RuntimeError("device wait timed out during the timed region")
@@ -366,28 +455,46 @@ def run_gpu(args, rank, world, local_rank):
     for _ in range(100):
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a0.record(stream)
-        call()
+        prep.call()
         a1.record(stream)
         warm.append((a0, a1))
     torch.cuda.synchronize()
     warm_ms = statistics.median(x.elapsed_time(y) for x, y in warm)
 
     # end to end: pinned host inputs -> device, call, result -> host, every step
-    e_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    e_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    h2d_bytes = sum(t.numel() * t.element_size()
-                    for t in (h_q, h_k, h_v, h_idx) + ((h_tl,) if h_tl is not None else ()) + h_meta)
+    e_out = torch.empty(prep.out.shape, dtype=prep.out.dtype).pin_memory()
+    e_lse = torch.empty(prep.lse.shape, dtype=prep.lse.dtype).pin_memory()
+    h2d_bytes = sum(t.numel() * t.element_size() for t in prep.host_in if t is not None)
     d2h = e_out.numel() * e_out.element_size() + e_lse.numel() * e_lse.element_size()
 
-    # Two device input sets: the copies of step i+1 run on a copy stream while step i computes
-    # (every step still copies all of its inputs in and its O / LSE out inside the timed region).
-    host_in = (h_q, h_k, h_v, h_idx, h_tl) + h_meta
-    sets = [(q, k, v, idx, tl) + d_meta,
-            tuple(None if t is None else torch.empty_like(t) for t in (q, k, v, idx, tl) + d_meta)]
-    outs = [(out, lse), (torch.empty_like(out), torch.empty_like(lse))]
-    wss = [ws, None if ws is None else torch.empty_like(ws)]
+    # (1) serial: each step copies its inputs in, calls and copies O / LSE out on one stream,
+    # nothing overlapped (the per-call latency a caller sees)
+    def serial_step():
+        for d, h in zip(prep.dev_in, prep.host_in):
+            if d is not None:
+                d.copy_(h, non_blocking=True)
+        prep.call()
+        e_out.copy_(prep.out, non_blocking=True)
+        e_lse.copy_(prep.lse, non_blocking=True)
+
+    serial_step()
+    torch.cuda.synchronize()
+    s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s_ev.record(stream)
+    for _ in range(args.steps):
+        serial_step()
+    e_ev.record(stream)
+    torch.cuda.synchronize()
+    serial_ms = s_ev.elapsed_time(e_ev) / args.steps
+
+    # (2) pipelined: two device input sets; step i+1's input copies and step i-1's output
+    # copies run on their own streams while step i computes (every step still copies all of its
+    # inputs in and its O / LSE out inside the timed region)
+    sets = [prep.dev_in, tuple(None if t is None else torch.empty_like(t) for t in prep.dev_in)]
+    outs = [(prep.out, prep.lse), (torch.empty_like(prep.out), torch.empty_like(prep.lse))]
+    wss = [prep.ws, None if prep.ws is None else torch.empty_like(prep.ws)]
     copy_stream = torch.cuda.Stream(device=dev)
-    out_stream = torch.cuda.Stream(device=dev)     # device -> host copies of O and LSE
+    out_stream = torch.cuda.Stream(device=dev)
     copied = [torch.cuda.Event(), torch.cuda.Event()]
     done = [torch.cuda.Event(), torch.cuda.Event()]
     read = [torch.cuda.Event(), torch.cuda.Event()]
@@ -395,7 +502,7 @@ def run_gpu(args, rank, world, local_rank):
 
     def h2d(si):
         with torch.cuda.stream(copy_stream):
-            for d, h in zip(sets[si], host_in):
+            for d, h in zip(sets[si], prep.host_in):
                 if d is not None:
                     d.copy_(h, non_blocking=True)
             copied[si].record(copy_stream)
@@ -404,9 +511,8 @@ def run_gpu(args, rank, world, local_rank):
         stream.wait_event(copied[si])
         if read_used[si]:
             stream.wait_event(read[si])     # outs[si] is free once its copy-out has finished
-        qq, kk, vv, ii, tt = sets[si][:5]
         oo, ll = outs[si]
-        call_on(qq, kk, vv, ii, tt, sets[si][5:], oo, ll, wss[si])
+        prep.call_on(sets[si], oo, ll, wss[si])
         done[si].record(stream)
         out_stream.wait_event(done[si])
         with torch.cuda.stream(out_stream):
@@ -442,82 +548,61 @@ def run_gpu(args, rank, world, local_rank):
 
     # max over ranks
     if world > 1:
-        ms, e_ms = max_over_ranks([ms, e_ms], dev)
+        ms, e_ms, serial_ms = max_over_ranks([ms, e_ms, serial_ms], dev)
 
     if rank != 0:
         return None
 
+    cpu = None
     if pool is not None:
         cores = os.cpu_count() or 1
-        rps, done, dt = time_oracle(pool, w.n_rows, args.cpu_rows, cores)
+        rps, n_done, dt = time_oracle(pool, w.n_rows, args.cpu_rows, cores)
         pool.close()
         pool.join()
         cpu = {"value": rps, "unit": UNIT, "cores": cores, "kind": "oracle",
-               "sample": f"{done} of {w.n_rows} rows of the same workload (evenly spaced), "
+               "sample": f"{n_done} of {w.n_rows} rows of the same workload (evenly spaced), "
                          f"numpy float64 oracle in {cores} spawned single-threaded processes, "
                          f"{dt:.2f} s wall"}
 
     peaks, peak_src = load_peaks()
-    kernel_s = ms / 1e3
-    t_tc = stats["flops"] / (peaks["bf16_tflops"] * 1e12)
-    t_hbm = stats["bytes"] / (peaks["hbm_gbs"] * 1e9)
-    bound = "tensor" if t_tc >= t_hbm else "hbm"
-    if bound == "tensor":
-        achieved = stats["flops"] / kernel_s / 1e12
-        peak, unit = peaks["bf16_tflops"], "TFLOP/s"
-    else:
-        achieved = stats["bytes"] / kernel_s / 1e9
-        peak, unit = peaks["hbm_gbs"], "GB/s"
+    roofline = roofline_of(prep, ms, peaks, peak_src, ceiling_gbs, prep.issued_mma_flops())
+    roofline["gather_ceiling_gbs"] = ceiling_gbs
+    roofline["gather_ceiling_by_engine_gbs"] = ceilings
+    roofline["gather_ceiling_source"] = ("qsa_probe_gather_ceiling on this workload's K cache and "
+                                         "rows (the kernel's ring and engines, no compute; the "
+                                         "faster engine)")
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath):
         with open(tpath) as f:
             tj = json.load(f)
-        key = (f"{args.config}:union{args.union}" + (":paged" if paged else "")
+        key = (f"{args.config}:union{args.union}" + (":paged" if args.paged else "")
                + (":fp8" if args.fp8 else ""))
         ent = tj.get(key)
         if ent and ent.get("kernel_sha") == kernel_sha(mla):
             traffic = ent.get("dram_bytes_per_launch")
-    roofline = {
-        "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-        "frac": achieved / peak, "traffic": traffic,
-        "peak_source": f"{peak_src} (MEASURED_PEAKS.json bf16 burst / hbm copy)",
-        "algorithmic_flops": stats["flops"], "algorithmic_bytes": stats["bytes"],
-        "roofline_us": max(t_tc, t_hbm) * 1e6,
-        "gathered_bytes": stats["gathered"],
-        "gather_gbs": stats["gathered"] / kernel_s / 1e9,
-        "gather_ceiling_gbs": ceiling_gbs,
-        "frac_of_gather_ceiling": stats["gathered"] / kernel_s / 1e9 / ceiling_gbs,
-        "gather_ceiling_by_engine_gbs": ceilings,
-        "gather_ceiling_source": "qsa_probe_gather_ceiling on this workload's K cache and rows "
-                                 "(the kernel's ring and engines, no compute; the faster engine)",
-        "kernel_ms": ms,
-    }
+    roofline["traffic"] = traffic
     rows_total = w.n_rows * world
     line = {
-        "metric": METRIC, "value": rows_total / kernel_s, "unit": UNIT, "n_gpus": world,
+        "metric": METRIC, "value": rows_total / (ms / 1e3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16 MMA on e4m3 KV" if args.fp8 else "bf16",
         "data": "synthetic (seeded; no dataset or weights)",
-        "config": {"workload": DESCRIPTIONS.get(args.config, args.config), "name": args.config,
-                   "rows": w.n_rows, "n_qheads": w.n_qheads, "n_kvheads": w.n_kvheads,
-                   "head_dim": w.head_dim, "topk": w.topk, "union_g": args.union,
-                   "valid_slots": stats["valid_slots"], "geometry": geo,
-                   "indices": ("logical positions + page table, translated in the kernels "
-                               "(qsa_sparse_prefill_paged)" if paged else "physical slots"),
-                   "kv_cache": (f"e4m3 with fp32 scales per {args.fp8_page_size}-slot page and KV "
-                                "head, dequantised in the gather (qsa_sparse_prefill_fp8)"
-                                if args.fp8 else "bf16"),
-                   "l2": "flushed before every timed step (512 MiB memset outside the events)",
-                   "parallelism": f"{world} independent shard(s), no collective"},
+        "config": config_of(args.config, w, stats, args.union, args.paged, args.fp8,
+                            args.fp8_page_size, world),
+        "geometry": prep.geo,
         "roofline": roofline,
         "e2e": {"value": rows_total / (e_ms / 1e3), "unit": UNIT,
                 "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms,
                 "method": "public API per step: pinned-host inputs copied in, call, O and LSE "
                           "copied out; step i+1's input copies and step i-1's output copies "
                           "overlap step i on their own streams (two device buffer sets); no L2 "
-                          "flush between steps (each step's copies replace the inputs)"},
+                          "flush between steps (each step's copies replace the inputs)",
+                "serial_ms_per_step": serial_ms,
+                "serial_value": rows_total / (serial_ms / 1e3),
+                "serial_method": "the same copies and call with nothing overlapped: copy in, "
+                                 "call, copy out, one step after another on one stream"},
         "warm_l2": {"ms_per_step": warm_ms, "value": rows_total / (warm_ms / 1e3), "unit": UNIT,
                     "method": "median of 100 back-to-back calls on the same buffers (L2 warm), "
                               "the pages' timing regime; value above flushes L2 before each step"},
@@ -527,7 +612,46 @@ def run_gpu(args, rank, world, local_rank):
     }
     if cpu is not None:
         line["cpu_baseline"] = cpu
+    if world == 1 and not args.no_configs and args.config == "group6_32k" and not (
+            args.fp8 or args.paged or args.union):
+        del prep, sets, outs, wss
+        torch.cuda.empty_cache()
+        line["configs"] = run_sub_configs(binding, W, dev, stream, flush, peaks, peak_src,
+                                          ceiling_gbs, args)
     return line
+
+
+def run_sub_configs(binding, W, dev, stream, flush, peaks, peak_src, ceiling_gbs, args):
+    """Every other workload, device-timed in this run as the headline one is (L2 flushed before
+    each step); one record per workload and mode."""
+    import torch
+    recs = {}
+    steps = max(3, min(args.steps, 10))
+    for name, kw in SUB_CONFIGS:
+        prep = Prepared(binding, W, name, fp8=kw.get("fp8", False), paged=kw.get("paged", False),
+                        union=kw.get("union", 0), dev=dev, stream=stream)
+        key = (name + (f" G={prep.union}" if "union" in kw else "") + (" paged" if prep.paged else "")
+               + (" fp8" if prep.fp8 else ""))
+        c0 = binding.counters()["kernel_launches"]
+        sampler = ClockSampler(dev.index or 0)
+        times = device_times(prep, steps, 3, flush, stream)
+        clocks = sampler.stop()
+        launches = (binding.counters()["kernel_launches"] - c0) // (steps + 3)
+        if binding.device_status(stream) != 0:
+            raise RuntimeError(f"device wait timed out on {key}")
+        ms = sum(times) / len(times)
+        roof = roofline_of(prep, ms, peaks, peak_src, None if prep.fp8 else ceiling_gbs,
+                           prep.issued_mma_flops())
+        recs[key] = {"ms": ms, "value": prep.w.n_rows / (ms / 1e3), "unit": UNIT,
+                     "rows": prep.w.n_rows, "steps": steps,
+                     "dtype": "f16 MMA on e4m3 KV" if prep.fp8 else "bf16",
+                     "config": config_of(name, prep.w, prep.stats, prep.union, prep.paged, prep.fp8,
+                                         64, 1),
+                     "geometry": prep.geo, "roofline": roof, "clocks": clocks,
+                     "launches_per_call": launches}
+        del prep
+        torch.cuda.empty_cache()
+    return recs
 
 
 def run_reference(args, rank, world):
@@ -536,16 +660,18 @@ def run_reference(args, rank, world):
         return None
     from top_sparse_attention_row_gb300 import workloads as W
     w = W.make(args.config)
+    if args.fp8:
+        w = W.with_fp8_cache(w, args.fp8_page_size)
+    stats = workload_stats(w)
     cores = os.cpu_count() or 1
     pool = oracle_pool(args.config, {}, cores, args.fp8_page_size if args.fp8 else 0)
     sample = min(w.n_rows, args.cpu_rows)
     for _ in range(args.warmup):
         time_oracle(pool, w.n_rows, max(cores, sample // 8), cores)
-    vals, secs = [], []
+    vals = []
     for _ in range(args.steps):
-        rps, done, dt = time_oracle(pool, w.n_rows, sample, cores)
+        rps, _, _ = time_oracle(pool, w.n_rows, sample, cores)
         vals.append(rps)
-        secs.append(dt)
     pool.close()
     pool.join()
     value = statistics.median(vals)
@@ -555,9 +681,8 @@ def run_reference(args, rank, world):
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; no dataset or weights)",
         "impl": "reference",
-        "config": {"workload": DESCRIPTIONS.get(args.config, args.config), "name": args.config,
-                   "rows": w.n_rows, "n_qheads": w.n_qheads, "n_kvheads": w.n_kvheads,
-                   "head_dim": w.head_dim, "topk": w.topk, "union_g": args.union},
+        "config": config_of(args.config, w, stats, args.union, args.paged, args.fp8,
+                            args.fp8_page_size, world),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"{sample} of {w.n_rows} rows per step (evenly spaced), numpy "
                                    f"float64 oracle in {cores} spawned single-threaded processes"},
@@ -644,6 +769,8 @@ def main():
     ap.add_argument("--fp8-page-size", type=int, default=64)
     ap.add_argument("--cpu-rows", type=int, default=8192)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload records timed beside the default headline line")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
