@@ -354,6 +354,12 @@ qsa_status run(const void* q, const void* k_cache, const void* v_cache, const in
     p.k_scale = fp8->k_scale;
     p.v_scale = fp8->v_scale;
     p.page_size = fp8->page_size;
+    p.page_shift = -1;
+    p.kv_shift = -1;
+    for (int s = 0; s < 31; ++s) {
+      if ((int32_t{1} << s) == fp8->page_size) p.page_shift = s;
+      if ((int32_t{1} << s) == n_kvheads) p.kv_shift = s;
+    }
     p.gather_tma = 1;   // the FP8 gather is TMA only
   }
 

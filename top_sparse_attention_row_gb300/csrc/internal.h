@@ -81,6 +81,8 @@ struct PrefillParams {
   const float* k_scale;
   const float* v_scale;
   int32_t page_size;
+  int32_t page_shift;           // log2(page_size) when a power of two, else -1
+  int32_t kv_shift;             // log2(n_kvheads) when a power of two, else -1
   int32_t stall_first_item;     // failure-detection test: the index warp withholds its items
   // Union mode: items are handed out through this counter (zeroed by the union build) in
   // reverse order, longest groups first; nullptr = static round robin over the grid.

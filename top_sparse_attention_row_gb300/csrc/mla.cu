@@ -291,6 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t lseq = 0, rseq = 0, it = 0;
     uint32_t l_issued = 0, r_issued = 0;
     bool aborted = false;
+    RingPos lpos;   // ring position of the next latent piece (no division by the stage count)
     for (;; ++it) {
       const uint32_t b = it & 1, ph = (it >> 1) & 1;
       if (!__all_sync(0xffffffffu, mla_wait(b_itemfull + 8 * b, ph, abort_flag, status, kMItemFull))) {
@@ -329,14 +330,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         int y0 = 0, y1 = 0, y2 = 0, y3 = 0;
         for (int q = 0; q < kMlaPairs * nt; ++q) {
           const uint32_t s = lseq + q;
-          const uint32_t st = s % RP;
+          const uint32_t st = lpos.st, lpar = lpos.par;
+          ring_next(lpos, RP);
           const int tile = q / kMlaPairs, c = q % kMlaPairs;
           if (c == 0) {
             y0 = n0; y1 = n1; y2 = n2; y3 = n3;
             if (tile + 1 < nt) rows_of(tile + 1, n0, n1, n2, n3);
           }
-          if (!__all_sync(0xffffffffu, mla_wait(b_lempty + 8 * st, ((s / RP) & 1) ^ 1, abort_flag,
-                                                status, kMLatEmpty))) {
+          if (!__all_sync(0xffffffffu, mla_wait(b_lempty + 8 * st, lpar ^ 1, abort_flag, status,
+                                                kMLatEmpty))) {
             aborted = true;
             break;
           }
@@ -384,11 +386,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer (one thread)
     constexpr uint32_t kIdescQK = idesc_bf16_f32(128, NP, false, false);
     constexpr uint32_t kIdescPV = idesc_bf16_f32(128, NP, true, false);
-    uint32_t lseq = 0, rseq = 0, js = 0, it = 0;
+    uint32_t rseq = 0, js = 0, it = 0;
     bool aborted = false;
     const uint32_t qaddr = base + L.qbuf;
     const uint32_t rope_addr = base + L.rope;
-    auto lstage = [&](uint32_t s) { return base + L.pairs + (s % RP) * kStageBytes; };
+    // Latent pieces are read twice, each time in ring order: by QK^T (qk_pos) and, a tile
+    // later, by P.V (pv_pos); running positions replace divisions by the stage count on the
+    // issue path.
+    RingPos qk_pos, pv_pos;
+    auto lstage = [&](uint32_t st) { return base + L.pairs + st * kStageBytes; };
     // S^T(sbuf) += latent chunk c (dims 128c .. 128c+127) of the tile held in `st_addr`
     auto qk_chunk = [&](uint32_t sb, int c, uint32_t st_addr, bool first) {
 #pragma unroll
@@ -443,11 +449,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sb = js & 1, sph = (js >> 1) & 1;
         bool ok = mla_wait(b_sfree + 8 * sb, sph ^ 1, abort_flag, status, kMSFree);
         for (int c = 0; c < kMlaPairs && ok; ++c) {
-          const uint32_t s = lseq + c;
-          ok = mla_wait(b_lfull + 8 * (s % RP), (s / RP) & 1, abort_flag, status, kMLatFull);
+          const RingPos at = qk_pos;
+          ring_next(qk_pos, RP);
+          ok = mla_wait(b_lfull + 8 * at.st, at.par, abort_flag, status, kMLatFull);
           if (ok) {
             tc_fence_after();
-            if (lane == 0) qk_chunk(sb, c, lstage(s), c == 0);
+            if (lane == 0) qk_chunk(sb, c, lstage(at.st), c == 0);
           }
         }
         ok = ok && mla_wait(b_rfull, rseq & 1, abort_flag, status, kMRopeFull);
@@ -472,11 +479,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (jj < nt) {
           ok = mla_wait(b_sfree + 8 * sbn, sphn ^ 1, abort_flag, status, kMSFree);
           for (int c = 0; c < E && ok; ++c) {
-            const uint32_t s = lseq + kMlaPairs * jj + c;
-            ok = mla_wait(b_lfull + 8 * (s % RP), (s / RP) & 1, abort_flag, status, kMLatFull);
+            const RingPos at = qk_pos;
+            ring_next(qk_pos, RP);
+            ok = mla_wait(b_lfull + 8 * at.st, at.par, abort_flag, status, kMLatFull);
             if (ok) {
               tc_fence_after();
-              if (lane == 0) qk_chunk(sbn, c, lstage(s), c == 0);
+              if (lane == 0) qk_chunk(sbn, c, lstage(at.st), c == 0);
             }
           }
           ok = ok && mla_wait(b_rfull, (rseq + jj) & 1, abort_flag, status, kMRopeFull);
@@ -496,12 +504,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
+        const RingPos pv_at = pv_pos;   // every lane keeps the position; lane 0 issues
+        for (int c = 0; c < kMlaPairs; ++c) ring_next(pv_pos, RP);
         if (lane == 0) {
           const uint32_t pbase = base + L.pbuf + pb * L.p_bytes;
+          RingPos at = pv_at;
           for (int c = 0; c < kMlaPairs; ++c) {
-            const uint32_t s = lseq + kMlaPairs * j + c;
-            pv_chunk(c, lstage(s), pbase, j == 0);
-            tc_commit(b_lempty + 8 * (s % RP));
+            pv_chunk(c, lstage(at.st), pbase, j == 0);
+            tc_commit(b_lempty + 8 * at.st);
+            ring_next(at, RP);
           }
           tc_commit(b_pvdone + 8 * pb);
         }
@@ -509,11 +520,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- rest of S(j+1)
         if (jj < nt) {
           for (int c = E; c < kMlaPairs && ok; ++c) {
-            const uint32_t s = lseq + kMlaPairs * jj + c;
-            ok = mla_wait(b_lfull + 8 * (s % RP), (s / RP) & 1, abort_flag, status, kMLatFull);
+            const RingPos at = qk_pos;
+            ring_next(qk_pos, RP);
+            ok = mla_wait(b_lfull + 8 * at.st, at.par, abort_flag, status, kMLatFull);
             if (ok) {
               tc_fence_after();
-              if (lane == 0) qk_chunk(sbn, c, lstage(s), false);
+              if (lane == 0) qk_chunk(sbn, c, lstage(at.st), false);
             }
           }
           if (!__all_sync(0xffffffffu, ok)) {
@@ -528,7 +540,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (aborted) break;
-      lseq += kMlaPairs * nt;
       rseq += nt;
       js += nt;
     }

@@ -198,6 +198,18 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
   return r;
 }
 
+// Position in a ring of n stages, advanced one piece at a time: the stage and the parity of its
+// current fill, kept without dividing a running piece count by a runtime stage count.
+struct RingPos {
+  uint32_t st = 0, par = 0;
+};
+__device__ __forceinline__ void ring_next(RingPos& r, uint32_t n) {
+  if (++r.st == n) {
+    r.st = 0;
+    r.par ^= 1;
+  }
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
