@@ -216,7 +216,7 @@ void mla_to_public(const qsa::MlaGeometry& g, qsa_geometry* out) {
   out->head_chunks = g.head_chunks;
   out->union_g = g.union_g;
   out->grid = g.grid;
-  out->threads = qsa::kThreads;
+  out->threads = qsa::kMlaThreads;
   out->smem_bytes = g.smem_bytes;
   out->tmem_cols = g.tmem_cols;
   out->n_items = g.n_items;

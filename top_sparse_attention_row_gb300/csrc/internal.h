@@ -20,8 +20,26 @@ constexpr int kSoftmaxWarps = 4;             // warps 0-3: softmax + epilogue (T
 constexpr int kMmaWarp = 4;                  // MMA issue + tensor-memory owner
 constexpr int kIndexWarp = 5;                // slot compaction, Q tile, item info
 constexpr int kProducerWarp0 = 6;            // first gather warp
-constexpr int kProducerWarps = 6;            // gather warps, each owning one ring stage
-constexpr int kThreads = 32 * (kProducerWarp0 + kProducerWarps);
+// d=256 kernel: each 32 KiB stage is filled by two gather warps, one per 64-dim block (a warp
+// issues TMA gathers one after another at ~13 GB/s, so two warps land a stage in half the time).
+// 20 warps = five warpgroups: softmax (0-3); MMA and index warps and two idle ones (4-7); twelve
+// gather warps (8-19), whose spare registers go to the softmax warpgroup (setmaxnreg).
+constexpr int kBlocksPerStage = 2;
+constexpr int kMaxStages = 6;
+constexpr int kGatherWarp0 = 8;
+constexpr int kProducerWarps = kBlocksPerStage * kMaxStages;
+constexpr int kThreads = 640;
+constexpr int kLaunchRegs = 96;              // 65536 / 640, rounded down to a multiple of 8
+constexpr int kSoftmaxRegs = 176;            // after setmaxnreg.inc (warpgroup 0)
+constexpr int kRoleRegs = 112;               // after setmaxnreg.inc (warpgroup 1: MMA, index)
+constexpr int kGatherRegs = 64;              // after setmaxnreg.dec (warpgroups 2-4)
+static_assert(kGatherWarp0 + kProducerWarps == kThreads / 32 && kGatherWarp0 % 4 == 0,
+              "gather warps fill whole warpgroups at the end of the CTA");
+static_assert(128 * kSoftmaxRegs + 128 * kRoleRegs + 384 * kGatherRegs <= kThreads * kLaunchRegs,
+              "register split within the launch's registers");
+// MLA kernel: six gather warps (five share the latent pieces, one the rope pieces), 384 threads.
+constexpr int kMlaProducerWarps = 6;
+constexpr int kMlaThreads = 32 * (kProducerWarp0 + kMlaProducerWarps);
 constexpr int kMinStages = 4;                // ring must hold V(j) and K(j+1) together
 // MMA issue lookahead of the d=256 kernel: QK^T(j+L) is issued before P.V(j), with L + 1 S^T
 // buffers.  Measured on GB300: per-token tiles (N = 16) run fastest at L = 1 (L = 2 or 3 cost
@@ -32,7 +50,6 @@ __host__ __device__ constexpr int lookahead_for(bool union_mode) { return union_
 // barrier (each commit costs ~45 ns of issue; measured 0.5 % faster per-token).  The stage
 // count is therefore even.
 constexpr int kMaxSBufs = 3;
-constexpr int kMaxStages = 8;
 constexpr int kSmemLimit = 232448;           // 227 KiB opt-in dynamic shared memory
 constexpr int kUnionMaxSmem = 200 * 1024;    // union-build kernel shared-memory cap
 

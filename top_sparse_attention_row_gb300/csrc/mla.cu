@@ -110,7 +110,7 @@ struct MlaItem {   // written by the index warp, read by every role
 }  // namespace
 
 template <int NP, bool UNION>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kMlaThreads, 1)
     sparse_mla_kernel(const __grid_constant__ CUtensorMap tmKV, const __grid_constant__ MlaParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(b_pfull + 8 * b, 128);
       mbar_init(b_pvdone + 8 * b, 1);
       mbar_init(b_itemfull + 8 * b, 1);
-      mbar_init(b_itemempty + 8 * b, 1 + 128 + kProducerWarps);
+      mbar_init(b_itemempty + 8 * b, 1 + 128 + kMlaProducerWarps);
     }
     mbar_init(b_qempty, 1);
     mbar_init(b_qfull, 1);
@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(b_qfull);
     }
-  } else if (warp >= kProducerWarp0 && warp < kProducerWarp0 + kProducerWarps) {
+  } else if (warp >= kProducerWarp0 && warp < kProducerWarp0 + kMlaProducerWarps) {
     // ------------------------------------------------------------ gather producers
     // Warps 0-4 share every latent piece: gather4 op o = 32a + lane (o < 64; atom a, slots
     // 4*lane .. 4*lane+3) is issued by warp o % 5, and each warp arms the stage's barrier with
@@ -781,7 +781,7 @@ cudaError_t launch_mla_np(const CUtensorMap& tm, const MlaParams& p, const MlaGe
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) opted_in[dev].store(g.smem_bytes);
   }
-  kern<<<g.grid, kThreads, g.smem_bytes, stream>>>(tm, p);
+  kern<<<g.grid, kMlaThreads, g.smem_bytes, stream>>>(tm, p);
   return cudaGetLastError();
 }
 

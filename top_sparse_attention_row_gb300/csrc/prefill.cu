@@ -74,7 +74,7 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 
-__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+__device__ __forceinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                        int32_t site, unsigned long long limit) {
   const unsigned long long t0 = global_ns();
   while (true) {
@@ -89,8 +89,9 @@ __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile i
 }
 
 // Bounded wait that ignores the abort flag: after an abort, lets copies and MMAs already issued
-// complete before shared or tensor memory is given up.
-__device__ __noinline__ bool drain_bar(uint32_t bar, uint32_t parity, unsigned long long limit) {
+// complete before shared or tensor memory is given up.  (The wait helpers are inlined: a called
+// function would have to fit the register budgets of every warpgroup after the reallocation.)
+__device__ __forceinline__ bool drain_bar(uint32_t bar, uint32_t parity, unsigned long long limit) {
   const unsigned long long t0 = global_ns();
   while (!mbar_try_wait(bar, parity)) {
     if (global_ns() - t0 > limit) {
@@ -251,6 +252,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* const gbase = smem_raw + (base - raw_u32);
 
   constexpr int kLookahead = lookahead_for(UNION);
+  // Gather warps per stage: two (one per 64-dim block) for bf16 caches; one for FP8 caches,
+  // whose stage rewrite from e4m3 to fp16 is done by one warp.
+  constexpr int kBPS = FP8 ? 1 : kBlocksPerStage;
   constexpr int kSBufs = kLookahead + 1;
   const int slot_cap = UNION ? 0 : p.slot_cap;
   const SmemLayout L = smem_layout(NP, p.stages, slot_cap, FP8);
@@ -282,8 +286,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < R; ++s) {
-      // owner warp: expect_tx (TMA), one arrival after converting (FP8), or 32 lane arrivals
-      mbar_init(b_full + 8 * s, (p.gather_tma || FP8) ? 1 : 32);
+      // TMA: one expect_tx per gather warp of the stage; FP8: one arrival after converting (the
+      // stage's first warp does the whole piece); cp.async: every lane of both warps
+      mbar_init(b_full + 8 * s, FP8 ? 1 : p.gather_tma ? kBPS : 32 * kBPS);
       mbar_init(b_empty + 8 * s, 1);   // stage pairs share empty[pair]: [0, R/2) are used
       if (FP8) mbar_init(b_land + 8 * s, 1);
     }
@@ -310,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), static_cast<uint32_t>(p.tmem_cols));
     tmem_relinquish();
   }
-  if (warp == kProducerWarp0 && lane == 0 && p.gather_tma) {
+  if (warp == kGatherWarp0 && lane == 0 && p.gather_tma) {
     prefetch_tmap(&tmK);
     prefetch_tmap(&tmV);
   }
@@ -323,9 +328,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int64_t n_items = p.n_items;
   const int64_t stride = gridDim.x;
+  // Every role ends here and returns, so no code is shared by warpgroups that run with
+  // different register counts after the reallocation below.
+  auto finish_role = [&]() {
+    tc_fence_before();
+    __syncthreads();
+  };
 
   if (warp == kIndexWarp) {
     // ------------------------------------------------------------ index / Q loader
+    regs_inc<kRoleRegs>();
     // Items: a static round robin over the grid, or (union mode) taken from a global counter in
     // reverse order -- the later row groups of a prefill have the longest union lists, so the
     // long items go first and the short ones even out the CTAs' finishing times.  After the
@@ -450,23 +462,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(b_qfull);
     }
-  } else if (warp >= kProducerWarp0 && warp < kProducerWarp0 + kProducerWarps) {
+    finish_role();
+    return;
+  } else if (warp >= kGatherWarp0) {
     // ------------------------------------------------------------ gather producers
-    // Producer warp w owns the ring stages st with st % W == w and gathers every piece that
-    // lands on them, whole (64 cp.async of 2 slots x 16 chunks, or 64 TMA gather4), in order.
-    // One owner per stage: no two warps ever wait on different phases of one stage, and a
-    // warp issues a whole 32 KiB piece back to back.  Measured alternatives were slower: six
-    // warps sharing every piece (1.3x the time), and two warps per piece with three, five or
-    // six warp pairs (3-8 % slower: more warps spinning on stage barriers, fewer registers).
-    const int pw = warp - kProducerWarp0;
-    constexpr int W = kProducerWarps;
+    // Warpgroups 2-4 run only this role: they give registers back to the CTA's pool for the
+    // softmax warpgroup (warpgroup register reallocation).
+    regs_dec<kGatherRegs>();
+    // Stage st is filled by warps 2 st and 2 st + 1, each gathering one 64-dim block of every
+    // piece that lands on it (32 TMA gather4, one per lane, or 32 cp.async of four slots x 16
+    // bytes per lane), in order.  Every piece's two halves are issued at once by two warps, and
+    // no warp ever waits on a stage it does not fill.  (With one owner warp per stage a piece
+    // took ~2.3 us to issue, and a V tile's pieces -- which reuse the stages of the same tile's
+    // K, freed only when its QK^T completes -- were the wait of every P.V.)  FP8 pieces are
+    // gathered and rewritten whole by the stage's first warp.
+    const int pw = warp - kGatherWarp0;
+    const uint32_t st = static_cast<uint32_t>(pw / kBPS);   // this warp's stage
+    const int blk = pw % kBPS;                              // and first 64-dim block
     const bool tma = p.gather_tma != 0;
-    uint32_t seq = 0, it = 0, issued = 0;
+    const bool active = static_cast<int>(st) < R;
+    uint32_t seq = 0, it = 0, uses = 0;   // uses: fills of stage st so far
+    int32_t last_issued = -1;             // the newest fill this warp issued copies for
     bool aborted = false;
-    // Stages pw and pw + W (when < R) and how often each has been filled: the barrier parities
-    // follow from these counts, with no division on the way to each piece.
-    const uint32_t st_a = static_cast<uint32_t>(pw), st_b = static_cast<uint32_t>(pw + W);
-    uint32_t uses_a = 0, uses_b = 0;
     for (;; ++it) {
       const uint32_t b = it & 1, ph = (it >> 1) & 1;
       if (!__all_sync(0xffffffffu, wait_bar(b_itemfull + 8 * b, ph, abort_flag, kSiteItemFull))) {
@@ -481,25 +498,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int32_t* ul =
           UNION ? p.union_idx + static_cast<int64_t>(I.group) * p.union_g * p.topk : nullptr;
       const int n_pieces = 4 * nt;
-      // This warp's pieces are those on its stages pw and pw + W: two arithmetic progressions
-      // of step R, merged in order.  Stepping straight to them, rather than testing every
-      // piece of the item, measured 1-2 % faster on GB300 (group6_32k 2.237 -> 2.205 ms).
+      // This warp's pieces are those on stage st: q = q_first + k R.
       const int sq = static_cast<int>(seq % static_cast<uint32_t>(R));
-      int qa = pw < R ? (pw - sq + R) % R : n_pieces;
-      int qb = pw + W < R ? (pw + W - sq + R) % R : n_pieces;
-      auto next_piece = [&](bool& on_b) {
-        int q;
-        if (qa <= qb) {
-          q = qa;
-          qa += R;
-          on_b = false;
-        } else {
-          q = qb;
-          qb += R;
-          on_b = true;
-        }
-        return q;
-      };
+      const int q_first = active ? (static_cast<int>(st) - sq + R) % R : n_pieces;
       // tensor-map row of union slot t; a slot whose row would pass the map (or int32) becomes
       // padding, as in the per-token compaction
       auto union_row = [&](int t) -> int32_t {
@@ -514,49 +515,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = tile * kTileTokens + 4 * lane;
         return make_int4(union_row(t), union_row(t + 1), union_row(t + 2), union_row(t + 3));
       };
-      bool b0 = false, bn = false;
-      const int q0 = next_piece(b0);
       // The union slots of the warp's next piece are loaded one piece ahead, so their latency
       // overlaps the wait for the current piece's stage and its issue.
       int4 uy_next = make_int4(0, 0, 0, 0);
-      if (UNION && q0 < n_pieces) uy_next = union_rows(q0);
-      for (int q = q0, qn = 0; q < n_pieces; q = qn, b0 = bn) {
-        qn = next_piece(bn);
+      if (UNION && q_first < n_pieces) uy_next = union_rows(q_first);
+      for (int q = q_first; q < n_pieces; q += R) {
         const int4 uy = uy_next;
-        if (UNION && qn < n_pieces) uy_next = union_rows(qn);
-        const uint32_t s = seq + q;
-        const uint32_t st = b0 ? st_b : st_a;
-        const uint32_t use = b0 ? uses_b++ : uses_a++;   // this fill's index on its stage
+        if (UNION && q + R < n_pieces) uy_next = union_rows(q + R);
+        const uint32_t use = uses++;
         int tile, is_v, half;
         piece_of<kLookahead>(q, nt, tile, is_v, half);
         const int t0 = tile * kTileTokens;
-        const uint32_t par = (use & 1) ^ 1;
         const uint32_t empty_bar = b_empty + 8 * (st >> 1);   // the stage pair's barrier
-        if (!__all_sync(0xffffffffu, wait_bar(empty_bar, par, abort_flag, kSiteStageEmpty))) {
+        if (!__all_sync(0xffffffffu, wait_bar(empty_bar, (use & 1) ^ 1, abort_flag, kSiteStageEmpty))) {
           aborted = true;
           break;
         }
         const uint32_t stage = base + L.ring + st * kStageBytes;
+        int y0, y1, y2, y3;   // tensor-map rows of slots 4 lane .. 4 lane + 3 of the tile
+        if (UNION) {
+          y0 = uy.x; y1 = uy.y; y2 = uy.z; y3 = uy.w;
+        } else {
+          const int t = t0 + 4 * lane;
+          const int4 v = *reinterpret_cast<const int4*>(sl + t);
+          y0 = t + 0 < nv ? v.x : p.pad_row;
+          y1 = t + 1 < nv ? v.y : p.pad_row;
+          y2 = t + 2 < nv ? v.z : p.pad_row;
+          y3 = t + 3 < nv ? v.w : p.pad_row;
+        }
+        const CUtensorMap* tm = is_v ? &tmV : &tmK;
         if (FP8) {
           // e4m3 half-rows (128 B) land in the stage's upper 16 KiB, then the warp rewrites the
-          // stage in place as the f16 tile: each lane takes whole rows (lane + 32k), reading a
-          // row's 128 bytes before writing its 256, so no row overwrites unread input.
-          int y0, y1, y2, y3;
-          if (UNION) {
-            y0 = uy.x; y1 = uy.y; y2 = uy.z; y3 = uy.w;
-          } else {
-            const int t = t0 + 4 * lane;
-            const int4 v = *reinterpret_cast<const int4*>(sl + t);
-            y0 = t + 0 < nv ? v.x : p.pad_row;
-            y1 = t + 1 < nv ? v.y : p.pad_row;
-            y2 = t + 2 < nv ? v.z : p.pad_row;
-            y3 = t + 3 < nv ? v.w : p.pad_row;
-          }
+          // stage in place as the f16 tile: each lane takes whole rows (lane + 32k).  A row's
+          // upper fp16 block overwrites its own e4m3 bytes, so dims 0-63 (lower block, no
+          // overlap) are written from the first four input chunks before the last four are read.
           if (lane == 0) mbar_arrive_expect_tx(b_land + 8 * st, kStageBytes / 2);
           __syncwarp();
-          tma_gather4(stage + 16384 + lane * 512, is_v ? &tmV : &tmK, half * 128, y0, y1, y2, y3,
-                      b_land + 8 * st);
-          issued = s + 1;
+          tma_gather4(stage + 16384 + lane * 512, tm, half * 128, y0, y1, y2, y3, b_land + 8 * st);
+          last_issued = static_cast<int32_t>(use);
           if (!__all_sync(0xffffffffu, wait_bar(b_land + 8 * st, use & 1, abort_flag, kSiteLanded))) {
             aborted = true;
             break;
@@ -565,20 +561,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 4; ++k) {
             const int t = lane + 32 * k;
             const uint32_t sw = static_cast<uint32_t>(t & 7);
-            uint4 in[8];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) in[c] = lds_v4(stage + 16384 + t * 128 + ((c ^ sw) << 4));
+            for (int hb = 0; hb < 2; ++hb) {
+              uint4 in[4];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              // dims 16c .. 16c+15 of the half -> atom c / 4, 16-byte chunks 2(c % 4), 2(c % 4) + 1
-              const uint4 lo = make_uint4(e4m3x2_to_f16x2(in[c].x & 0xffffu), e4m3x2_to_f16x2(in[c].x >> 16),
-                                          e4m3x2_to_f16x2(in[c].y & 0xffffu), e4m3x2_to_f16x2(in[c].y >> 16));
-              const uint4 hi = make_uint4(e4m3x2_to_f16x2(in[c].z & 0xffffu), e4m3x2_to_f16x2(in[c].z >> 16),
-                                          e4m3x2_to_f16x2(in[c].w & 0xffffu), e4m3x2_to_f16x2(in[c].w >> 16));
-              const uint32_t row = stage + (c >> 2) * 16384 + t * 128;
-              const uint32_t j0 = static_cast<uint32_t>((c & 3) * 2);
-              sts_v4(row + ((j0 ^ sw) << 4), lo);
-              sts_v4(row + (((j0 + 1) ^ sw) << 4), hi);
+              for (int c = 0; c < 4; ++c)
+                in[c] = lds_v4(stage + 16384 + t * 128 + (((4 * hb + c) ^ sw) << 4));
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                // dims 16(4 hb + c) .. +15 -> atom hb, 16-byte chunks 2c, 2c + 1
+                const uint4 lo = make_uint4(e4m3x2_to_f16x2(in[c].x & 0xffffu), e4m3x2_to_f16x2(in[c].x >> 16),
+                                            e4m3x2_to_f16x2(in[c].y & 0xffffu), e4m3x2_to_f16x2(in[c].y >> 16));
+                const uint4 hi = make_uint4(e4m3x2_to_f16x2(in[c].z & 0xffffu), e4m3x2_to_f16x2(in[c].z >> 16),
+                                            e4m3x2_to_f16x2(in[c].w & 0xffffu), e4m3x2_to_f16x2(in[c].w >> 16));
+                const uint32_t row = stage + hb * 16384 + t * 128;
+                const uint32_t j0 = static_cast<uint32_t>(2 * c);
+                sts_v4(row + ((j0 ^ sw) << 4), lo);
+                sts_v4(row + (((j0 + 1) ^ sw) << 4), hi);
+              }
             }
           }
           fence_proxy_async_smem();   // generic writes -> tensor-core (async proxy) reads
@@ -587,50 +587,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           continue;
         }
         if (tma) {
-          // gather4 op (lane, c): slots 4*lane .. 4*lane+3, dims half*128 + 64c .. +63
-          int y0, y1, y2, y3;
-          if (UNION) {
-            y0 = uy.x; y1 = uy.y; y2 = uy.z; y3 = uy.w;
-          } else {
-            const int t = t0 + 4 * lane;
-            const int4 v = *reinterpret_cast<const int4*>(sl + t);
-            y0 = t + 0 < nv ? v.x : p.pad_row;
-            y1 = t + 1 < nv ? v.y : p.pad_row;
-            y2 = t + 2 < nv ? v.z : p.pad_row;
-            y3 = t + 3 < nv ? v.w : p.pad_row;
-          }
-          if (lane == 0) mbar_arrive_expect_tx(b_full + 8 * st, kStageBytes);
+          // per lane and block: slots 4 lane .. 4 lane + 3, dims half * 128 + 64 c .. +63
+          if (lane == 0) mbar_arrive_expect_tx(b_full + 8 * st, kStageBytes / kBPS);
           __syncwarp();
-          const CUtensorMap* tm = is_v ? &tmV : &tmK;
 #pragma unroll
-          for (int c = 0; c < 2; ++c)
+          for (int c = blk; c < kBlocksPerStage; c += kBPS)
             tma_gather4(stage + c * 16384 + lane * 512, tm, half * 128 + c * 64, y0, y1, y2, y3,
                         b_full + 8 * st);
         } else {
-          const uint8_t* cache = (is_v ? p.v_bytes : p.k_bytes) + half * 256;
-          const int ch = lane & 15;
+          // 16-byte copies: eight lanes per slot row of 128 bytes, four slots per instruction
+          const int ch = lane & 7;
+#pragma unroll 1
+          for (int c = blk; c < kBlocksPerStage; c += kBPS) {
+            const uint8_t* cache = (is_v ? p.v_bytes : p.k_bytes) + half * 256 + c * 128;
 #pragma unroll 8
-          for (int i = 0; i < 64; ++i) {
-            const int t = 2 * i + (lane >> 4);          // slot within the tile
-            int32_t y;
-            if (UNION) {
-              const int src = t >> 2, el = t & 3;
-              const int a0 = __shfl_sync(0xffffffffu, uy.x, src), a1 = __shfl_sync(0xffffffffu, uy.y, src);
-              const int a2 = __shfl_sync(0xffffffffu, uy.z, src), a3 = __shfl_sync(0xffffffffu, uy.w, src);
-              y = el == 0 ? a0 : el == 1 ? a1 : el == 2 ? a2 : a3;
-            } else {
-              y = t0 + t < nv ? sl[t0 + t] : p.pad_row;
+            for (int i = 0; i < 32; ++i) {
+              const int t = 4 * i + (lane >> 3);          // slot within the tile
+              const int src_lane = t >> 2, el = t & 3;
+              const int a0 = __shfl_sync(0xffffffffu, y0, src_lane), a1 = __shfl_sync(0xffffffffu, y1, src_lane);
+              const int a2 = __shfl_sync(0xffffffffu, y2, src_lane), a3 = __shfl_sync(0xffffffffu, y3, src_lane);
+              const int32_t y = el == 0 ? a0 : el == 1 ? a1 : el == 2 ? a2 : a3;
+              const bool pad = y == p.pad_row;
+              const uint8_t* src = cache + (pad ? 0 : static_cast<int64_t>(y) * (kHeadDim * 2)) + ch * 16;
+              const uint32_t dst = stage + c * 16384 + t * 128 + ((ch ^ (t & 7)) << 4);
+              cp_async_16_zfill(dst, src, pad ? 0u : 16u);
             }
-            const bool pad = y == p.pad_row;
-            const uint8_t* src = cache + (pad ? 0 : static_cast<int64_t>(y) * (kHeadDim * 2)) + ch * 16;
-            const uint32_t dst = stage + (ch >> 3) * 16384 + t * 128 + (((ch & 7) ^ (t & 7)) << 4);
-            cp_async_16_zfill(dst, src, pad ? 0u : 16u);
           }
           // Each lane's arrival fires once all its earlier copies have landed; the MMA thread
           // orders them before its tensor-core reads with a proxy fence after the wait.
           cp_async_arrive_noinc(b_full + 8 * st);
         }
-        issued = s + 1;
+        last_issued = static_cast<int32_t>(use);
       }
       if (aborted) break;
       seq += 4 * nt;
@@ -639,15 +626,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!tma && !FP8) {
       cp_async_wait_0();
-    } else if (aborted && lane == 0) {
-      // Drain: wait (bounded) for the newest copy into every stage this warp filled.
+    } else if (aborted && lane == 0 && last_issued >= 0) {
+      // Drain: wait (bounded) for this warp's newest copy into its stage to land.
       const uint32_t landed = FP8 ? b_land : b_full;
-      for (uint32_t s = issued > static_cast<uint32_t>(R) ? issued - R : 0; s < issued; ++s)
-        if (static_cast<int>(s % R) % W == pw)
-          drain_bar(landed + 8 * (s % R), (s / R) & 1, kDrainLimitNs);
+      drain_bar(landed + 8 * st, static_cast<uint32_t>(last_issued) & 1, kDrainLimitNs);
     }
+    finish_role();
+    return;
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
+    regs_inc<kRoleRegs>();
     constexpr uint32_t kIdescQK = FP8 ? idesc_f16_f32(128, NP, false, false)
                                       : idesc_bf16_f32(128, NP, false, false);
     constexpr uint32_t kIdescPV = FP8 ? idesc_f16_f32(128, NP, true, false)
@@ -762,8 +750,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain_bar(b_fin, 0, aborted ? kDrainLimitNs : kWaitLimitNs);
     }
     __syncwarp();
-  } else {
+    finish_role();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, static_cast<uint32_t>(p.tmem_cols));
+    return;
+  } else if (warp < kSoftmaxWarps) {
     // ------------------------------------------------------------ softmax + epilogue (warps 0-3)
+    regs_inc<kSoftmaxRegs>();   // the registers warpgroups 2-4 returned
     const int t = threadIdx.x;                       // tensor-memory lane = slot within tile
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     uint32_t js = 0, it = 0, rb = 0;
@@ -1024,14 +1017,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       js += nt;
       if (FP8) mbar_arrive(b_itemempty + 8 * b);
     }
+    finish_role();
+    return;
   }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == kMmaWarp) {
-    tc_fence_after();
-    tmem_dealloc(tmem_base, static_cast<uint32_t>(p.tmem_cols));
-  }
+  // warps 6 and 7 have no role; they take part in their warpgroup's register reallocation
+  regs_inc<kRoleRegs>();
+  finish_role();
 }
 
 // ---------------------------------------------------------------------------- host side

@@ -198,6 +198,17 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
   return r;
 }
 
+// Warpgroup register reallocation: every thread of the executing warpgroup ends with `N`
+// registers (inc waits for the CTA's free pool, dec returns registers to it).
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // Position in a ring of n stages, advanced one piece at a time: the stage and the parity of its
 // current fill, kept without dividing a running piece count by a runtime stage count.
 struct RingPos {
