@@ -37,9 +37,13 @@ static_assert(kGatherWarp0 + kProducerWarps == kThreads / 32 && kGatherWarp0 % 4
               "gather warps fill whole warpgroups at the end of the CTA");
 static_assert(128 * kSoftmaxRegs + 128 * kRoleRegs + 384 * kGatherRegs <= kThreads * kLaunchRegs,
               "register split within the launch's registers");
-// MLA kernel: six gather warps (five share the latent pieces, one the rope pieces), 384 threads.
-constexpr int kMlaProducerWarps = 6;
-constexpr int kMlaThreads = 32 * (kProducerWarp0 + kMlaProducerWarps);
+// MLA kernel: the same 20-warp layout and register split; gather warps 8-17 share every latent
+// piece and warps 18-19 every rope piece.
+constexpr int kMlaLatentWarps = 10;
+constexpr int kMlaRopeWarps = 2;
+constexpr int kMlaProducerWarps = kMlaLatentWarps + kMlaRopeWarps;
+constexpr int kMlaThreads = kThreads;
+static_assert(kGatherWarp0 + kMlaProducerWarps == kMlaThreads / 32, "MLA gather warpgroups");
 constexpr int kMinStages = 4;                // ring must hold V(j) and K(j+1) together
 // MMA issue lookahead of the d=256 kernel: QK^T(j+L) is issued before P.V(j), with L + 1 S^T
 // buffers.  Measured on GB300: per-token tiles (N = 16) run fastest at L = 1 (L = 2 or 3 cost

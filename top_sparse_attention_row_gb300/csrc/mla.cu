@@ -17,10 +17,12 @@
 //    a spare stage) and the rope chunk of S(j+1) go first, overlapping the softmax of tile j;
 //    then P.V(j), each 128-dim output chunk releasing its latent piece as soon as its MMAs
 //    complete, so the gather of tile j+1 runs under P.V(j); then the rest of S(j+1).
-//  * Gather: TMA tile::gather4 (4 rows x 128 bytes per op).  Five producer warps share every
-//    latent piece (each issues about a fifth of its 64 ops), so a stage freed by P.V refills in
-//    a fifth of the time one warp would take; a sixth warp gathers the rope pieces.  Padding rows
-//    use a row past the tensor map, which TMA zero-fills.
+//  * Gather: TMA tile::gather4 (4 rows x 128 bytes per op).  Ten gather warps share every
+//    latent piece (each issues about a tenth of its 64 ops), so a stage freed by P.V refills in
+//    a tenth of the time one warp would take; two more share the rope pieces.  Padding rows use
+//    a row past the tensor map, which TMA zero-fills.
+//  * 20 warps (five warpgroups) with warpgroup register reallocation, as in the d=256 kernel:
+//    softmax (0-3), MMA and index (4-5, with two idle warps), gather (8-19).
 //  * Online softmax, epilogue, union masks, bounded waits and failure containment follow the
 //    d=256 kernel.
 #include <cuda.h>
@@ -40,8 +42,7 @@ constexpr unsigned long long kMlaWaitNs = 2000000000ull;    // 2 s per wait
 constexpr unsigned long long kMlaDrainNs = 200000000ull;    // 0.2 s per drain wait
 constexpr float kMlaRescale = 8.0f;                         // log2 units
 constexpr float kMlaLn2 = 0.6931471805599453f;
-constexpr int kMlaPairOwners = 5;                           // producer warps 0-4: latent stages
-constexpr int kMlaRopeOwner = 5;                            // producer warp 5: the rope stage
+constexpr int kMlaPairOwners = kMlaLatentWarps;             // gather warps sharing latent pieces
 
 // Wait sites of this kernel in the status word (0x100 | site), after the d=256 kernel's.
 enum MlaSite : int32_t {
@@ -55,7 +56,7 @@ __device__ __forceinline__ unsigned long long mla_ns() {
   return t;
 }
 
-__device__ __noinline__ bool mla_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+__device__ __forceinline__ bool mla_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                            int32_t* status, int32_t site,
                                            unsigned long long limit) {
   const unsigned long long t0 = mla_ns();
@@ -72,7 +73,7 @@ __device__ __noinline__ bool mla_wait_slow(uint32_t bar, uint32_t parity, volati
 
 // Bounded wait that ignores the abort flag: after an abort, lets copies and MMAs already issued
 // complete before shared or tensor memory is given up.
-__device__ __noinline__ bool mla_drain(uint32_t bar, uint32_t parity, int32_t* status,
+__device__ __forceinline__ bool mla_drain(uint32_t bar, uint32_t parity, int32_t* status,
                                        unsigned long long limit) {
   const unsigned long long t0 = mla_ns();
   while (!mbar_try_wait(bar, parity)) {
@@ -152,7 +153,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       mbar_init(b_lfull + 8 * s, kMlaPairOwners);   // each latent warp arms its share
       mbar_init(b_lempty + 8 * s, 1);
     }
-    mbar_init(b_rfull, 1);
+    mbar_init(b_rfull, kMlaRopeWarps);   // each rope warp arms its share
     mbar_init(b_rempty, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(b_sfull + 8 * b, 1);
@@ -175,7 +176,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), static_cast<uint32_t>(p.tmem_cols));
     tmem_relinquish();
   }
-  if (warp == kProducerWarp0 && lane == 0) prefetch_tmap(&tmKV);
+  if (warp == kGatherWarp0 && lane == 0) prefetch_tmap(&tmKV);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -185,8 +186,15 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
 
   const int64_t n_items = p.n_items;
   const int64_t stride = gridDim.x;
+  // Every role ends here and returns (no code shared by warpgroups with different register
+  // counts after the reallocation).
+  auto finish_role = [&]() {
+    tc_fence_before();
+    __syncthreads();
+  };
 
   if (warp == kIndexWarp) {
+    regs_inc<kRoleRegs>();
     // ------------------------------------------------------------ index / Q loader
     // Items as in the d=256 kernel: static round robin, or (union mode) longest-first from a
     // global counter; a record with n_valid = -1 ends every role.
@@ -277,17 +285,23 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(b_qfull);
     }
-  } else if (warp >= kProducerWarp0 && warp < kProducerWarp0 + kMlaProducerWarps) {
+    finish_role();
+    return;
+  } else if (warp >= kGatherWarp0) {
+    regs_dec<kGatherRegs>();
     // ------------------------------------------------------------ gather producers
-    // Warps 0-4 share every latent piece: gather4 op o = 32a + lane (o < 64; atom a, slots
-    // 4*lane .. 4*lane+3) is issued by warp o % 5, and each warp arms the stage's barrier with
-    // its own share of the bytes.  A warp's gather instructions issue one after another (~1.2 us
-    // per 32-lane gather4 on GB300), and here a freed stage is on the critical path -- the next
-    // tile's QK^T waits for it -- so five warps filling it together beat one owner per stage
-    // (mla_8k 4.30 -> 3.61 ms).  Warp 5 gathers every rope piece.
-    const int pw = warp - kProducerWarp0;
+    // Gather warps 0-9 share every latent piece: gather4 op o = 32a + lane (o < 64; atom a,
+    // slots 4*lane .. 4*lane+3) is issued by warp o % 10, and each warp arms the stage's barrier
+    // with its own share of the bytes.  A warp's gather instructions issue one after another
+    // (~40 ns each on GB300), and here a freed stage is on the critical path -- the next tile's
+    // QK^T waits for it -- so many warps filling it together beat one owner per stage (five
+    // warps: mla_8k 4.30 -> 3.61 ms).  Warps 10 and 11 share every rope piece the same way.
+    const int pw = warp - kGatherWarp0;
+    const int rw = pw - kMlaPairOwners;   // rope warp index (>= 0 for the rope warps)
     const uint32_t share_bytes =
-        static_cast<uint32_t>((64 - pw + kMlaPairOwners - 1) / kMlaPairOwners) * 512u;
+        pw < kMlaPairOwners
+            ? static_cast<uint32_t>((64 - pw + kMlaPairOwners - 1) / kMlaPairOwners) * 512u
+            : static_cast<uint32_t>(32 / kMlaRopeWarps) * 512u;
     uint32_t lseq = 0, rseq = 0, it = 0;
     uint32_t l_issued = 0, r_issued = 0;
     bool aborted = false;
@@ -352,7 +366,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
                           b_lfull + 8 * st);
           l_issued = s + 1;
         }
-      } else if (pw == kMlaRopeOwner) {
+      } else {
         for (int j = 0; j < nt; ++j) {
           const uint32_t s = rseq + j;
           const int y0 = n0, y1 = n1, y2 = n2, y3 = n3;
@@ -361,9 +375,10 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
             aborted = true;
             break;
           }
-          if (lane == 0) mbar_arrive_expect_tx(b_rfull, kMlaRopeBytes);
+          if (lane == 0) mbar_arrive_expect_tx(b_rfull, share_bytes);
           __syncwarp();
-          tma_gather4(base + L.rope + lane * 512, &tmKV, kMlaDv, y0, y1, y2, y3, b_rfull);
+          if (lane % kMlaRopeWarps == rw)
+            tma_gather4(base + L.rope + lane * 512, &tmKV, kMlaDv, y0, y1, y2, y3, b_rfull);
           r_issued = s + 1;
         }
       }
@@ -378,11 +393,14 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       if (pw < kMlaPairOwners) {
         for (uint32_t s = l_issued > static_cast<uint32_t>(RP) ? l_issued - RP : 0; s < l_issued; ++s)
           mla_drain(b_lfull + 8 * (s % RP), (s / RP) & 1, status, kMlaDrainNs);
-      } else if (pw == kMlaRopeOwner && r_issued > 0) {
+      } else if (r_issued > 0) {
         mla_drain(b_rfull, (r_issued - 1) & 1, status, kMlaDrainNs);
       }
     }
+    finish_role();
+    return;
   } else if (warp == kMmaWarp) {
+    regs_inc<kRoleRegs>();
     // ------------------------------------------------------------ MMA issuer (one thread)
     constexpr uint32_t kIdescQK = idesc_bf16_f32(128, NP, false, false);
     constexpr uint32_t kIdescPV = idesc_bf16_f32(128, NP, true, false);
@@ -549,7 +567,12 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       mla_drain(b_fin, 0, status, aborted ? kMlaDrainNs : kMlaWaitNs);
     }
     __syncwarp();
+    finish_role();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, static_cast<uint32_t>(p.tmem_cols));
+    return;
   } else if (warp < kSoftmaxWarps) {
+    regs_inc<kSoftmaxRegs>();
     // ------------------------------------------------------------ softmax + epilogue (warps 0-3)
     const int t = threadIdx.x;                       // tensor-memory lane = slot within tile
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
@@ -756,14 +779,12 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       tc_fence_before();
       js += nt;
     }
+    finish_role();
+    return;
   }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == kMmaWarp) {
-    tc_fence_after();
-    tmem_dealloc(tmem_base, static_cast<uint32_t>(p.tmem_cols));
-  }
+  // warps 6 and 7 have no role; they take part in their warpgroup's register reallocation
+  regs_inc<kRoleRegs>();
+  finish_role();
 }
 
 namespace {
