@@ -140,8 +140,8 @@ __host__ __device__ inline SmemLayout smem_layout(int np, int stages, int slot_c
   L.slots = L.pbuf + 2 * L.p_bytes;
   L.bars = L.slots + 2 * slot_cap * 4;
   // full[st], empty[st], s_full[kMaxSBufs], s_free[kMaxSBufs], p_full[2], pv_done[2],
-  // item_full[2], item_empty[2], q_empty, q_full, final, landed[st] (FP8 caches only)
-  L.misc = L.bars + ((fp8 ? 3 : 2) * stages + 2 * kMaxSBufs + 11) * 8;
+  // item_full[2], item_empty[2], q_empty, q_full, final, landed[st][block] (FP8 caches only)
+  L.misc = L.bars + ((fp8 ? 2 + kBlocksPerStage : 2) * stages + 2 * kMaxSBufs + 11) * 8;
   // info[2][8] int32, red[2][4][np] float, tmem base, abort flag, vote[3]
   int misc_bytes = 2 * 8 * 4 + 2 * 4 * np * 4 + 32;
   L.total = L.misc + misc_bytes + 1024;   // + alignment slack for the 1024-aligned base

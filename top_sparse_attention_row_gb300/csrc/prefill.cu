@@ -21,21 +21,26 @@
 //  * K/V rows are gathered into a ring of 32 KiB stages (128 slots x 128 dims, 128-byte
 //    swizzled rows) in exactly the order the MMA consumes them -- with L = 1: K(0), K(1), V(0),
 //    K(2), V(1), ..., V(nt-1), two half-row pieces each -- so the ring drains FIFO; one commit
-//    releases a piece pair's two stages.  Each of six producer warps owns one stage and gathers
-//    whole pieces into it: per-SM gather bandwidth grows with the number of warps issuing
-//    copies concurrently.  Two gather engines: TMA tile::gather4 (default; 4 slots x 128 B per
-//    instruction, out-of-bounds rows zero-filled) and cp.async 16-byte copies (lanes arrive on
-//    the stage barrier as their copies land and the MMA thread fences them into the async
-//    proxy).
-//  * FP8 caches (template FP8): e4m3 half-rows land in the upper half of the stage and the
-//    owning producer rewrites the stage in place as the fp16 tile; the MMAs run fp16 operands,
-//    the K page scale multiplies the logit and the V page scale the probability fed to P.V.
+//    releases a piece pair's two stages, and the MMA thread and the gather warps track ring
+//    positions by counting, never by dividing by the (runtime) stage count.  Two gather warps
+//    fill each stage, one per 64-dim block: per-SM gather bandwidth grows with the number of
+//    warps issuing copies concurrently, and a V tile -- which reuses the stages of the same
+//    tile's K, freed when its QK^T completes -- lands in half the time.  Two gather engines:
+//    TMA tile::gather4 (default; 4 slots x 128 B per instruction, out-of-bounds rows
+//    zero-filled) and cp.async 16-byte copies (lanes arrive on the stage barrier as their copies
+//    land and the MMA thread fences them into the async proxy).
+//  * FP8 caches (template FP8): a piece's e4m3 rows land in the upper half of the stage and
+//    the two gather warps each rewrite 64 of its rows in place as fp16; the MMAs run fp16 operands,
+//    the K page scale multiplies the logit and the V page scale (normalised per item) the
+//    probability fed to P.V.
 //  * Online softmax in registers, one thread per slot (tensor-memory lane).  The running max
 //    is only raised when a tile's logits exceed it by more than 2^8 (log2 domain), so the
 //    O^T rescale through tensor memory is rare; the result is exact either way because O and
 //    the row sum use the same stale max.
-//  * Warp roles: 0-3 softmax + epilogue, 4 MMA issue + tensor-memory owner, 5 index/Q loader
-//    (per-token: compacts the row's valid slots into shared memory), 6-11 gather producers.
+//  * Warp roles (20 warps, five warpgroups): 0-3 softmax + epilogue; 4 MMA issue + tensor-memory
+//    owner; 5 index/Q loader (per-token: compacts the row's valid slots into shared memory);
+//    6-7 idle; 8-19 gather, two per stage.  Warpgroup register reallocation (setmaxnreg) moves
+//    registers from the gather warpgroups to the softmax and MMA/index warpgroups.
 //  * Every mbarrier wait is bounded (~2 s); a timeout records a code in a device status word,
 //    all roles leave their loops, in-flight copies and MMAs are drained, tensor memory is
 //    freed and the kernel returns.
@@ -252,9 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* const gbase = smem_raw + (base - raw_u32);
 
   constexpr int kLookahead = lookahead_for(UNION);
-  // Gather warps per stage: two (one per 64-dim block) for bf16 caches; one for FP8 caches,
-  // whose stage rewrite from e4m3 to fp16 is done by one warp.
-  constexpr int kBPS = FP8 ? 1 : kBlocksPerStage;
+  constexpr int kBPS = kBlocksPerStage;   // gather warps per stage, one per 64-dim block
   constexpr int kSBufs = kLookahead + 1;
   const int slot_cap = UNION ? 0 : p.slot_cap;
   const SmemLayout L = smem_layout(NP, p.stages, slot_cap, FP8);
@@ -272,7 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t b_qempty = b_itemempty + 16;     // Q buffer free (MMA commit, once per item)
   const uint32_t b_qfull = b_qempty + 8;          // Q buffer written (index warp, once per item)
   const uint32_t b_fin = b_qempty + 16;           // MMA issuer drained
-  const uint32_t b_land = b_fin + 8;              // FP8: a stage's e4m3 bytes landed [R]
+  const uint32_t b_land = b_fin + 8;              // FP8: a block's e4m3 bytes landed [R][2]
 
   ItemInfo* const info = reinterpret_cast<ItemInfo*>(gbase + L.misc);
   float* const red = reinterpret_cast<float*>(gbase + L.misc + 2 * sizeof(ItemInfo));  // [2][4][NP]
@@ -288,9 +291,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < R; ++s) {
       // TMA: one expect_tx per gather warp of the stage; FP8: one arrival after converting (the
       // stage's first warp does the whole piece); cp.async: every lane of both warps
-      mbar_init(b_full + 8 * s, FP8 ? 1 : p.gather_tma ? kBPS : 32 * kBPS);
+      // TMA: one expect_tx per gather warp; FP8: each warp arrives after rewriting its block;
+      // cp.async: every lane of both warps
+      mbar_init(b_full + 8 * s, (FP8 || p.gather_tma) ? kBPS : 32 * kBPS);
       mbar_init(b_empty + 8 * s, 1);   // stage pairs share empty[pair]: [0, R/2) are used
-      if (FP8) mbar_init(b_land + 8 * s, 1);
+      if (FP8)
+        for (int c = 0; c < kBPS; ++c) mbar_init(b_land + 8 * (kBPS * s + c), 1);
     }
     for (int b = 0; b < kSBufs; ++b) {
       mbar_init(b_sfull + 8 * b, 1);
@@ -545,21 +551,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const CUtensorMap* tm = is_v ? &tmV : &tmK;
         if (FP8) {
-          // e4m3 half-rows (128 B) land in the stage's upper 16 KiB, then the warp rewrites the
-          // stage in place as the f16 tile: each lane takes whole rows (lane + 32k).  A row's
-          // upper fp16 block overwrites its own e4m3 bytes, so dims 0-63 (lower block, no
-          // overlap) are written from the first four input chunks before the last four are read.
-          if (lane == 0) mbar_arrive_expect_tx(b_land + 8 * st, kStageBytes / 2);
+          // The piece's e4m3 rows (128 B: its 128 dims) land in the stage's upper 16 KiB, and
+          // each of the stage's two warps gathers and rewrites 64 of the 128 slot rows: 16
+          // gather4 (half the requests of a bf16 piece's block), then the rows in place as fp16.
+          // A row's upper fp16 block overwrites only its own e4m3 bytes, so the rows, and the
+          // two warps, are independent: dims 0-63 (lower block, no overlap) are written from the
+          // first four input chunks before the last four are read.
+          const uint32_t land = b_land + 8 * (kBPS * st + blk);
+          const int g = 16 * blk + (lane & 15);          // this lane's 4-slot group of the tile
+          int f0, f1, f2, f3;
+          if (UNION) {
+            f0 = __shfl_sync(0xffffffffu, y0, g);
+            f1 = __shfl_sync(0xffffffffu, y1, g);
+            f2 = __shfl_sync(0xffffffffu, y2, g);
+            f3 = __shfl_sync(0xffffffffu, y3, g);
+          } else {
+            const int t = t0 + 4 * g;
+            const int4 v = *reinterpret_cast<const int4*>(sl + t);
+            f0 = t + 0 < nv ? v.x : p.pad_row;
+            f1 = t + 1 < nv ? v.y : p.pad_row;
+            f2 = t + 2 < nv ? v.z : p.pad_row;
+            f3 = t + 3 < nv ? v.w : p.pad_row;
+          }
+          if (lane == 0) mbar_arrive_expect_tx(land, 64 * 128);
           __syncwarp();
-          tma_gather4(stage + 16384 + lane * 512, tm, half * 128, y0, y1, y2, y3, b_land + 8 * st);
+          if (lane < 16) tma_gather4(stage + 16384 + g * 512, tm, half * 128, f0, f1, f2, f3, land);
           last_issued = static_cast<int32_t>(use);
-          if (!__all_sync(0xffffffffu, wait_bar(b_land + 8 * st, use & 1, abort_flag, kSiteLanded))) {
+          if (!__all_sync(0xffffffffu, wait_bar(land, use & 1, abort_flag, kSiteLanded))) {
             aborted = true;
             break;
           }
 #pragma unroll 1
-          for (int k = 0; k < 4; ++k) {
-            const int t = lane + 32 * k;
+          for (int k = 0; k < 2; ++k) {
+            const int t = 64 * blk + lane + 32 * k;
             const uint32_t sw = static_cast<uint32_t>(t & 7);
 #pragma unroll
             for (int hb = 0; hb < 2; ++hb) {
@@ -575,9 +599,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint4 hi = make_uint4(e4m3x2_to_f16x2(in[c].z & 0xffffu), e4m3x2_to_f16x2(in[c].z >> 16),
                                             e4m3x2_to_f16x2(in[c].w & 0xffffu), e4m3x2_to_f16x2(in[c].w >> 16));
                 const uint32_t row = stage + hb * 16384 + t * 128;
-                const uint32_t j0 = static_cast<uint32_t>(2 * c);
-                sts_v4(row + ((j0 ^ sw) << 4), lo);
-                sts_v4(row + (((j0 + 1) ^ sw) << 4), hi);
+                sts_v4(row + (((2 * c) ^ sw) << 4), lo);
+                sts_v4(row + (((2 * c + 1) ^ sw) << 4), hi);
               }
             }
           }
@@ -628,8 +651,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       cp_async_wait_0();
     } else if (aborted && lane == 0 && last_issued >= 0) {
       // Drain: wait (bounded) for this warp's newest copy into its stage to land.
-      const uint32_t landed = FP8 ? b_land : b_full;
-      drain_bar(landed + 8 * st, static_cast<uint32_t>(last_issued) & 1, kDrainLimitNs);
+      const uint32_t landed = FP8 ? b_land + 8 * (kBPS * st + blk) : b_full + 8 * st;
+      drain_bar(landed, static_cast<uint32_t>(last_issued) & 1, kDrainLimitNs);
     }
     finish_role();
     return;
