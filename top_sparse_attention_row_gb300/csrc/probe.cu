@@ -1,12 +1,9 @@
 // Gather-ceiling probe: how fast can one GB300 SM pull random half-rows (256 B) of a KV cache
 // from L2 into shared memory, with nothing else running?  It uses the same engines and shapes as
-// the attention kernel's producers -- TMA tile::gather4 (4 rows x 128 B per op) or cp.async
-// 16-byte copies, 32 KiB pieces of 128 rows x 256 B, 128-byte swizzled destinations, a 6-stage
-// ring -- but the consumer only releases each stage, so the result bounds what the gather side
-// of the kernel can approach.
-//
-// Each of the six producer warps owns one stage of the ring and gathers every piece that lands
-// on it, so no two warps ever wait on different phases of one stage.
+// the d=256 attention kernel's gather warps -- TMA tile::gather4 (4 rows x 128 B per op) or
+// cp.async 16-byte copies, 32 KiB pieces of 128 rows x 256 B, 128-byte swizzled destinations, a
+// 6-stage ring filled by two warps per stage, one per 64-dim block -- but the consumer only
+// releases each stage, so the result bounds what the gather side of the kernel can approach.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -14,7 +11,8 @@ namespace qsa {
 namespace {
 
 constexpr int kProbeStages = 6;
-constexpr int kProbeWarps = kProbeStages + 1;     // six owners + one releasing consumer
+constexpr int kProbeGatherWarps = kProbeStages * kBlocksPerStage;
+constexpr int kProbeWarps = kProbeGatherWarps + 1;     // gather warps + one releasing consumer
 
 __device__ __forceinline__ unsigned long long probe_ns() {
   unsigned long long t;
@@ -58,7 +56,7 @@ __global__ void __launch_bounds__(32 * kProbeWarps, 1)
     for (int s = 0; s < kProbeStages; ++s) {
       // engine 2 (mixed): even stages TMA, odd stages cp.async
       const bool stage_tma = use_tma == 1 || (use_tma == 2 && (s & 1) == 0);
-      mbar_init(full + 8 * s, stage_tma ? 1 : 32);
+      mbar_init(full + 8 * s, stage_tma ? kBlocksPerStage : 32 * kBlocksPerStage);
       mbar_init(empty + 8 * s, 1);
     }
     abort_flag = 0;
@@ -66,32 +64,30 @@ __global__ void __launch_bounds__(32 * kProbeWarps, 1)
   }
   __syncthreads();
   volatile int* ab = &abort_flag;
-  if (warp < kProbeStages) {
-    const int st = warp;
+  if (warp < kProbeGatherWarps) {
+    const int st = warp / kBlocksPerStage, blk = warp % kBlocksPerStage;
     const bool warp_tma = use_tma == 1 || (use_tma == 2 && (st & 1) == 0);
     int last = -1;   // newest piece this warp issued
     for (int p = st; p < pieces_per_cta; p += kProbeStages) {
       const uint32_t par = ((p / kProbeStages) & 1) ^ 1;
       if (!__all_sync(0xffffffffu, probe_wait(empty + 8 * st, par, ab, status))) break;
       const int32_t* prow = rows + ((blockIdx.x * 131 + p) % n_table_pieces) * kTileTokens;
-      const uint32_t dst = base + st * kStageBytes;
+      const uint32_t dst = base + st * kStageBytes + blk * 16384;
       if (warp_tma) {
-        // lane: rows 4*lane .. 4*lane+3, two gather4 ops (dims 0-63 and 64-127)
+        // lane: rows 4*lane .. 4*lane+3 of this warp's 64-dim block
         const int4 y = *reinterpret_cast<const int4*>(prow + 4 * lane);
-        if (lane == 0) mbar_arrive_expect_tx(full + 8 * st, kStageBytes);
+        if (lane == 0) mbar_arrive_expect_tx(full + 8 * st, kStageBytes / kBlocksPerStage);
         __syncwarp();
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-          tma_gather4(dst + c * 16384 + lane * 512, &tm, c * 64, y.x, y.y, y.z, y.w, full + 8 * st);
+        tma_gather4(dst + lane * 512, &tm, blk * 64, y.x, y.y, y.z, y.w, full + 8 * st);
         last = p;
         continue;
       }
-      const int ch = lane & 15;
+      const int ch = lane & 7;
 #pragma unroll 8
-      for (int i = 0; i < 64; ++i) {
-        const int t = 2 * i + (lane >> 4);
-        const uint8_t* src = cache + static_cast<int64_t>(prow[t]) * (kHeadDim * 2) + ch * 16;
-        const uint32_t d = dst + (ch >> 3) * 16384 + t * 128 + (((ch & 7) ^ (t & 7)) << 4);
+      for (int i = 0; i < 32; ++i) {
+        const int t = 4 * i + (lane >> 3);
+        const uint8_t* src = cache + static_cast<int64_t>(prow[t]) * (kHeadDim * 2) + blk * 128 + ch * 16;
+        const uint32_t d = dst + t * 128 + ((ch ^ (t & 7)) << 4);
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
       }
       asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(full + 8 * st)
@@ -104,7 +100,7 @@ __global__ void __launch_bounds__(32 * kProbeWarps, 1)
       // land (bounded) before the block exits
       probe_drain(full + 8 * st, (last / kProbeStages) & 1);
     }
-  } else if (warp == kProbeStages) {
+  } else if (warp == kProbeGatherWarps) {
     for (int p = 0; p < pieces_per_cta; ++p) {
       const int st = p % kProbeStages;
       if (!__all_sync(0xffffffffu, probe_wait(full + 8 * st, (p / kProbeStages) & 1, ab, status)))
