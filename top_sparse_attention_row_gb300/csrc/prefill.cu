@@ -289,8 +289,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < R; ++s) {
-      // TMA: one expect_tx per gather warp of the stage; FP8: one arrival after converting (the
-      // stage's first warp does the whole piece); cp.async: every lane of both warps
       // TMA: one expect_tx per gather warp; FP8: each warp arrives after rewriting its block;
       // cp.async: every lane of both warps
       mbar_init(b_full + 8 * s, (FP8 || p.gather_tma) ? kBPS : 32 * kBPS);
