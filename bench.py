@@ -280,6 +280,7 @@ class Prepared:
                     if self.mla else torch.empty_like(q))
         self.lse = torch.empty((w.n_rows, w.n_qheads), dtype=torch.float32, device=dev)
         self.ws = None
+        self.forced = None   # forced geometry fields for the plain entry (None = selector)
         if union > 1 and not (self.mla or fp8 or paged):
             nb = binding.union_workspace_bytes(w.n_rows, w.topk, union)
             self.ws = torch.empty(max(nb, 256), dtype=torch.uint8, device=dev)
@@ -305,7 +306,7 @@ class Prepared:
                                    n_pages=w.meta["n_pages"], out=out, lse=lse, union_g=u, stream=st)
         else:
             b.sparse_prefill(q, k, v, idx, tl, w.scale, out=out, lse=lse, union_g=u, workspace=ws,
-                             stream=st)
+                             forced=self.forced, stream=st)
 
     def call(self):
         self.call_on(self.dev_in, self.out, self.lse, self.ws)
@@ -381,7 +382,7 @@ SUB_CONFIGS = [
     ("union_8k", {"union": 1}), ("union_8k", {"union": 2}), ("union_8k", {"union": 4}),
     ("mixed_paged", {"paged": True}), ("mla_8k", {"union": 0}), ("mla_8k", {"union": 2}),
     ("mla_8k", {"union": 4}), ("group6_32k", {"fp8": True}), ("union_8k", {"union": 4, "fp8": True}),
-]
+] + [(f"rows{r}_8k", {}) for r in (32, 64, 128, 256, 512, 1024)]   # query-count sweep
 
 
 def run_gpu(args, rank, world, local_rank):
@@ -649,6 +650,13 @@ def run_sub_configs(binding, W, dev, stream, flush, peaks, peak_src, ceiling_gbs
                                          64, 1),
                      "geometry": prep.geo, "roofline": roof, "clocks": clocks,
                      "launches_per_call": launches}
+        if prep.geo.get("split", 1) > 1:
+            # the same calls without the split (one CTA per row), for the sweep's comparison
+            prep.forced = {"split": 1}
+            t1 = device_times(prep, steps, 3, flush, stream)
+            prep.forced = None
+            ms1 = sum(t1) / len(t1)
+            recs[key]["unsplit"] = {"ms": ms1, "value": prep.w.n_rows / (ms1 / 1e3)}
         del prep
         torch.cuda.empty_cache()
     return recs

@@ -68,6 +68,14 @@ typedef struct qsa_geometry {
   int32_t smem_bytes;       /* dynamic shared memory per CTA */
   int32_t tmem_cols;        /* tensor-memory columns allocated per CTA */
   int64_t n_items;          /* work items: row groups x KV heads x head chunks */
+  int32_t split;            /* CTAs (one thread-block cluster) sharing each work item: 1, 2, 4 or 8.
+                               Per-token bf16 calls (tiles of <= 32 columns) with fewer items
+                               than SMs split each row's 128-slot tiles over a cluster and
+                               merge the partial softmax statistics and outputs through
+                               distributed shared memory ("[QSA] Tune sm120 sparse prefill
+                               geometry", Query-count sweep: small row counts).  A row's result
+                               is then summed in another order than with split 1 (within the
+                               stated tolerance, deterministic per geometry). */
 } qsa_geometry;
 
 /* Per-path call counters (host side, process wide), in the spirit of the pages' invocation
@@ -105,8 +113,10 @@ qsa_status qsa_sparse_prefill(const void* q, const void* k_cache, const void* v_
  *   workspace / workspace_bytes: caller scratch for union mode (NULL = allocate on stream);
  *               must hold qsa_union_workspace_bytes(n_rows, topk, effective union_g) bytes and be
  *               256-byte aligned.  Unused by the per-token path.
- *   forced:     host pointer, NULL = selector; fields > 0 override stages and grid (an
- *               oversized stage count is stepped down to fit and counted). */
+ *   forced:     host pointer, NULL = selector; fields > 0 override stages, grid and split (an
+ *               oversized stage count is stepped down to fit and counted; split is rounded down
+ *               to a power of two <= 8 and applies to per-token bf16 tiles of <= 32 columns
+ *               only). */
 qsa_status qsa_sparse_prefill_ex(const void* q, const void* k_cache, const void* v_cache,
                                  const int32_t* indices, const int32_t* topk_len,
                                  void* out, float* lse,

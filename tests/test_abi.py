@@ -55,6 +55,23 @@ def test_selector_configs(lib):
     assert g["tmem_cols"] in (32, 64, 128, 256, 512) and g["tmem_cols"] >= 4 * g["n_pad"]
 
 
+def test_selector_splits_small_calls(lib):
+    """Per-token calls with fewer items than SMs share each item over a cluster of 2, 4 or 8
+    CTAs (at most one tile each, tiles of <= 32 columns); everything else keeps split 1."""
+    from top_sparse_attention_row_gb300 import binding as B
+    expect = {1: 8, 7: 8, 19: 8, 20: 4, 32: 4, 38: 4, 39: 2, 64: 2, 76: 2, 77: 1, 128: 1, 8192: 1}
+    for rows, split in expect.items():
+        g = B.select_geometry(6, 1, 0, 2051, 256, rows, 152)
+        assert g["split"] == split, (rows, g)
+        assert g["grid"] == min(rows, 152 // split) * split and g["grid"] <= 152
+        assert g["smem_bytes"] <= 232448 and (split == 1 or g["stages"] == 4)
+    assert B.select_geometry(24, 2, 0, 2051, 256, 7, 152)["split"] == 8      # 14 items
+    assert B.select_geometry(6, 1, 0, 300, 256, 7, 152)["split"] == 2       # 3 tiles a row
+    assert B.select_geometry(6, 1, 0, 128, 256, 7, 152)["split"] == 1       # one tile
+    assert B.select_geometry(6, 1, 4, 2051, 256, 7, 152)["split"] == 1      # union
+    assert B.select_geometry(48, 1, 0, 2051, 256, 7, 152)["split"] == 1     # 48 columns
+
+
 def test_selector_union_fallback_and_head_chunks(lib):
     from top_sparse_attention_row_gb300 import binding as B
     # 32 heads per KV group x G=4 = 128 columns > 64: falls back to per-token

@@ -38,7 +38,7 @@ class Geometry(ctypes.Structure):
                 ("head_chunks", ctypes.c_int32), ("union_g", ctypes.c_int32),
                 ("grid", ctypes.c_int32), ("threads", ctypes.c_int32),
                 ("smem_bytes", ctypes.c_int32), ("tmem_cols", ctypes.c_int32),
-                ("n_items", ctypes.c_int64)]
+                ("n_items", ctypes.c_int64), ("split", ctypes.c_int32)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}

@@ -113,10 +113,30 @@ qsa_status select(int32_t Hq, int32_t Hkv, int32_t union_g, int32_t topk, int32_
     np = static_cast<int>(round_up(chunk_cols, 16));
     slot_cap = 0;
   }
+  const int64_t n_groups = ceil_div(n_rows, G);
+  const int64_t n_items = n_groups * Hkv * chunks;
+  // Split items: per-token bf16 calls with fewer items than SMs give each item a cluster of
+  // `split` CTAs (each a contiguous range of the row's 128-slot tiles, at least one tile each), so
+  // a short call still fills the GPU ("[QSA] Tune sm120 sparse prefill geometry", Query-count
+  // sweep: the row count decides the launch shape).
+  int split = 1;
+  if (G == 1 && !fp8 && np <= qsa::kSplitMaxNPad) {
+    const int64_t tiles = ceil_div(topk, qsa::kTileTokens);
+    for (int c = qsa::kMaxSplit; c >= 2; c /= 2) {
+      if (n_items > 0 && n_items * c <= num_sms && c <= tiles) {
+        split = c;
+        break;
+      }
+    }
+    if (forced && forced->split > 0) {
+      split = 1;
+      while (split * 2 <= forced->split && split * 2 <= qsa::kMaxSplit) split *= 2;
+    }
+  }
   int stages = 0;
   // even stage counts: a piece pair's two stages share one empty barrier
   for (int s = qsa::kMaxStages; s >= qsa::kMinStages; s -= 2) {
-    if (qsa::smem_layout(np, s, slot_cap, fp8).total <= qsa::kSmemLimit) {
+    if (qsa::smem_layout(np, s, slot_cap, fp8, split).total <= qsa::kSmemLimit) {
       stages = s;
       break;
     }
@@ -130,10 +150,12 @@ qsa_status select(int32_t Hq, int32_t Hkv, int32_t union_g, int32_t topk, int32_
     }
     stages = want;
   }
-  const int64_t n_groups = ceil_div(n_rows, G);
-  const int64_t n_items = n_groups * Hkv * chunks;
-  int64_t grid = n_items < num_sms ? n_items : num_sms;
-  if (forced && forced->grid > 0 && forced->grid < grid) grid = forced->grid;
+  // grid: whole clusters, at most one CTA per SM
+  int64_t clusters = n_items < num_sms / split ? n_items : num_sms / split;
+  if (clusters < 1) clusters = 1;
+  if (forced && forced->grid > 0 && forced->grid / split < clusters)
+    clusters = forced->grid / split > 0 ? forced->grid / split : 1;
+  const int64_t grid = clusters * split;
   g->np = np;
   g->cols = chunk_cols;
   g->head_chunks = chunks;
@@ -141,7 +163,8 @@ qsa_status select(int32_t Hq, int32_t Hkv, int32_t union_g, int32_t topk, int32_
   g->union_g = G;
   g->stages = stages;
   g->grid = static_cast<int>(grid);
-  g->smem_bytes = qsa::smem_layout(np, stages, slot_cap, fp8).total;
+  g->smem_bytes = qsa::smem_layout(np, stages, slot_cap, fp8, split).total;
+  g->split = split;
   // S^T buffers (lookahead + 1) + two O^T halves
   g->tmem_cols = pow2_at_least((qsa::lookahead_for(G > 1) + 3) * np);
   g->slot_cap = slot_cap;
@@ -220,6 +243,7 @@ void mla_to_public(const qsa::MlaGeometry& g, qsa_geometry* out) {
   out->smem_bytes = g.smem_bytes;
   out->tmem_cols = g.tmem_cols;
   out->n_items = g.n_items;
+  out->split = 1;
 }
 
 void to_public(const Geometry& g, qsa_geometry* out) {
@@ -234,6 +258,7 @@ void to_public(const Geometry& g, qsa_geometry* out) {
   out->smem_bytes = g.smem_bytes;
   out->tmem_cols = g.tmem_cols;
   out->n_items = g.n_items;
+  out->split = g.split;
 }
 
 // Gather engine: TMA tile::gather4 by default; QSA_GATHER=cpasync selects cp.async 16-byte
@@ -316,10 +341,10 @@ qsa_status run(const void* q, const void* k_cache, const void* v_cache, const in
   if (log_geometry())
     std::fprintf(stderr,
                  "qsa: d=256 rows=%lld heads=%d/%d topk=%d union=%d%s -> N=%d cols=%d chunks=%d "
-                 "stages=%d grid=%d smem=%d tmem=%d items=%lld%s%s\n",
+                 "stages=%d grid=%d split=%d smem=%d tmem=%d items=%lld%s%s\n",
                  static_cast<long long>(n_rows), n_qheads, n_kvheads, topk, g.union_g,
                  fp8 ? " fp8" : (paged ? " paged" : ""), g.np, g.cols, g.head_chunks, g.stages,
-                 g.grid, g.smem_bytes, g.tmem_cols, static_cast<long long>(g.n_items),
+                 g.grid, g.split, g.smem_bytes, g.tmem_cols, static_cast<long long>(g.n_items),
                  fell_back ? " (union fallback)" : "", stepped ? " (stepped down)" : "");
 
   qsa::PrefillParams p{};
@@ -350,6 +375,7 @@ qsa_status run(const void* q, const void* k_cache, const void* v_cache, const in
   p.pad_row = static_cast<int32_t>(tmap_rows);
   if (paged) p.pa = *paged;
   p.stall_first_item = g_stall_next.exchange(0);
+  p.split = g.split;
   if (fp8) {
     p.k_scale = fp8->k_scale;
     p.v_scale = fp8->v_scale;

@@ -105,6 +105,10 @@ struct PrefillParams {
   int32_t page_shift;           // log2(page_size) when a power of two, else -1
   int32_t kv_shift;             // log2(n_kvheads) when a power of two, else -1
   int32_t stall_first_item;     // failure-detection test: the index warp withholds its items
+  // Per-token calls with fewer work items than SMs: the `split` CTAs of a thread-block cluster
+  // share one item, each taking a contiguous range of its 128-slot tiles, and merge their
+  // (max, row sum, O) partials through distributed shared memory.  1 = no split.
+  int32_t split;
   // Union mode: items are handed out through this counter (zeroed by the union build) in
   // reverse order, longest groups first; nullptr = static round robin over the grid.
   int32_t* item_counter;
@@ -123,14 +127,24 @@ struct Geometry {
   int slot_cap;
   int64_t n_items;
   int n_groups;
+  int split;          // CTAs sharing one item (a cluster); 1 = none
 };
+
+// Split items: at most eight CTAs per cluster (the portable cluster size), per-token tiles of
+// at most 32 query columns.
+constexpr int kMaxSplit = 8;
+constexpr int kSplitMaxNPad = 32;
+// Row stride (floats) of a split item's received O partials: NP columns + 4 of padding, so the
+// merge's loads of one column by consecutive dims spread over the banks.
+__host__ __device__ constexpr int merge_row_floats(int np) { return np + 4; }
 
 // Shared-memory layout of the attention kernel (offsets from a 1024-aligned base).
 struct SmemLayout {
-  int ring, qbuf, pbuf, slots, bars, misc, total;
+  int ring, qbuf, pbuf, slots, bars, misc, merge_o, merge_ml, total;
   int q_bytes, p_bytes;
 };
-__host__ __device__ inline SmemLayout smem_layout(int np, int stages, int slot_cap, bool fp8) {
+__host__ __device__ inline SmemLayout smem_layout(int np, int stages, int slot_cap, bool fp8,
+                                                  int split = 1) {
   SmemLayout L;
   L.q_bytes = np * 512;
   L.p_bytes = np * 256;
@@ -140,11 +154,18 @@ __host__ __device__ inline SmemLayout smem_layout(int np, int stages, int slot_c
   L.slots = L.pbuf + 2 * L.p_bytes;
   L.bars = L.slots + 2 * slot_cap * 4;
   // full[st], empty[st], s_full[kMaxSBufs], s_free[kMaxSBufs], p_full[2], pv_done[2],
-  // item_full[2], item_empty[2], q_empty, q_full, final, landed[st][block] (FP8 caches only)
-  L.misc = L.bars + ((fp8 ? 2 + kBlocksPerStage : 2) * stages + 2 * kMaxSBufs + 11) * 8;
-  // info[2][8] int32, red[2][4][np] float, tmem base, abort flag, vote[3]
-  int misc_bytes = 2 * 8 * 4 + 2 * 4 * np * 4 + 32;
-  L.total = L.misc + misc_bytes + 1024;   // + alignment slack for the 1024-aligned base
+  // item_full[2], item_empty[2], q_empty, q_full, final, merge_recv, merge_sendok,
+  // landed[st][block] (FP8 caches only)
+  L.misc = L.bars + ((fp8 ? 2 + kBlocksPerStage : 2) * stages + 2 * kMaxSBufs + 13) * 8;
+  // info[2][12] int32, red[2][4][np] float, tmem base, abort flag, vote[3]
+  int misc_bytes = 2 * 12 * 4 + 2 * 4 * np * 4 + 32;
+  L.merge_o = (L.misc + misc_bytes + 15) & ~15;
+  // split items: O partials [split][256 / split dims][merge_row_floats(np)] and the (max, row
+  // sum) pairs [split][np] of every CTA of the cluster
+  const int merge_bytes = split > 1 ? 256 * merge_row_floats(np) * 4 : 0;
+  L.merge_ml = L.merge_o + merge_bytes;
+  const int ml_bytes = split > 1 ? split * np * 8 : 0;
+  L.total = L.merge_ml + ml_bytes + 1024;   // + alignment slack for the 1024-aligned base
   return L;
 }
 
@@ -182,6 +203,10 @@ struct MlaParams {
   float scale_log2;
   PagedAddr pa;                 // page_table == nullptr = physical slots
   int32_t stall_first_item;     // failure-detection test: the index warp withholds its items
+  // Per-token calls with fewer work items than SMs: the `split` CTAs of a thread-block cluster
+  // share one item, each taking a contiguous range of its 128-slot tiles, and merge their
+  // (max, row sum, O) partials through distributed shared memory.  1 = no split.
+  int32_t split;
   int32_t* item_counter;        // union mode: longest-first item counter (as PrefillParams)
 };
 

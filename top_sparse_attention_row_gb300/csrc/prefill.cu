@@ -49,6 +49,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstring>
 #include <mutex>
@@ -70,7 +71,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 enum WaitSite : int32_t {
   kSiteItemEmpty = 1, kSiteQEmpty, kSiteItemFull, kSiteStageEmpty, kSiteStageFull,
-  kSiteSFree, kSiteSFull, kSitePFull, kSitePvDone, kSiteDrain, kSiteQFull, kSiteLanded
+  kSiteSFree, kSiteSFull, kSitePFull, kSitePvDone, kSiteDrain, kSiteQFull, kSiteLanded,
+  kSiteMerge
 };
 
 __device__ __forceinline__ unsigned long long global_ns() {
@@ -105,6 +107,23 @@ __device__ __forceinline__ bool drain_bar(uint32_t bar, uint32_t parity, unsigne
     }
   }
   return true;
+}
+
+// Bounded wait on a local mbarrier that other CTAs of the cluster arrive on (acquire at cluster
+// scope).  False on timeout or abort.
+__device__ __forceinline__ bool wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                             int32_t site) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (true) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      atomicCAS(&g_device_status, 0, 0x100 | site);
+      return false;
+    }
+  }
 }
 
 // Bounded wait for phase `parity` of mbarrier `bar`.  False on timeout or abort.
@@ -188,7 +207,9 @@ __device__ __forceinline__ void cp_async_wait_0() { asm volatile("cp.async.wait_
 struct ItemInfo {   // written by the index warp, read by every role
   int32_t n_valid, group, kvh, chunk, cols, row0, rows_in_group;
   float v_scale_max;   // FP8 caches: largest |V page scale| over the item's slots
+  int32_t slot0;       // split items: first slot-list entry of this CTA's tile range
 };
+static_assert(2 * sizeof(ItemInfo) <= 2 * 12 * 4, "item records fit their shared-memory slot");
 
 // One butterfly step of a warp reduce-scatter: lanes with bit `o` set keep the upper half of
 // their N values, the others the lower half, and each adds (or maxes in) its partner's copy of
@@ -260,7 +281,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kBPS = kBlocksPerStage;   // gather warps per stage, one per 64-dim block
   constexpr int kSBufs = kLookahead + 1;
   const int slot_cap = UNION ? 0 : p.slot_cap;
-  const SmemLayout L = smem_layout(NP, p.stages, slot_cap, FP8);
+  // Split items (per-token bf16 tiles of at most 32 columns): the CTAs of a cluster share an
+  // item.  FP8 instances are left without the split: its merge code in the softmax warpgroup cost
+  // the FP8 per-token kernel 6 % on full-size calls (measured), through register allocation.
+  constexpr bool kCanSplit = !UNION && !FP8 && NP <= kSplitMaxNPad;
+  const int split = kCanSplit ? p.split : 1;
+  const SmemLayout L = smem_layout(NP, p.stages, slot_cap, FP8, split);
   const int R = p.stages;
 
   // barrier addresses
@@ -275,7 +301,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t b_qempty = b_itemempty + 16;     // Q buffer free (MMA commit, once per item)
   const uint32_t b_qfull = b_qempty + 8;          // Q buffer written (index warp, once per item)
   const uint32_t b_fin = b_qempty + 16;           // MMA issuer drained
-  const uint32_t b_land = b_fin + 8;              // FP8: a block's e4m3 bytes landed [R][2]
+  const uint32_t b_recv = b_fin + 8;              // split: every CTA's partials have arrived
+  const uint32_t b_sendok = b_fin + 16;           // split: every CTA has read this one's partials
+  const uint32_t b_land = b_fin + 24;             // FP8: a block's e4m3 bytes landed [R][2]
 
   ItemInfo* const info = reinterpret_cast<ItemInfo*>(gbase + L.misc);
   float* const red = reinterpret_cast<float*>(gbase + L.misc + 2 * sizeof(ItemInfo));  // [2][4][NP]
@@ -309,6 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(b_qempty, 1);
     mbar_init(b_qfull, 1);
     mbar_init(b_fin, 1);
+    mbar_init(b_recv, 128 * split);     // 128 softmax threads of every CTA of the cluster
+    mbar_init(b_sendok, 128 * split);
     *abort_flag = 0;
     vote[0] = 0;
     vote[1] = 0;
@@ -325,18 +355,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // split items: every CTA's barriers are initialised before any CTA of the cluster can arrive
+  // on them remotely
+  if (split > 1) cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const uint32_t tm_s0 = tmem_base;                 // S^T buffers: columns [b NP, (b+1) NP)
   const uint32_t tm_o = tmem_base + kSBufs * NP;    // O^T halves: the next 2 NP columns
 
   const int64_t n_items = p.n_items;
-  const int64_t stride = gridDim.x;
+  // Per-token items go round robin over the grid's clusters (a cluster is one CTA unless items
+  // are split); every CTA of a cluster takes the same items.
+  const uint32_t crank = split > 1 ? cluster_ctarank() : 0u;
+  const int64_t first_item = static_cast<int64_t>(blockIdx.x) / split;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) / split;
   // Every role ends here and returns, so no code is shared by warpgroups that run with
   // different register counts after the reallocation below.
   auto finish_role = [&]() {
     tc_fence_before();
     __syncthreads();
+    // no CTA of a split cluster leaves while another may still access its shared memory
+    if (split > 1) cluster_sync_all();
   };
 
   if (warp == kIndexWarp) {
@@ -354,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       return k < n_items ? n_items - 1 - k : n_items;
     };
     uint32_t it = 0;
-    for (int64_t item = p.item_counter == nullptr ? static_cast<int64_t>(blockIdx.x) : next_item(0);;
+    for (int64_t item = p.item_counter == nullptr ? first_item : next_item(0);;
          item = next_item(item), ++it) {
       // failure-detection test hook: withhold the first item so every other wait runs out
       if (p.stall_first_item) break;
@@ -398,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint4 qv[kQPre];
 #pragma unroll
       for (int c = 0; c < kQPre; ++c) qv[c] = c < cols ? ldg_nc_v4(q_src(c)) : make_uint4(0u, 0u, 0u, 0u);
-      int32_t nv;
+      int32_t nv, nv_all, slot0 = 0;
       if (!UNION) {
         // Compact the row's valid slots (in order) into the slot list, as tensor-map rows.
         int32_t Lr = p.topk;
@@ -409,8 +448,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             sl_u32, p.n_kv_slots, p.n_kvheads, kvh, p.pad_row, p.pa,
                                             row0, lane);
         nv = n;
+        nv_all = n;
+        if (kCanSplit && split > 1) {
+          // this CTA's contiguous range of the row's 128-slot tiles
+          const int32_t nt_all = (n + kTileTokens - 1) / kTileTokens;
+          const int32_t ta = static_cast<int32_t>(crank) * nt_all / split;
+          const int32_t tb = (static_cast<int32_t>(crank) + 1) * nt_all / split;
+          slot0 = ta * kTileTokens;
+          nv = max(0, min(n, tb * kTileTokens) - slot0);
+        }
       } else {
         nv = p.union_len[group];
+        nv_all = nv;
       }
       // FP8 caches: the largest |V page scale| of the item's slots, for the softmax's per-item
       // normalisation; eight loads per lane in flight, one item ahead of the softmax.
@@ -419,13 +468,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int32_t* sl_b = reinterpret_cast<const int32_t*>(gbase + L.slots) + b * slot_cap;
         const int32_t* ul_b =
             UNION ? p.union_idx + static_cast<int64_t>(group) * p.union_g * p.topk : nullptr;
-        for (int t0 = 0; t0 < nv; t0 += 256) {
+        for (int t0 = 0; t0 < nv_all; t0 += 256) {
           float sc[8];
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             const int t = t0 + 32 * u + lane;
             sc[u] = 0.f;
-            if (t < nv) {
+            if (t < nv_all) {
               const int64_t slot = UNION ? static_cast<int64_t>(ul_b[t])
                                          : div_by(sl_b[t], p.n_kvheads, p.kv_shift);
               sc[u] = fabsf(__ldg(p.v_scale + scale_index(p, slot, kvh)));
@@ -447,6 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         I.row0 = row0;
         I.rows_in_group = rows_in_group;
         I.v_scale_max = vmax;
+        I.slot0 = slot0;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(b_itemfull + 8 * b);
@@ -498,7 +548,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (I.n_valid < 0) break;                // no more items
       const int nv = I.n_valid;
       const int nt = (nv + kTileTokens - 1) / kTileTokens;
-      const int32_t* sl = reinterpret_cast<const int32_t*>(gbase + L.slots) + b * slot_cap;
+      const int32_t* sl = reinterpret_cast<const int32_t*>(gbase + L.slots) + b * slot_cap +
+                          (kCanSplit ? I.slot0 : 0);
       const int32_t* ul =
           UNION ? p.union_idx + static_cast<int64_t>(I.group) * p.union_g * p.topk : nullptr;
       const int n_pieces = 4 * nt;
@@ -797,7 +848,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nv = I.n_valid;
       const int nt = (nv + kTileTokens - 1) / kTileTokens;
       const int cols = I.cols;
-      const int32_t* slots_b = reinterpret_cast<const int32_t*>(gbase + L.slots) + b * slot_cap;
+      const int32_t* slots_b = reinterpret_cast<const int32_t*>(gbase + L.slots) + b * slot_cap +
+                               (kCanSplit ? I.slot0 : 0);
       const int32_t* ul_b =
           UNION ? p.union_idx + static_cast<int64_t>(I.group) * p.union_g * p.topk : nullptr;
       // Column masks: bit c of colmask[u] set when query column c belongs to row u of the group.
@@ -978,59 +1030,139 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       named_bar_sync(1, 128);
-      // Thread t < cols finishes column t once: its row sum, 1 / l, LSE and output offset go to
-      // the other reduction buffer (free: its last readers passed the barrier above), so the
-      // store loop below reads them instead of every thread redoing NP divisions.
-      float* const inv_s = red + (rb ^ 1) * 4 * NP;
-      int64_t* const off_s = reinterpret_cast<int64_t*>(inv_s + NP);
-      const int64_t Hq = p.n_qheads;
-      if (t < cols) {
-        const float l = (rbuf[t] + rbuf[NP + t]) + (rbuf[2 * NP + t] + rbuf[3 * NP + t]);
-        float my_m = NEG_INF;
-#pragma unroll
-        for (int c = 0; c < NP; ++c)
-          if (c == t) my_m = m_used[c];
-        int64_t row, head;
-        if (UNION) {
-          row = I.row0 + t / p.group;
-          head = static_cast<int64_t>(I.kvh) * p.group + t % p.group;
-        } else {
-          row = I.row0;
-          head = static_cast<int64_t>(I.kvh) * p.group + I.chunk * p.chunk_cols + t;
-        }
-        inv_s[t] = l > 0.f ? (FP8 ? ldexpf(1.f / l, v_exp) : 1.f / l) : 0.f;
-        off_s[t] = (row * Hq + head) * kHeadDim;
-        if (p.lse != nullptr) p.lse[row * Hq + head] = l > 0.f ? (my_m + log2f(l)) * kLn2 : NEG_INF;
-      }
-      named_bar_sync(1, 128);
-      rb ^= 1;
-      if (nt > 0) {
-        const uint32_t jl = js + nt - 1;
-        bad |= !wait_bar(b_pvdone + 8 * (jl & 1), (jl >> 1) & 1, abort_flag, kSitePvDone);
-        tc_fence_after();
-      }
       __nv_bfloat16* const outp = reinterpret_cast<__nv_bfloat16*>(p.out);
-      // 16 columns at a time, both 128-dim halves loaded before one wait
+      const int64_t Hq = p.n_qheads;
+      if (kCanSplit && split > 1) {
+        // ---- split item: this CTA holds (m, l, O) over its own tile range.  The partials are
+        // merged by dims: CTA s of the cluster finishes dims [s D, (s + 1) D), D = 256 / split, of
+        // every column, from what every CTA (itself included) sends it through distributed shared
+        // memory.  merge_o[src][dim - s D][column] and merge_ml[src][column] = (m, l) are this
+        // CTA's receive buffers; b_sendok says every CTA has read the previous item's.
+        const int D = kHeadDim / split;
+        constexpr int RF = merge_row_floats(NP);
+        bad |= !wait_cluster(b_sendok, (it & 1) ^ 1, abort_flag, kSiteMerge);
+        if (t < cols) {
+          const float l = (rbuf[t] + rbuf[NP + t]) + (rbuf[2 * NP + t] + rbuf[3 * NP + t]);
+          float my_m = NEG_INF;
 #pragma unroll
-      for (int q = 0; q < NP / 16; ++q) {
-        if (16 * q >= cols) break;
-        float o[2][16];
-        if (nt > 0) {
-          tmem_ld16(tm_o + lane_off + 16 * q, o[0]);
-          tmem_ld16(tm_o + lane_off + NP + 16 * q, o[1]);
-          tc_wait_ld();
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) o[0][i] = o[1][i] = 0.f;
+          for (int c = 0; c < NP; ++c)
+            if (c == t) my_m = m_used[c];
+          const uint32_t ml = base + L.merge_ml + (crank * NP + t) * 8;
+          for (int s = 0; s < split; ++s) st_cluster_v2(cluster_map(ml, s), my_m, l);
         }
+        named_bar_sync(1, 128);   // rbuf is read before the next item's reductions reuse it
+        rb ^= 1;
+        if (nt > 0) {
+          const uint32_t jl = js + nt - 1;
+          bad |= !wait_bar(b_pvdone + 8 * (jl & 1), (jl >> 1) & 1, abort_flag, kSitePvDone);
+          tc_fence_after();
+        }
+        // this thread's dims are t (O^T half 0) and t + 128 (half 1)
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int c = 16 * q + i;
-          if (c < cols) {
-            const float il = inv_s[c];
-            __nv_bfloat16* const dst = outp + off_s[c] + t;
-            dst[0] = __float2bfloat16_rn(o[0][i] * il);
-            dst[128] = __float2bfloat16_rn(o[1][i] * il);
+        for (int q = 0; q < NP / 16; ++q) {
+          if (16 * q >= cols) break;
+          float o[2][16];
+          if (nt > 0) {
+            tmem_ld16(tm_o + lane_off + 16 * q, o[0]);
+            tmem_ld16(tm_o + lane_off + NP + 16 * q, o[1]);
+            tc_wait_ld();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[0][i] = o[1][i] = 0.f;
+          }
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int d = t + 128 * hh;
+            const int s = d / D, dl = d - s * D;
+            const uint32_t dst = cluster_map(
+                base + L.merge_o + ((static_cast<int>(crank) * D + dl) * RF + 16 * q) * 4, s);
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4)
+              st_cluster_v4(dst + 16 * k4, o[hh][4 * k4], o[hh][4 * k4 + 1], o[hh][4 * k4 + 2],
+                            o[hh][4 * k4 + 3]);
+          }
+        }
+        for (int s = 0; s < split; ++s) mbar_arrive_cluster(cluster_map(b_recv, s));
+        bad |= !wait_cluster(b_recv, it & 1, abort_flag, kSiteMerge);
+        const float* const mo = reinterpret_cast<const float*>(gbase + L.merge_o);
+        const float2* const mml = reinterpret_cast<const float2*>(gbase + L.merge_ml);
+        const int tpd = 128 / D;                 // threads per dim: split / 2
+        const int dl = t % D, cg = t / D;
+        for (int c = cg; c < cols; c += tpd) {
+          float M = NEG_INF;
+          for (int s = 0; s < split; ++s) M = fmaxf(M, mml[s * NP + c].x);
+          float lsum = 0.f, acc = 0.f;
+          if (M != NEG_INF) {
+            for (int s = 0; s < split; ++s) {
+              const float2 ml = mml[s * NP + c];
+              const float w = ml.x == NEG_INF ? 0.f : fast_exp2(ml.x - M);
+              lsum += w * ml.y;
+              acc += w * mo[(s * D + dl) * RF + c];
+            }
+          }
+          const float inv = lsum > 0.f ? (FP8 ? ldexpf(1.f / lsum, v_exp) : 1.f / lsum) : 0.f;
+          const int64_t head = static_cast<int64_t>(I.kvh) * p.group + I.chunk * p.chunk_cols + c;
+          const int64_t row = I.row0;
+          outp[(row * Hq + head) * kHeadDim + static_cast<int>(crank) * D + dl] =
+              __float2bfloat16_rn(acc * inv);
+          if (crank == 0 && dl == 0 && p.lse != nullptr)
+            p.lse[row * Hq + head] = lsum > 0.f ? (M + log2f(lsum)) * kLn2 : NEG_INF;
+        }
+        // this thread is done with every CTA's partials in its receive buffers
+        for (int s = 0; s < split; ++s) mbar_arrive_cluster(cluster_map(b_sendok, s));
+      } else {
+        // Thread t < cols finishes column t once: its row sum, 1 / l, LSE and output offset go to
+        // the other reduction buffer (free: its last readers passed the barrier above), so the
+        // store loop below reads them instead of every thread redoing NP divisions.
+        float* const inv_s = red + (rb ^ 1) * 4 * NP;
+        int64_t* const off_s = reinterpret_cast<int64_t*>(inv_s + NP);
+        if (t < cols) {
+          const float l = (rbuf[t] + rbuf[NP + t]) + (rbuf[2 * NP + t] + rbuf[3 * NP + t]);
+          float my_m = NEG_INF;
+#pragma unroll
+          for (int c = 0; c < NP; ++c)
+            if (c == t) my_m = m_used[c];
+          int64_t row, head;
+          if (UNION) {
+            row = I.row0 + t / p.group;
+            head = static_cast<int64_t>(I.kvh) * p.group + t % p.group;
+          } else {
+            row = I.row0;
+            head = static_cast<int64_t>(I.kvh) * p.group + I.chunk * p.chunk_cols + t;
+          }
+          inv_s[t] = l > 0.f ? (FP8 ? ldexpf(1.f / l, v_exp) : 1.f / l) : 0.f;
+          off_s[t] = (row * Hq + head) * kHeadDim;
+          if (p.lse != nullptr) p.lse[row * Hq + head] = l > 0.f ? (my_m + log2f(l)) * kLn2 : NEG_INF;
+        }
+        named_bar_sync(1, 128);
+        rb ^= 1;
+        if (nt > 0) {
+          const uint32_t jl = js + nt - 1;
+          bad |= !wait_bar(b_pvdone + 8 * (jl & 1), (jl >> 1) & 1, abort_flag, kSitePvDone);
+          tc_fence_after();
+        }
+        // 16 columns at a time, both 128-dim halves loaded before one wait
+#pragma unroll
+        for (int q = 0; q < NP / 16; ++q) {
+          if (16 * q >= cols) break;
+          float o[2][16];
+          if (nt > 0) {
+            tmem_ld16(tm_o + lane_off + 16 * q, o[0]);
+            tmem_ld16(tm_o + lane_off + NP + 16 * q, o[1]);
+            tc_wait_ld();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[0][i] = o[1][i] = 0.f;
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int c = 16 * q + i;
+            if (c < cols) {
+              const float il = inv_s[c];
+              __nv_bfloat16* const dst = outp + off_s[c] + t;
+              dst[0] = __float2bfloat16_rn(o[0][i] * il);
+              dst[128] = __float2bfloat16_rn(o[1][i] * il);
+            }
           }
         }
       }
@@ -1115,7 +1247,37 @@ cudaError_t launch_np(const CUtensorMap& tk, const CUtensorMap& tv, const Prefil
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) opted_in[dev].store(g.smem_bytes);
   }
-  kern<<<g.grid, kThreads, g.smem_bytes, stream>>>(tk, tv, p);
+  if (g.split <= 1) {
+    kern<<<g.grid, kThreads, g.smem_bytes, stream>>>(tk, tv, p);
+    return cudaGetLastError();
+  }
+  // Split items: clusters of g.split CTAs (one per SM).  Fewer clusters may fit at once than the
+  // SM count suggests (a cluster's CTAs share one GPC), so the grid is capped at the clusters that
+  // can be resident together, looked up once per device and shape.
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(g.split);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(g.smem_bytes);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  static std::atomic<int> max_clusters[64][kMaxSplit + 1];
+  int fit = dev >= 0 && dev < 64 ? max_clusters[dev][g.split].load() : 0;
+  if (fit <= 0) {
+    cfg.gridDim = dim3(static_cast<unsigned>(g.grid));
+    e = cudaOccupancyMaxActiveClusters(&fit, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (fit <= 0) return cudaErrorInvalidConfiguration;
+    if (dev >= 0 && dev < 64) max_clusters[dev][g.split].store(fit);
+  }
+  const int clusters = std::min(g.grid / g.split, fit);
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * g.split));
+  e = cudaLaunchKernelEx(&cfg, kern, tk, tv, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -178,6 +178,13 @@ def make_group12(seed: int = 2, n_rows: int = 8192, context: int = 131072,
                       f"group12_128k_{n_qheads}q{n_kvheads}kv")
 
 
+def make_rows(n_rows: int, seed: int = 9) -> Workload:
+    """Query-count sweep point: ``n_rows`` rows at the end of an 8192-token context (the rest a
+    prefix), group 6, topk 2051, so every row streams the full budget ("[QSA] Tune sm120 sparse
+    prefill geometry", Query-count sweep)."""
+    return make_chunk(n_rows, 8192, 6, 1, 2051, seed + n_rows, f"rows{n_rows}_8k")
+
+
 def make_union(seed: int = 3, n_rows: int = 8192, topk: int = 2048) -> Workload:
     """Prefill of n_rows tokens from position 0, 8 Q / 1 KV, topk 2048, random-walk indices."""
     rng = np.random.default_rng(seed)
@@ -329,6 +336,9 @@ CONFIGS = {
     "mla_4k": lambda seed=6: make_mla(seed, n_rows=4096, name="mla_4k"),
     "mla_2k": lambda seed=7: make_mla(seed, n_rows=2048, name="mla_2k"),
 }
+# query-count sweep at KV 8192
+for _r in (32, 64, 128, 256, 512, 1024):
+    CONFIGS[f"rows{_r}_8k"] = (lambda r: (lambda seed=9: make_rows(r, seed)))(_r)
 
 
 def make(name: str, **kw) -> Workload:
