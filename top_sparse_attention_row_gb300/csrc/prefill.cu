@@ -719,6 +719,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // running pointer (pair index, parity) replaces per-piece divisions by the stage count,
     // which sat on the issue path (measured: ~4 % of group6_32k, ~18 % with the gather removed).
     const uint32_t n_pairs = static_cast<uint32_t>(R) / 2;
+    // Operand descriptors as a per-buffer low word plus a constant offset (one add per operand).
+    constexpr uint32_t kHi = sw128_desc_hi(1024);
+    const uint32_t q_lo = sw128_desc_lo(base + L.qbuf, 16);
+    const uint32_t ring_k_lo = sw128_desc_lo(base + L.ring, 16);          // K-major stage reads
+    const uint32_t ring_v_lo = sw128_desc_lo(base + L.ring, 16384);       // MN-major stage reads
+    const uint32_t pbuf_lo = sw128_desc_lo(base + L.pbuf, 16);
     uint32_t c_pair = 0, c_par = 0;
     auto advance = [&]() {
       if (++c_pair == n_pairs) {
@@ -737,7 +743,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nt = (nv + kTileTokens - 1) / kTileTokens;
       __syncwarp();
       if (lane == 0) mbar_arrive(b_itemempty + 8 * b);
-      const uint32_t qaddr = base + L.qbuf;
       if (!__all_sync(0xffffffffu, wait_bar(b_qfull, it & 1, abort_flag, kSiteQFull))) {
         aborted = true;
         break;
@@ -760,15 +765,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the async proxy, and the FP8 rewrite fences on the writer side
           if (cp_engine) fence_proxy_async_smem();
           if (lane == 0) {
-            const uint32_t klo = base + L.ring + st_lo * kStageBytes;
-            const uint32_t khi = base + L.ring + st_hi * kStageBytes;
+            const uint32_t k_lo = ring_k_lo + st_lo * (kStageBytes >> 4);   // stages st_lo, st_hi
 #pragma unroll
             for (int kk = 0; kk < 16; ++kk) {
-              const uint32_t kst = kk < 8 ? klo : khi;
               const int kq = kk & 7;
-              const uint64_t a = sw128_desc(kst + (kq >> 2) * 16384 + (kq & 3) * 32, 16, 1024);
-              const uint64_t bq = sw128_desc(qaddr + (kk >> 2) * (NP * 128) + (kk & 3) * 32, 16, 1024);
-              tc_mma(tm_s0 + sb * NP, a, bq, kIdescQK, kk > 0 ? 1u : 0u);
+              const uint32_t a_off = (kk < 8 ? 0u : static_cast<uint32_t>(kStageBytes)) +
+                                     (kq >> 2) * 16384 + (kq & 3) * 32;
+              const uint32_t b_off = (kk >> 2) * (NP * 128) + (kk & 3) * 32;
+              tc_mma_w(tm_s0 + sb * NP, k_lo + (a_off >> 4), kHi, q_lo + (b_off >> 4), kHi, kIdescQK,
+                       kk > 0 ? 1u : 0u);
             }
             tc_commit(b_empty + 8 * e_pair);   // one commit frees the stage pair
             tc_commit(b_sfull + 8 * sb);
@@ -794,15 +799,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the async proxy, and the FP8 rewrite fences on the writer side
           if (cp_engine) fence_proxy_async_smem();
           if (lane == 0) {
-            const uint32_t pbase = base + L.pbuf + pb * L.p_bytes;
+            const uint32_t v_lo = ring_v_lo + st_vlo * (kStageBytes >> 4);   // stages st_vlo, st_vhi
+            const uint32_t p_lo = pbuf_lo + pb * (static_cast<uint32_t>(L.p_bytes) >> 4);
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-              const uint32_t vst = base + L.ring + (hh ? st_vhi : st_vlo) * kStageBytes;
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t a = sw128_desc(vst + kk * 2048, 16384, 1024);
-                const uint64_t bp = sw128_desc(pbase + (kk >> 2) * (NP * 128) + (kk & 3) * 32, 16, 1024);
-                tc_mma(tm_o + hh * NP, a, bp, kIdescPV, (jp == 0 && kk == 0) ? 0u : 1u);
+                const uint32_t a_off = hh * kStageBytes + kk * 2048;
+                const uint32_t b_off = (kk >> 2) * (NP * 128) + (kk & 3) * 32;
+                tc_mma_w(tm_o + hh * NP, v_lo + (a_off >> 4), kHi, p_lo + (b_off >> 4), kHi, kIdescPV,
+                         (jp == 0 && kk == 0) ? 0u : 1u);
               }
             }
             tc_commit(b_empty + 8 * e_pair);

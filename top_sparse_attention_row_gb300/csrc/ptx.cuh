@@ -163,6 +163,29 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
   return d;
 }
 
+// The same descriptor as two 32-bit words.  The low word holds the start address (>> 4) and the
+// leading byte offset, the high word the stride byte offset, the descriptor version and the
+// 128-byte swizzle.  Operands inside one buffer differ only in the address field, which never
+// carries out of its 14 bits (shared-memory addresses are below 2^18), so the descriptor of
+// buffer + off is the buffer's low word + (off >> 4): one add per MMA operand on the issue path.
+__host__ __device__ constexpr uint32_t sw128_desc_hi(uint32_t sbo) {
+  return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+__device__ __forceinline__ uint32_t sw128_desc_lo(uint32_t saddr, uint32_t lbo) {
+  return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
+}
+__device__ __forceinline__ void tc_mma_w(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                         uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "mov.b64 da, {%1, %2};\n\t"
+      "mov.b64 db, {%3, %4};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Named barrier `id` over `n` threads that also ORs a predicate across them: every participant
 // gets true when any passed true (a uniform decision).
 __device__ __forceinline__ bool named_bar_any(uint32_t id, uint32_t n, bool pred) {
