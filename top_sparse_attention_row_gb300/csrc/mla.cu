@@ -413,14 +413,21 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     // issue path.
     RingPos qk_pos, pv_pos;
     auto lstage = [&](uint32_t st) { return base + L.pairs + st * kStageBytes; };
+    // Operand descriptors as a per-buffer low word plus a constant offset: one add per operand
+    // on the issue path (sw128_desc_lo / sw128_desc_hi).
+    constexpr uint32_t kHi = sw128_desc_hi(1024);
+    const uint32_t q_lo = sw128_desc_lo(qaddr, 16);
+    const uint32_t rope_lo = sw128_desc_lo(rope_addr, 16);
     // S^T(sbuf) += latent chunk c (dims 128c .. 128c+127) of the tile held in `st_addr`
     auto qk_chunk = [&](uint32_t sb, int c, uint32_t st_addr, bool first) {
+      const uint32_t a_lo = sw128_desc_lo(st_addr, 16);
 #pragma unroll
       for (int kq = 0; kq < 8; ++kq) {
         const int g = 8 * c + kq;
-        const uint64_t a = sw128_desc(st_addr + (kq >> 2) * 16384 + (kq & 3) * 32, 16, 1024);
-        const uint64_t bq = sw128_desc(qaddr + (g >> 2) * (NP * 128) + (g & 3) * 32, 16, 1024);
-        tc_mma(tm_s0 + sb * NP, a, bq, kIdescQK, (first && kq == 0) ? 0u : 1u);
+        const uint32_t a_off = (kq >> 2) * 16384 + (kq & 3) * 32;
+        const uint32_t b_off = (g >> 2) * (NP * 128) + (g & 3) * 32;
+        tc_mma_w(tm_s0 + sb * NP, a_lo + (a_off >> 4), kHi, q_lo + (b_off >> 4), kHi, kIdescQK,
+                 (first && kq == 0) ? 0u : 1u);
       }
     };
     // S^T(sbuf) += rope dims 512 .. 575
@@ -428,18 +435,20 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
 #pragma unroll
       for (int kq = 0; kq < 4; ++kq) {
         const int g = 32 + kq;
-        const uint64_t a = sw128_desc(rope_addr + kq * 32, 16, 1024);
-        const uint64_t bq = sw128_desc(qaddr + (g >> 2) * (NP * 128) + (g & 3) * 32, 16, 1024);
-        tc_mma(tm_s0 + sb * NP, a, bq, kIdescQK, (first && kq == 0) ? 0u : 1u);
+        const uint32_t b_off = (g >> 2) * (NP * 128) + (g & 3) * 32;
+        tc_mma_w(tm_s0 + sb * NP, rope_lo + ((kq * 32) >> 4), kHi, q_lo + (b_off >> 4), kHi,
+                 kIdescQK, (first && kq == 0) ? 0u : 1u);
       }
     };
     // O^T chunk c += V^T(chunk c of the tile in st_addr) . P^T(pbuf)
     auto pv_chunk = [&](int c, uint32_t st_addr, uint32_t pbase, bool first) {
+      const uint32_t a_lo = sw128_desc_lo(st_addr, 16384);
+      const uint32_t p_lo = sw128_desc_lo(pbase, 16);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
-        const uint64_t a = sw128_desc(st_addr + kk * 2048, 16384, 1024);
-        const uint64_t bp = sw128_desc(pbase + (kk >> 2) * (NP * 128) + (kk & 3) * 32, 16, 1024);
-        tc_mma(tm_o + c * NP, a, bp, kIdescPV, (first && kk == 0) ? 0u : 1u);
+        const uint32_t b_off = (kk >> 2) * (NP * 128) + (kk & 3) * 32;
+        tc_mma_w(tm_o + c * NP, a_lo + ((kk * 2048) >> 4), kHi, p_lo + (b_off >> 4), kHi, kIdescPV,
+                 (first && kk == 0) ? 0u : 1u);
       }
     };
     for (;; ++it) {
