@@ -492,7 +492,7 @@ def mla_case(seed, S=40, R=14, H=4, Dqk=12, Dv=8):
 
 def check_mla_dense(fn):
     """Whole-prefix selection equals dense causal attention with keys = the full latent row and
-    values = its first d_v dims (torch's math attention; LSE by torch.logsumexp)."""
+    values = its first d_v dims (torch's math attention; LSE by scipy's logsumexp)."""
     fails = []
     for seed, (H, Dqk, Dv) in enumerate([(4, 12, 8), (1, 9, 9), (3, 16, 5)]):
         q, kv, idx, pos, Dv = mla_case(400 + seed, H=H, Dqk=Dqk, Dv=Dv)
@@ -505,9 +505,13 @@ def check_mla_dense(fn):
         mask = torch.where(keypos <= torch.from_numpy(pos)[:, None], 0.0, float("-inf")).double()
         out = torch.ops.aten._scaled_dot_product_attention_math(tq, tk, tv, attn_mask=mask,
                                                                 scale=scale)[0]
-        lse = torch.logsumexp(scale * tq @ tk.transpose(-1, -2) + mask, dim=-1)
+        # LSE from scipy over the masked logits (numpy float64): torch.logsumexp here was seen to
+        # miss the float64 value by ~6e-10 in some runs of the suite, which is above this pin's
+        # 1e-10 bound and not an error of the oracle.
+        logits = scale * np.einsum("rhd,sd->hrs", q, kv)
+        logits = np.where(np.arange(kv.shape[0])[None, None, :] <= pos[None, :, None], logits, -np.inf)
         Od = out[0].permute(1, 0, 2).numpy()
-        Ld = lse[0].permute(1, 0).numpy()
+        Ld = logsumexp(logits, axis=-1).T
         if not (_close(O, Od, 1e-10) and _close(L, Ld, 1e-10)):
             fails.append(f"MLA dense mismatch (H={H}, d_qk={Dqk}, d_v={Dv})")
     return fails
