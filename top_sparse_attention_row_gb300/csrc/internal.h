@@ -22,8 +22,9 @@ constexpr int kIndexWarp = 5;                // slot compaction, Q tile, item in
 constexpr int kProducerWarp0 = 6;            // first gather warp
 // d=256 kernel: each 32 KiB stage is filled by two gather warps, one per 64-dim block (a warp
 // issues TMA gathers one after another at ~13 GB/s, so two warps land a stage in half the time).
-// 20 warps = five warpgroups: softmax (0-3); MMA and index warps and two idle ones (4-7); twelve
-// gather warps (8-19), whose spare registers go to the softmax warpgroup (setmaxnreg).
+// 20 warps = five warpgroups: softmax (0-3); MMA and index warps and two gather warps (4-7); ten
+// gather warps and two idle ones (8-19), whose spare registers go to the softmax warpgroup
+// (setmaxnreg).
 constexpr int kBlocksPerStage = 2;
 constexpr int kMaxStages = 6;
 constexpr int kGatherWarp0 = 8;
@@ -37,6 +38,19 @@ static_assert(kGatherWarp0 + kProducerWarps == kThreads / 32 && kGatherWarp0 % 4
               "gather warps fill whole warpgroups at the end of the CTA");
 static_assert(128 * kSoftmaxRegs + 128 * kRoleRegs + 384 * kGatherRegs <= kThreads * kLaunchRegs,
               "register split within the launch's registers");
+// A warp's SM sub-partition (scheduler) is its index mod 4.  The MMA warp (4) issues measurably
+// slower while gather warps share its sub-partition (their TMA request streams compete with its
+// MMA issue), so in the d=256 kernel two of sub-partition 0's gather slots (warps 8 and 12) stay
+// idle and warps 6 and 7 of warpgroup 1 gather in their place; sub-partition 0 keeps one gather
+// warp (16).  Measured on GB300: group6_32k 1.639 -> 1.532 ms, union_8k G = 4 0.515 -> 0.502.
+__host__ __device__ constexpr bool is_gather_warp(int warp) {
+  return warp == 6 || warp == 7 || (warp >= kGatherWarp0 && warp != 8 && warp != 12);
+}
+// index of gather warp `warp` in 0 .. kProducerWarps - 1: stage index / kBlocksPerStage, block
+// index % kBlocksPerStage (warps 6 and 7 take the idle slots' indices)
+__host__ __device__ constexpr int gather_index(int warp) {
+  return warp == 6 ? 8 - kGatherWarp0 : warp == 7 ? 12 - kGatherWarp0 : warp - kGatherWarp0;
+}
 // MLA kernel: the same 20-warp layout and register split; gather warps 8-17 share every latent
 // piece and warps 18-19 every rope piece.
 constexpr int kMlaLatentWarps = 10;

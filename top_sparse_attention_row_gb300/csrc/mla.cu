@@ -22,7 +22,8 @@
 //    a tenth of the time one warp would take; two more share the rope pieces.  Padding rows use
 //    a row past the tensor map, which TMA zero-fills.
 //  * 20 warps (five warpgroups) with warpgroup register reallocation, as in the d=256 kernel:
-//    softmax (0-3), MMA and index (4-5, with two idle warps), gather (8-19).
+//    softmax (0-3), MMA and index (4-5), gather (6, 7, 9-11, 13-19; 8 and 12 idle so that the
+//    MMA warp's sub-partition holds one gather warp).
 //  * Online softmax, epilogue, union masks, bounded waits and failure containment follow the
 //    d=256 kernel.
 #include <cuda.h>
@@ -287,16 +288,22 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     }
     finish_role();
     return;
-  } else if (warp >= kGatherWarp0) {
-    regs_dec<kGatherRegs>();
+  } else if (warp >= kGatherWarp0 || is_gather_warp(warp)) {
     // ------------------------------------------------------------ gather producers
+    // Warps 6 and 7 gather at warpgroup 1's register count and warps 8 and 12 stay idle, so the
+    // MMA warp's sub-partition keeps one gather warp (the same layout as the d=256 kernel).
+    if (warp >= kGatherWarp0) regs_dec<kGatherRegs>(); else regs_inc<kRoleRegs>();
+    if (!is_gather_warp(warp)) {
+      finish_role();
+      return;
+    }
     // Gather warps 0-9 share every latent piece: gather4 op o = 32a + lane (o < 64; atom a,
     // slots 4*lane .. 4*lane+3) is issued by warp o % 10, and each warp arms the stage's barrier
     // with its own share of the bytes.  A warp's gather instructions issue one after another
     // (~40 ns each on GB300), and here a freed stage is on the critical path -- the next tile's
     // QK^T waits for it -- so many warps filling it together beat one owner per stage (five
     // warps: mla_8k 4.30 -> 3.61 ms).  Warps 10 and 11 share every rope piece the same way.
-    const int pw = warp - kGatherWarp0;
+    const int pw = gather_index(warp);
     const int rw = pw - kMlaPairOwners;   // rope warp index (>= 0 for the rope warps)
     const uint32_t share_bytes =
         pw < kMlaPairOwners
@@ -791,9 +798,7 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     finish_role();
     return;
   }
-  // warps 6 and 7 have no role; they take part in their warpgroup's register reallocation
-  regs_inc<kRoleRegs>();
-  finish_role();
+  // every warp of the CTA has returned from its role above
 }
 
 namespace {

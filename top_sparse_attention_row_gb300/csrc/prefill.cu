@@ -39,8 +39,10 @@
 //    the row sum use the same stale max.
 //  * Warp roles (20 warps, five warpgroups): 0-3 softmax + epilogue; 4 MMA issue + tensor-memory
 //    owner; 5 index/Q loader (per-token: compacts the row's valid slots into shared memory);
-//    6-7 idle; 8-19 gather, two per stage.  Warpgroup register reallocation (setmaxnreg) moves
-//    registers from the gather warpgroups to the softmax and MMA/index warpgroups.
+//    6, 7, 9-11, 13-19 gather, two per stage; 8 and 12 idle, so that the MMA warp's SM
+//    sub-partition (warp index mod 4) has one gather warp instead of three.  Warpgroup register
+//    reallocation (setmaxnreg) moves registers from the gather warpgroups to the softmax and
+//    MMA/index warpgroups.
 //  * Every mbarrier wait is bounded (~2 s); a timeout records a code in a device status word,
 //    all roles leave their loops, in-flight copies and MMAs are drained, tensor memory is
 //    freed and the kernel returns.
@@ -518,11 +520,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     finish_role();
     return;
-  } else if (warp >= kGatherWarp0) {
+  } else if (warp >= kGatherWarp0 || is_gather_warp(warp)) {
     // ------------------------------------------------------------ gather producers
-    // Warpgroups 2-4 run only this role: they give registers back to the CTA's pool for the
-    // softmax warpgroup (warpgroup register reallocation).
-    regs_dec<kGatherRegs>();
+    // Warpgroups 2-4 give registers back to the CTA's pool for the softmax warpgroup (warpgroup
+    // register reallocation); warps 6 and 7 gather at warpgroup 1's count, and warps 8 and 12
+    // stay idle so that the MMA warp's sub-partition keeps a single gather warp.
+    if (warp >= kGatherWarp0) regs_dec<kGatherRegs>(); else regs_inc<kRoleRegs>();
+    if (!is_gather_warp(warp)) {
+      finish_role();
+      return;
+    }
     // Stage st is filled by warps 2 st and 2 st + 1, each gathering one 64-dim block of every
     // piece that lands on it (32 TMA gather4, one per lane, or 32 cp.async of four slots x 16
     // bytes per lane), in order.  Every piece's two halves are issued at once by two warps, and
@@ -530,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // took ~2.3 us to issue, and a V tile's pieces -- which reuse the stages of the same tile's
     // K, freed only when its QK^T completes -- were the wait of every P.V.)  FP8 pieces are
     // gathered and rewritten whole by the stage's first warp.
-    const int pw = warp - kGatherWarp0;
+    const int pw = gather_index(warp);
     const uint32_t st = static_cast<uint32_t>(pw / kBPS);   // this warp's stage
     const int blk = pw % kBPS;                              // and first 64-dim block
     const bool tma = p.gather_tma != 0;
@@ -1179,9 +1186,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     finish_role();
     return;
   }
-  // warps 6 and 7 have no role; they take part in their warpgroup's register reallocation
-  regs_inc<kRoleRegs>();
-  finish_role();
+  // every warp of the CTA has returned from its role above
 }
 
 // ---------------------------------------------------------------------------- host side
