@@ -380,9 +380,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (split > 1) cluster_sync_all();
   };
 
-  if (warp == kIndexWarp) {
+  // Per-token bf16 tiles of N = 16 (the group-6 and group-12 shapes) move the index warp to warp
+  // 16 and let warp 5 gather: the MMA warp's sub-partition then holds no gather warp.  Its 64
+  // registers hold Q rows for 8 columns ahead instead of 16; wider instances spill there and keep
+  // the index warp on warp 5 (measured on GB300: group6_32k 1.539 -> 1.506 ms; union G = 4
+  // 0.501 -> 0.595 ms with the move).
+  constexpr bool kIdxSub0 = !UNION && !FP8 && NP == 16;
+  constexpr int kIdxWarp = kIdxSub0 ? 16 : kIndexWarp;
+  if (warp == kIdxWarp) {
     // ------------------------------------------------------------ index / Q loader
-    regs_inc<kRoleRegs>();
+    if constexpr (kIdxSub0) regs_dec<kGatherRegs>(); else regs_inc<kRoleRegs>();
     // Items: a static round robin over the grid, or (union mode) taken from a global counter in
     // reverse order -- the later row groups of a prefill have the longest union lists, so the
     // long items go first and the short ones even out the CTAs' finishing times.  After the
@@ -435,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return p.q + (row * p.n_qheads + head) * kHeadDim + lane * 8;
       };
-      constexpr int kQPre = NP < 16 ? NP : 16;
+      constexpr int kQPre = kIdxSub0 ? 8 : (NP < 16 ? NP : 16);
       uint4 qv[kQPre];
 #pragma unroll
       for (int c = 0; c < kQPre; ++c) qv[c] = c < cols ? ldg_nc_v4(q_src(c)) : make_uint4(0u, 0u, 0u, 0u);
@@ -520,13 +527,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     finish_role();
     return;
-  } else if (warp >= kGatherWarp0 || is_gather_warp(warp)) {
+  } else if (warp >= kGatherWarp0 || warp == 6 || warp == 7 || (kIdxSub0 && warp == kIndexWarp)) {
     // ------------------------------------------------------------ gather producers
     // Warpgroups 2-4 give registers back to the CTA's pool for the softmax warpgroup (warpgroup
     // register reallocation); warps 6 and 7 gather at warpgroup 1's count, and warps 8 and 12
     // stay idle so that the MMA warp's sub-partition keeps a single gather warp.
     if (warp >= kGatherWarp0) regs_dec<kGatherRegs>(); else regs_inc<kRoleRegs>();
-    if (!is_gather_warp(warp)) {
+    if (warp == 8 || warp == 12) {   // idle
       finish_role();
       return;
     }
@@ -537,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // took ~2.3 us to issue, and a V tile's pieces -- which reuse the stages of the same tile's
     // K, freed only when its QK^T completes -- were the wait of every P.V.)  FP8 pieces are
     // gathered and rewritten whole by the stage's first warp.
-    const int pw = gather_index(warp);
+    const int pw = (kIdxSub0 && warp == kIndexWarp) ? kIdxWarp - kGatherWarp0 : gather_index(warp);
     const uint32_t st = static_cast<uint32_t>(pw / kBPS);   // this warp's stage
     const int blk = pw % kBPS;                              // and first 64-dim block
     const bool tma = p.gather_tma != 0;
