@@ -269,7 +269,9 @@ __device__ __forceinline__ void decode_item(const PrefillParams& p, int64_t item
 
 }  // namespace
 
-template <int NP, bool UNION, bool FP8>
+// SC: query columns the softmax computes (SC < NP when an item's real columns fit in SC; the MMA
+// still runs N = NP, and P's columns past SC stay zero).
+template <int NP, bool UNION, bool FP8, int SC>
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_prefill_kernel(const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV,
@@ -850,6 +852,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ softmax + epilogue (warps 0-3)
     regs_inc<kSoftmaxRegs>();   // the registers warpgroups 2-4 returned
     const int t = threadIdx.x;                       // tensor-memory lane = slot within tile
+    if constexpr (SC < NP) {
+      // P columns SC .. NP-1 are never written: zero both P buffers once (the MMA reads them)
+      for (int i = t; i < 2 * L.p_bytes / 16; i += 128) sts_v4(base + L.pbuf + 16 * i, make_uint4(0u, 0u, 0u, 0u));
+      fence_proxy_async_smem();
+    }
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     uint32_t js = 0, it = 0, rb = 0;
     bool bad = false;
@@ -947,6 +954,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool need = false;
 #pragma unroll
         for (int c = 0; c < NP; ++c) {
+          if (c >= SC) {   // no real column past SC: P stays zero there
+            x[c] = NEG_INF;
+            continue;
+          }
           x[c] = ((vmask >> c) & 1ull) ? x[c] * logit_scale : NEG_INF;
           need |= x[c] > m_used[c] + kRescaleThreshold;
         }
@@ -1021,7 +1032,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* prow = pbuf + (t >> 6) * (NP * 128) + ((t & 7) << 1);
         const int tchunk = (t & 63) >> 3;
 #pragma unroll
-        for (int c = 0; c < NP; ++c) {
+        for (int c = 0; c < SC; ++c) {
           const float pv = x[c] == NEG_INF ? 0.f : fast_exp2(x[c] - m_used[c]);
           l_part[c] += pv;
           uint8_t* const dst = prow + (c >> 3) * 1024 + (c & 7) * 128 + ((tchunk ^ (c & 7)) << 4);
@@ -1250,10 +1261,10 @@ cudaError_t make_cache_map_e4m3(CUtensorMap* m, const void* cache, int64_t rows)
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int NP, bool UNION, bool FP8>
+template <int NP, bool UNION, bool FP8, int SC = NP>
 cudaError_t launch_np(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
                       const Geometry& g, cudaStream_t stream) {
-  auto kern = sparse_prefill_kernel<NP, UNION, FP8>;
+  auto kern = sparse_prefill_kernel<NP, UNION, FP8, SC>;
   // The shared-memory opt-in is set once per device and size, so calls made while a stream
   // is being captured into a CUDA graph only enqueue the launch.
   static std::atomic<int> opted_in[64];
@@ -1315,13 +1326,17 @@ cudaError_t launch_prefill(const PrefillParams& p, const Geometry& g, const void
   const bool u = p.union_g > 1;
   if (fp8) {
     switch (g.np) {
-      case 16: return u ? launch_np<16, true, true>(tk, tv, p, g, stream) : launch_np<16, false, true>(tk, tv, p, g, stream);
+      case 16: return u ? launch_np<16, true, true>(tk, tv, p, g, stream)
+                        : (g.cols <= 8 ? launch_np<16, false, true, 8>(tk, tv, p, g, stream)
+                                       : launch_np<16, false, true>(tk, tv, p, g, stream));
       case 32: return u ? launch_np<32, true, true>(tk, tv, p, g, stream) : launch_np<32, false, true>(tk, tv, p, g, stream);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (g.np) {
-    case 16: return u ? launch_np<16, true, false>(tk, tv, p, g, stream) : launch_np<16, false, false>(tk, tv, p, g, stream);
+    case 16: return u ? launch_np<16, true, false>(tk, tv, p, g, stream)
+                      : (g.cols <= 8 ? launch_np<16, false, false, 8>(tk, tv, p, g, stream)
+                                     : launch_np<16, false, false>(tk, tv, p, g, stream));
     case 32: return u ? launch_np<32, true, false>(tk, tv, p, g, stream) : launch_np<32, false, false>(tk, tv, p, g, stream);
     case 48: return u ? launch_np<48, true, false>(tk, tv, p, g, stream) : launch_np<48, false, false>(tk, tv, p, g, stream);
     case 64: return u ? launch_np<64, true, false>(tk, tv, p, g, stream) : launch_np<64, false, false>(tk, tv, p, g, stream);
