@@ -382,12 +382,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (split > 1) cluster_sync_all();
   };
 
-  // Per-token bf16 tiles of N = 16 (the group-6 and group-12 shapes) move the index warp to warp
-  // 16 and let warp 5 gather: the MMA warp's sub-partition then holds no gather warp.  Its 64
+  // Per-token tiles of N = 16 (the group-6 and group-12 shapes) move the index warp to warp 16
+  // and let warp 5 gather: the MMA warp's sub-partition then holds no gather warp.  Its 64
   // registers hold Q rows for 8 columns ahead instead of 16; wider instances spill there and keep
-  // the index warp on warp 5 (measured on GB300: group6_32k 1.539 -> 1.506 ms; union G = 4
-  // 0.501 -> 0.595 ms with the move).
-  constexpr bool kIdxSub0 = !UNION && !FP8 && NP == 16;
+  // the index warp on warp 5 (measured on GB300: group6_32k 1.539 -> 1.506 ms, FP8 1.874 ->
+  // 1.592 ms; union G = 4 0.501 -> 0.595 ms with the move).
+  constexpr bool kIdxSub0 = !UNION && NP == 16;
   constexpr int kIdxWarp = kIdxSub0 ? 16 : kIndexWarp;
   if (warp == kIdxWarp) {
     // ------------------------------------------------------------ index / Q loader
