@@ -181,6 +181,22 @@ qsa_status qsa_sparse_prefill_fp8(const void* q, const void* k_cache, const void
                                   int32_t head_dim, int32_t topk, float scale, int32_t union_g,
                                   int64_t n_kv_slots, void* stream);
 
+/* FP8 caches over a paged pool: qsa_sparse_prefill_fp8's e4m3 caches and scales with
+ * qsa_sparse_prefill_paged's logical indices, translated in the kernels ("DSA prefill ...
+ * triton_sparse_mla", Robustness and Accuracy Tests: the served FP8 KV pool is paged).  The
+ * scale of a physical slot s is k_scale[(s / fp8_page_size) * n_kvheads + h] (v_scale likewise),
+ * fp8_page_size being the scale granularity and page_size the paging of the pool; everything
+ * else as qsa_sparse_prefill_paged and qsa_sparse_prefill_fp8. */
+qsa_status qsa_sparse_prefill_fp8_paged(const void* q, const void* k_cache, const void* v_cache,
+                                        const float* k_scale, const float* v_scale,
+                                        int32_t fp8_page_size, const int32_t* indices,
+                                        const int32_t* topk_len, const int32_t* cu_seqlens_q,
+                                        const int32_t* kv_lens, const int32_t* page_table,
+                                        void* out, float* lse, int64_t n_rows, int32_t n_requests,
+                                        int32_t pages_per_req, int32_t page_size, int64_t n_pages,
+                                        int32_t n_qheads, int32_t n_kvheads, int32_t head_dim,
+                                        int32_t topk, float scale, int32_t union_g, void* stream);
+
 /* MLA-shaped sparse prefill ("DSA prefill ... triton_sparse_mla", Motivation and Speed Tests:
  * one latent KV row per token, kv_lora_rank 512 + qk_rope_head_dim 64 = 576 dims for QK^T, the
  * 512 latent dims as V, topk 2048, 8 heads at TP8, union G = 2 / 4).  Every query head attends

@@ -120,3 +120,30 @@ def test_fp8_mixed_page_scale_magnitudes(B):
         dO, dL, mism = compare(out, lse, O, L)
         bound = 2e-2 * max(1.0, float(np.abs(O).max()))
         assert mism == 0 and dO <= bound and dL <= LSE_RTOL, (G, dO, bound, dL, mism)
+
+
+@pytest.mark.parametrize("G", [0, 4])
+def test_fp8_paged_matches_oracle_and_plain_fp8_entry(B, G):
+    """FP8 caches over a paged pool: logical indices translated in the kernels, e4m3 scales by
+    physical slot.  Against the FP8 oracle on the batch's physical slots, and bit for bit against
+    the plain FP8 entry given those slots (both compact the same slots in the same order)."""
+    import torch
+    w = W.make_mixed(new_tokens=(64, 200, 130, 300), prefixes=(0, 3000, 700, 5000), page_size=64)
+    w = W.with_fp8_cache(w, 16)                  # scale pages of 16 slots, pool pages of 64
+    m = w.meta
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+    q, _, _, idx, tl = to_device(w)
+    out, lse = B.sparse_prefill_fp8_paged(q, t(m["k8"]), t(m["v8"]), t(m["k_scale"]), t(m["v_scale"]),
+                                          16, i32(m["logical_indices"]), tl, i32(m["cu_seqlens_q"]),
+                                          i32(m["kv_lens_array"]), i32(m["page_table"]), 64, w.scale,
+                                          n_pages=m["n_pages"], union_g=G)
+    torch.cuda.synchronize()
+    assert B.device_status() == 0
+    O, L = ref(w)
+    assert_parity(out, lse, O, L, what=f"fp8 paged G={G}")
+    out2, lse2 = B.sparse_prefill_fp8(q, t(m["k8"]), t(m["v8"]), t(m["k_scale"]), t(m["v_scale"]),
+                                      16, idx, tl, w.scale, union_g=G)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse, lse2)

@@ -26,7 +26,8 @@ EXPORTED = ["qsa_sparse_prefill", "qsa_sparse_prefill_ex", "qsa_union_workspace_
             "qsa_sparse_prefill_noalloc", "qsa_probe_gather_ceiling",
             "qsa_sparse_prefill_paged", "qsa_sparse_mla_prefill", "qsa_select_mla_geometry",
             "qsa_page_mark", "qsa_page_split", "qsa_split_touched_pages",
-            "qsa_sparse_prefill_fp8", "qsa_debug_stall_next_call", "qsa_sparse_mla_prefill_paged"]
+            "qsa_sparse_prefill_fp8", "qsa_debug_stall_next_call", "qsa_sparse_mla_prefill_paged",
+            "qsa_sparse_prefill_fp8_paged"]
 
 # Size of the library-owned scratch array used by qsa_sparse_prefill_noalloc (include/qsa.h).
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -91,6 +92,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qsa_sparse_prefill_fp8.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, i64, i32, i32,
                                            i32, i32, f32, i32, i64, vp]
     lib.qsa_sparse_prefill_fp8.restype = ctypes.c_int
+    lib.qsa_sparse_prefill_fp8_paged.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, vp,
+                                                 i64, i32, i32, i32, i64, i32, i32, i32, i32, f32,
+                                                 i32, vp]
+    lib.qsa_sparse_prefill_fp8_paged.restype = ctypes.c_int
     lib.qsa_debug_stall_next_call.argtypes = []
     lib.qsa_debug_stall_next_call.restype = None
     lib.qsa_sparse_mla_prefill_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, i32,
@@ -235,6 +240,50 @@ def sparse_prefill_paged(q, k_cache, v_cache, indices, topk_len, cu_seqlens_q, k
                                       page_table.shape[1], int(page_size), int(n_pages), Hq, Hkv,
                                       D, topk, float(scale), int(union_g), _stream_ptr(stream))
     _check(st, "qsa_sparse_prefill_paged")
+    return out, lse
+
+
+def sparse_prefill_fp8_paged(q, k_cache, v_cache, k_scale, v_scale, fp8_page_size: int, indices,
+                             topk_len, cu_seqlens_q, kv_lens, page_table, page_size: int,
+                             scale: float, *, n_pages: int = 0, out=None, lse=None,
+                             union_g: int = 0, want_lse: bool = True, stream=None):
+    """FP8 caches over a paged pool (qsa_sparse_prefill_fp8_paged): the e4m3 caches and scales of
+    sparse_prefill_fp8 (scale granularity fp8_page_size) with the logical indices and page table
+    of sparse_prefill_paged (pool page size page_size)."""
+    import torch
+    lib = load_library()
+    _require(q, torch.bfloat16, "q", 3)
+    _require(k_cache, torch.uint8, "k_cache", 3)
+    _require(v_cache, torch.uint8, "v_cache", 3)
+    _require(k_scale, torch.float32, "k_scale", 2)
+    _require(v_scale, torch.float32, "v_scale", 2)
+    _require(indices, torch.int32, "indices", 2)
+    _require(topk_len, torch.int32, "topk_len", 1)
+    _require(cu_seqlens_q, torch.int32, "cu_seqlens_q", 1)
+    _require(kv_lens, torch.int32, "kv_lens", 1)
+    _require(page_table, torch.int32, "page_table", 2)
+    R, Hq, D = q.shape
+    Hkv = k_cache.shape[1]
+    topk = indices.shape[1]
+    n_req = page_table.shape[0]
+    if indices.shape[0] != R or (topk_len is not None and topk_len.shape[0] != R):
+        raise ValueError("indices / topk_len rows must match q")
+    if cu_seqlens_q.shape[0] != n_req + 1 or (kv_lens is not None and kv_lens.shape[0] != n_req):
+        raise ValueError("cu_seqlens_q / kv_lens must match the page table's requests")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((R, Hq), dtype=torch.float32, device=q.device)
+    _require(out, torch.bfloat16, "out", 3)
+    _require(lse, torch.float32, "lse", 2)
+    st = lib.qsa_sparse_prefill_fp8_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                          _ptr(v_scale), int(fp8_page_size), _ptr(indices),
+                                          _ptr(topk_len), _ptr(cu_seqlens_q), _ptr(kv_lens),
+                                          _ptr(page_table), _ptr(out), _ptr(lse), R, n_req,
+                                          page_table.shape[1], int(page_size), int(n_pages), Hq,
+                                          Hkv, D, topk, float(scale), int(union_g),
+                                          _stream_ptr(stream))
+    _check(st, "qsa_sparse_prefill_fp8_paged")
     return out, lse
 
 

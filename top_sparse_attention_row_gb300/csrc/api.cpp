@@ -669,6 +669,26 @@ qsa_status qsa_sparse_prefill_paged(const void* q, const void* k_cache, const vo
              head_dim, topk, scale, union_g, n_kv_slots, nullptr, 0, nullptr, &pa, stream);
 }
 
+qsa_status qsa_sparse_prefill_fp8_paged(const void* q, const void* k_cache, const void* v_cache,
+                                        const float* k_scale, const float* v_scale,
+                                        int32_t fp8_page_size, const int32_t* indices,
+                                        const int32_t* topk_len, const int32_t* cu_seqlens_q,
+                                        const int32_t* kv_lens, const int32_t* page_table,
+                                        void* out, float* lse, int64_t n_rows, int32_t n_requests,
+                                        int32_t pages_per_req, int32_t page_size, int64_t n_pages,
+                                        int32_t n_qheads, int32_t n_kvheads, int32_t head_dim,
+                                        int32_t topk, float scale, int32_t union_g, void* stream) {
+  if (!k_scale || !v_scale || fp8_page_size < 1) return QSA_ERR_INVALID_ARG;
+  qsa::PagedAddr pa{};
+  int64_t n_kv_slots = 0;
+  const qsa_status st = paged_args(cu_seqlens_q, kv_lens, page_table, n_requests, pages_per_req,
+                                   page_size, n_pages, n_kvheads, &pa, &n_kv_slots);
+  if (st != QSA_OK) return st;
+  const Fp8Cache f{k_scale, v_scale, fp8_page_size};
+  return run(q, k_cache, v_cache, indices, topk_len, out, lse, n_rows, n_qheads, n_kvheads,
+             head_dim, topk, scale, union_g, n_kv_slots, nullptr, 0, nullptr, &pa, stream, &f);
+}
+
 qsa_status qsa_sparse_mla_prefill_paged(const void* q, const void* kv_cache, const int32_t* indices,
                                         const int32_t* topk_len, const int32_t* cu_seqlens_q,
                                         const int32_t* kv_lens, const int32_t* page_table,
