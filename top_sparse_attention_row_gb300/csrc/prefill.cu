@@ -1335,8 +1335,9 @@ cudaError_t launch_prefill(const PrefillParams& p, const Geometry& g, const void
   }
   switch (g.np) {
     case 16: return u ? launch_np<16, true, false>(tk, tv, p, g, stream)
-                      : (g.cols <= 8 ? launch_np<16, false, false, 8>(tk, tv, p, g, stream)
-                                     : launch_np<16, false, false>(tk, tv, p, g, stream));
+                      : (g.cols <= 8    ? launch_np<16, false, false, 8>(tk, tv, p, g, stream)
+                         : g.cols <= 12 ? launch_np<16, false, false, 12>(tk, tv, p, g, stream)
+                                        : launch_np<16, false, false>(tk, tv, p, g, stream));
     case 32: return u ? launch_np<32, true, false>(tk, tv, p, g, stream) : launch_np<32, false, false>(tk, tv, p, g, stream);
     case 48: return u ? launch_np<48, true, false>(tk, tv, p, g, stream) : launch_np<48, false, false>(tk, tv, p, g, stream);
     case 64: return u ? launch_np<64, true, false>(tk, tv, p, g, stream) : launch_np<64, false, false>(tk, tv, p, g, stream);
