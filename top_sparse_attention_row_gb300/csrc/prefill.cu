@@ -897,10 +897,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const uint8_t* ub =
           UNION ? p.union_bits + static_cast<int64_t>(I.group) * p.union_g * p.topk : nullptr;
+      // Columns past the item's real ones start (and stay) at a finite max of 0, so that a tile
+      // whose slots are all valid can exponentiate every column without a -inf guard.
       float m_used[NP], l_part[NP];
 #pragma unroll
       for (int c = 0; c < NP; ++c) {
-        m_used[c] = NEG_INF;
+        m_used[c] = c < cols ? NEG_INF : 0.f;
         l_part[c] = 0.f;
       }
       // FP8 caches: P is stored in fp16 as p * v_scale with p <= 2^8 (the lazy rescale
@@ -951,15 +953,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_wait_ld();
         tc_fence_before();
         mbar_arrive(b_sfree + 8 * ss);
+        // A warp whose 32 slots are valid for every real column (all but a row's last tile and
+        // the union tiles with unowned slots) skips the per-column masking, and its P loop the
+        // -inf guard: its padding columns see S = 0 (Q's padding rows are zero), a finite max of 0
+        // and P = 1, and feed only O^T columns the epilogue never reads.
+        // (bf16 per-token instances only: in the union and FP8 instances the second copy of the
+        // loops cost registers and measured slower.)
+        constexpr bool kFastTiles = !UNION && !FP8;
+        const bool full = kFastTiles && __all_sync(0xffffffffu, vmask == allcols);
         bool need = false;
+        if (full) {
 #pragma unroll
-        for (int c = 0; c < NP; ++c) {
-          if (c >= SC) {   // no real column past SC: P stays zero there
-            x[c] = NEG_INF;
-            continue;
+          for (int c = 0; c < NP; ++c) {
+            if (c >= SC) {   // no real column past SC: P stays zero there
+              x[c] = NEG_INF;
+              continue;
+            }
+            x[c] *= logit_scale;
+            need |= x[c] > m_used[c] + kRescaleThreshold;
           }
-          x[c] = ((vmask >> c) & 1ull) ? x[c] * logit_scale : NEG_INF;
-          need |= x[c] > m_used[c] + kRescaleThreshold;
+        } else {
+#pragma unroll
+          for (int c = 0; c < NP; ++c) {
+            if (c >= SC) {
+              x[c] = NEG_INF;
+              continue;
+            }
+            x[c] = ((vmask >> c) & 1ull) ? x[c] * logit_scale : NEG_INF;
+            need |= x[c] > m_used[c] + kRescaleThreshold;
+          }
         }
         // One barrier per tile decides, uniformly for the 128 threads, whether the max moves
         // and whether some role gave up.
@@ -1031,15 +1053,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* pbuf = gbase + L.pbuf + sb * L.p_bytes;
         uint8_t* prow = pbuf + (t >> 6) * (NP * 128) + ((t & 7) << 1);
         const int tchunk = (t & 63) >> 3;
-#pragma unroll
-        for (int c = 0; c < SC; ++c) {
-          const float pv = x[c] == NEG_INF ? 0.f : fast_exp2(x[c] - m_used[c]);
+        auto store_p = [&](int c, float pv) {
           l_part[c] += pv;
           uint8_t* const dst = prow + (c >> 3) * 1024 + (c & 7) * 128 + ((tchunk ^ (c & 7)) << 4);
           if (FP8)
             *reinterpret_cast<__half*>(dst) = __float2half_rn(pv * v_scale);
           else
             *reinterpret_cast<__nv_bfloat16*>(dst) = __float2bfloat16_rn(pv);
+        };
+        if (full) {   // every x and every max is finite here (see above)
+#pragma unroll
+          for (int c = 0; c < SC; ++c) store_p(c, fast_exp2(x[c] - m_used[c]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < SC; ++c) store_p(c, x[c] == NEG_INF ? 0.f : fast_exp2(x[c] - m_used[c]));
         }
         fence_proxy_async_smem();
         tc_fence_before();
