@@ -33,16 +33,21 @@
 //    the two gather warps each rewrite 64 of its rows in place as fp16; the MMAs run fp16 operands,
 //    the K page scale multiplies the logit and the V page scale (normalised per item) the
 //    probability fed to P.V.
-//  * Online softmax in registers, one thread per slot (tensor-memory lane).  The running max
-//    is only raised when a tile's logits exceed it by more than 2^8 (log2 domain), so the
-//    O^T rescale through tensor memory is rare; the result is exact either way because O and
-//    the row sum use the same stale max.
+//  * Online softmax in registers, one thread per slot (tensor-memory lane), over the SC columns
+//    that can hold real heads (template SC <= NP: 8 or 12 for per-token N = 16 tiles).  The
+//    running max is only raised when a tile's logits exceed it by more than 2^8 (log2 domain),
+//    so the O^T rescale through tensor memory is rare; the result is exact either way because O
+//    and the row sum use the same stale max.
 //  * Warp roles (20 warps, five warpgroups): 0-3 softmax + epilogue; 4 MMA issue + tensor-memory
 //    owner; 5 index/Q loader (per-token: compacts the row's valid slots into shared memory);
 //    6, 7, 9-11, 13-19 gather, two per stage; 8 and 12 idle, so that the MMA warp's SM
-//    sub-partition (warp index mod 4) has one gather warp instead of three.  Warpgroup register
-//    reallocation (setmaxnreg) moves registers from the gather warpgroups to the softmax and
-//    MMA/index warpgroups.
+//    sub-partition (warp index mod 4) has one gather warp instead of three.  Per-token N = 16
+//    instances swap warps 5 and 16 (index on 16, at 64 registers), leaving that sub-partition
+//    with none.  Warpgroup register reallocation (setmaxnreg) moves registers from the gather
+//    warpgroups to the softmax and MMA/index warpgroups.  The MMA issue path builds operand
+//    descriptors as per-buffer 32-bit words plus constant offsets.
+//  * Per-token calls with fewer items than SMs split each row's tiles over a thread-block
+//    cluster and merge (max, row sum, O) through distributed shared memory (split > 1).
 //  * Every mbarrier wait is bounded (~2 s); a timeout records a code in a device status word,
 //    all roles leave their loops, in-flight copies and MMAs are drained, tensor memory is
 //    freed and the kernel returns.
