@@ -111,7 +111,9 @@ struct MlaItem {   // written by the index warp, read by every role
 
 }  // namespace
 
-template <int NP, bool UNION>
+// SC: query columns the softmax computes (SC < NP when an item's real columns fit in SC; the MMA
+// still runs N = NP, and P's columns past SC stay zero).
+template <int NP, bool UNION, int SC>
 __global__ void __launch_bounds__(kMlaThreads, 1)
     sparse_mla_kernel(const __grid_constant__ CUtensorMap tmKV, const __grid_constant__ MlaParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -595,6 +597,12 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
     uint32_t js = 0, it = 0, rb = 0;
     bool bad = false;
     const float NEG_INF = -INFINITY;
+    if constexpr (SC < NP) {
+      // P columns SC .. NP-1 are never written: zero both P buffers once (the MMA reads them)
+      for (int i = t; i < 2 * L.p_bytes / 16; i += 128)
+        mla_sts_v4(base + L.pbuf + 16 * i, make_uint4(0u, 0u, 0u, 0u));
+      fence_proxy_async_smem();
+    }
     for (;; ++it) {
       const uint32_t b = it & 1, ph = (it >> 1) & 1;
       bad |= !mla_wait(b_itemfull + 8 * b, ph, abort_flag, status, kMItemFull);
@@ -623,10 +631,11 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
       }
       const uint8_t* ub =
           UNION ? p.union_bits + static_cast<int64_t>(I.group) * p.union_g * p.topk : nullptr;
+      // columns past the real ones start at a finite max of 0 (see the fully valid tiles below)
       float m_used[NP], l_part[NP];
 #pragma unroll
       for (int c = 0; c < NP; ++c) {
-        m_used[c] = NEG_INF;
+        m_used[c] = c < cols ? NEG_INF : 0.f;
         l_part[c] = 0.f;
       }
       uint32_t bits_next = 0;
@@ -654,11 +663,31 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         tc_wait_ld();
         tc_fence_before();
         mbar_arrive(b_sfree + 8 * sb);
+        // As in the d=256 kernel: per-token warps whose slots are all valid skip the per-column
+        // masking and the -inf guard (padding columns see S = 0, a max of 0 and P = 1, feeding
+        // only unread O^T columns); columns past SC are not computed.
+        const bool full = !UNION && __all_sync(0xffffffffu, vmask == allcols);
         bool need = false;
+        if (full) {
 #pragma unroll
-        for (int c = 0; c < NP; ++c) {
-          x[c] = ((vmask >> c) & 1ull) ? x[c] * p.scale_log2 : NEG_INF;
-          need |= x[c] > m_used[c] + kMlaRescale;
+          for (int c = 0; c < NP; ++c) {
+            if (c >= SC) {
+              x[c] = NEG_INF;
+              continue;
+            }
+            x[c] *= p.scale_log2;
+            need |= x[c] > m_used[c] + kMlaRescale;
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < NP; ++c) {
+            if (c >= SC) {
+              x[c] = NEG_INF;
+              continue;
+            }
+            x[c] = ((vmask >> c) & 1ull) ? x[c] * p.scale_log2 : NEG_INF;
+            need |= x[c] > m_used[c] + kMlaRescale;
+          }
         }
         const int myvote = (need ? 1 : 0) | ((bad || *abort_flag) ? 2 : 0);
         if (myvote) atomicOr(&vote[jsj % 3], myvote);
@@ -717,13 +746,18 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
         uint8_t* pbuf = gbase + L.pbuf + sb * L.p_bytes;
         uint8_t* prow = pbuf + (t >> 6) * (NP * 128) + ((t & 7) << 1);
         const int tchunk = (t & 63) >> 3;
-#pragma unroll
-        for (int c = 0; c < NP; ++c) {
-          const float pv = x[c] == NEG_INF ? 0.f : fast_exp2(x[c] - m_used[c]);
+        auto store_p = [&](int c, float pv) {
           l_part[c] += pv;
           const __nv_bfloat16 pb16 = __float2bfloat16_rn(pv);
           *reinterpret_cast<__nv_bfloat16*>(prow + (c >> 3) * 1024 + (c & 7) * 128 +
                                             ((tchunk ^ (c & 7)) << 4)) = pb16;
+        };
+        if (full) {
+#pragma unroll
+          for (int c = 0; c < SC; ++c) store_p(c, fast_exp2(x[c] - m_used[c]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < SC; ++c) store_p(c, x[c] == NEG_INF ? 0.f : fast_exp2(x[c] - m_used[c]));
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -803,10 +837,10 @@ __global__ void __launch_bounds__(kMlaThreads, 1)
 
 namespace {
 
-template <int NP, bool UNION>
+template <int NP, bool UNION, int SC = NP>
 cudaError_t launch_mla_np(const CUtensorMap& tm, const MlaParams& p, const MlaGeometry& g,
                           cudaStream_t stream) {
-  auto kern = sparse_mla_kernel<NP, UNION>;
+  auto kern = sparse_mla_kernel<NP, UNION, SC>;
   static std::atomic<int> opted_in[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -830,7 +864,9 @@ cudaError_t launch_mla(const MlaParams& p, const MlaGeometry& g, const void* kv_
   if (e != cudaSuccess) return e;
   const bool u = p.union_g > 1;
   switch (g.np) {
-    case 16: return u ? launch_mla_np<16, true>(tm, p, g, stream) : launch_mla_np<16, false>(tm, p, g, stream);
+    case 16: return u ? launch_mla_np<16, true>(tm, p, g, stream)
+                      : (g.cols <= 8 ? launch_mla_np<16, false, 8>(tm, p, g, stream)
+                                     : launch_mla_np<16, false>(tm, p, g, stream));
     case 32: return u ? launch_mla_np<32, true>(tm, p, g, stream) : launch_mla_np<32, false>(tm, p, g, stream);
     default: return cudaErrorInvalidValue;
   }
