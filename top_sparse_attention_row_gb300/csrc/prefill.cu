@@ -168,6 +168,18 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
   return make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
                     bf16x2_to_f16x2(v.w));
 }
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  uint32_t r;
+  memcpy(&r, &v, 4);
+  return r;
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 v = __floats2half2_rn(lo, hi);
+  uint32_t r;
+  memcpy(&r, &v, 4);
+  return r;
+}
 __device__ __forceinline__ void sts_v4(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w)
@@ -295,6 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the FP8 per-token kernel 6 % on full-size calls (measured), through register allocation.
   constexpr bool kCanSplit = !UNION && !FP8 && NP <= kSplitMaxNPad;
   const int split = kCanSplit ? p.split : 1;
+  // P^T is stored MN-major (a slot's columns contiguous, one 16-byte store per eight columns)
+  // where N fits one 32- or 64-byte swizzle row; wider tiles keep the K-major 128-byte layout.
+  constexpr bool kPMnMajor = NP == 16 || NP == 32;
   const SmemLayout L = smem_layout(NP, p.stages, slot_cap, FP8, split);
   const int R = p.stages;
 
@@ -731,8 +746,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_inc<kRoleRegs>();
     constexpr uint32_t kIdescQK = FP8 ? idesc_f16_f32(128, NP, false, false)
                                       : idesc_bf16_f32(128, NP, false, false);
-    constexpr uint32_t kIdescPV = FP8 ? idesc_f16_f32(128, NP, true, false)
-                                      : idesc_bf16_f32(128, NP, true, false);
+    constexpr uint32_t kIdescPV = FP8 ? idesc_f16_f32(128, NP, true, kPMnMajor)
+                                      : idesc_bf16_f32(128, NP, true, kPMnMajor);
     uint32_t js = 0, it = 0;
     bool aborted = false;
     const bool cp_engine = !FP8 && p.gather_tma == 0;
@@ -745,7 +760,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t q_lo = sw128_desc_lo(base + L.qbuf, 16);
     const uint32_t ring_k_lo = sw128_desc_lo(base + L.ring, 16);          // K-major stage reads
     const uint32_t ring_v_lo = sw128_desc_lo(base + L.ring, 16384);       // MN-major stage reads
-    const uint32_t pbuf_lo = sw128_desc_lo(base + L.pbuf, 16);
+    // P^T MN-major (N = 16: 32-byte rows, N = 32: 64-byte rows; one row per slot): 8-slot
+    // groups kPSbo apart.  The leading offset is given the same value, so the operand stays
+    // inside its 16 slots under either reading of the two fields.
+    constexpr uint32_t kPSbo = 8 * NP * 2;
+    constexpr uint32_t kPHi = !kPMnMajor ? kHi : NP == 16 ? sw32_desc_hi(kPSbo) : sw64_desc_hi(kPSbo);
+    const uint32_t pbuf_lo = sw128_desc_lo(base + L.pbuf, kPMnMajor ? kPSbo : 16);
     uint32_t c_pair = 0, c_par = 0;
     auto advance = [&]() {
       if (++c_pair == n_pairs) {
@@ -827,8 +847,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t a_off = hh * kStageBytes + kk * 2048;
-                const uint32_t b_off = (kk >> 2) * (NP * 128) + (kk & 3) * 32;
-                tc_mma_w(tm_o + hh * NP, v_lo + (a_off >> 4), kHi, p_lo + (b_off >> 4), kHi, kIdescPV,
+                const uint32_t b_off = kPMnMajor ? kk * (16 * NP * 2)
+                                                 : (kk >> 2) * (NP * 128) + (kk & 3) * 32;
+                tc_mma_w(tm_o + hh * NP, v_lo + (a_off >> 4), kHi, p_lo + (b_off >> 4), kPHi, kIdescPV,
                          (jp == 0 && kk == 0) ? 0u : 1u);
               }
             }
@@ -1055,23 +1076,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // P buffer sb is free once the P.V of tile jsj-2 has completed.
         bad |= !wait_bar(b_pvdone + 8 * sb, sph ^ 1, abort_flag, kSitePvDone);
-        uint8_t* pbuf = gbase + L.pbuf + sb * L.p_bytes;
-        uint8_t* prow = pbuf + (t >> 6) * (NP * 128) + ((t & 7) << 1);
-        const int tchunk = (t & 63) >> 3;
-        auto store_p = [&](int c, float pv) {
-          l_part[c] += pv;
-          uint8_t* const dst = prow + (c >> 3) * 1024 + (c & 7) * 128 + ((tchunk ^ (c & 7)) << 4);
-          if (FP8)
-            *reinterpret_cast<__half*>(dst) = __float2half_rn(pv * v_scale);
-          else
-            *reinterpret_cast<__nv_bfloat16*>(dst) = __float2bfloat16_rn(pv);
-        };
         if (full) {   // every x and every max is finite here (see above)
 #pragma unroll
-          for (int c = 0; c < SC; ++c) store_p(c, fast_exp2(x[c] - m_used[c]));
+          for (int c = 0; c < SC; ++c) x[c] = fast_exp2(x[c] - m_used[c]);
         } else {
 #pragma unroll
-          for (int c = 0; c < SC; ++c) store_p(c, x[c] == NEG_INF ? 0.f : fast_exp2(x[c] - m_used[c]));
+          for (int c = 0; c < SC; ++c) x[c] = x[c] == NEG_INF ? 0.f : fast_exp2(x[c] - m_used[c]);
+        }
+#pragma unroll
+        for (int c = 0; c < SC; ++c) l_part[c] += x[c];
+        if constexpr (kPMnMajor) {
+          // This thread's slot is one row of P^T: its columns in 16-byte chunks (eight columns
+          // each; past SC zero), chunk i at position i ^ (address bits 7-8, or bit 7 for N = 16).
+          const uint32_t prow = base + L.pbuf + sb * L.p_bytes + t * (NP * 2);
+          const uint32_t sw = NP == 16 ? ((t >> 2) & 1) : ((t >> 1) & 3);
+#pragma unroll
+          for (int i = 0; i < (SC + 7) / 8; ++i) {
+            uint32_t w[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const int c = 8 * i + 2 * h;
+              const float a = c < SC ? x[c] : 0.f, b = c + 1 < SC ? x[c + 1] : 0.f;
+              w[h] = FP8 ? pack_f16x2(a * v_scale, b * v_scale) : pack_bf16x2(a, b);
+            }
+            sts_v4(prow + ((i ^ sw) << 4), make_uint4(w[0], w[1], w[2], w[3]));
+          }
+        } else {
+          uint8_t* pbuf = gbase + L.pbuf + sb * L.p_bytes;
+          uint8_t* prow = pbuf + (t >> 6) * (NP * 128) + ((t & 7) << 1);
+          const int tchunk = (t & 63) >> 3;
+#pragma unroll
+          for (int c = 0; c < SC; ++c) {
+            uint8_t* const dst = prow + (c >> 3) * 1024 + (c & 7) * 128 + ((tchunk ^ (c & 7)) << 4);
+            if (FP8)
+              *reinterpret_cast<__half*>(dst) = __float2half_rn(x[c] * v_scale);
+            else
+              *reinterpret_cast<__nv_bfloat16*>(dst) = __float2bfloat16_rn(x[c]);
+          }
         }
         fence_proxy_async_smem();
         tc_fence_before();
