@@ -168,6 +168,16 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
   return make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
                     bf16x2_to_f16x2(v.w));
 }
+// Shared-memory descriptor high words for the narrower swizzles (layout type 4 = SWIZZLE_64B,
+// 6 = SWIZZLE_32B; the low word as for 128 bytes).  An MN-major operand in these layouts has rows
+// of 64 (32) bytes, one per K index, in 8-row atoms of 512 (256) bytes, its 16-byte chunks XORed
+// with address bits 7-8 (bit 7).
+__host__ __device__ constexpr uint32_t sw64_desc_hi(uint32_t sbo) {
+  return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (4u << 29);
+}
+__host__ __device__ constexpr uint32_t sw32_desc_hi(uint32_t sbo) {
+  return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (6u << 29);
+}
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   uint32_t r;

@@ -174,15 +174,6 @@ __host__ __device__ constexpr uint32_t sw128_desc_hi(uint32_t sbo) {
 __device__ __forceinline__ uint32_t sw128_desc_lo(uint32_t saddr, uint32_t lbo) {
   return ((saddr & 0x3FFFFu) >> 4) | (((lbo >> 4) & 0x3FFFu) << 16);
 }
-// High words for the narrower swizzles (layout type 4 = SWIZZLE_64B, 6 = SWIZZLE_32B); the low
-// word is built as above.  An MN-major operand in these layouts has rows of 64 (32) bytes, one
-// per K index, in 8-row atoms of 512 (256) bytes, 16-byte chunks XORed with address bits 7-8 (7).
-__host__ __device__ constexpr uint32_t sw64_desc_hi(uint32_t sbo) {
-  return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (4u << 29);
-}
-__host__ __device__ constexpr uint32_t sw32_desc_hi(uint32_t sbo) {
-  return ((sbo >> 4) & 0x3FFFu) | (1u << 14) | (6u << 29);
-}
 __device__ __forceinline__ void tc_mma_w(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
                                          uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
