@@ -163,8 +163,8 @@ qsa_status qsa_sparse_prefill_paged(const void* q, const void* k_cache, const vo
 
 /* FP8 KV cache: K and V stored as e4m3 bytes with a fp32 scale per page and KV head, dequantised
  * in the gather ("DSA prefill ... triton_sparse_mla", Robustness and Accuracy Tests: the Triton
- * kernel refuses a packed FP8 pool and takes dequantised rows; flashinfer consumes the FP8 pool
- * with its scales).  The value of cache byte x at slot s, KV head h is
+ * kernel refuses a packed FP8 pool and takes dequantised rows; flashinfer reads the FP8 cache
+ * together with its scales).  The value of cache byte x at slot s, KV head h is
  *   e4m3(x) * k_scale[(s / page_size) * n_kvheads + h]      (v_scale likewise)
  * and the result is that of qsa_sparse_prefill on the dequantised caches.
  *   k_cache, v_cache [n_slots, n_kvheads, head_dim] e4m3 bytes (16-byte aligned)
@@ -173,7 +173,7 @@ qsa_status qsa_sparse_prefill_paged(const void* q, const void* k_cache, const vo
  * tensor cores run fp16 operands here: q is rounded to fp16 (|q| must stay below 65504), the
  * e4m3 values convert to fp16 exactly, and each slot's V scale multiplies its probability.
  * Query columns per tile are capped at 32: larger head groups run in head chunks, and unions
- * past 32 columns fall back to the per-token path (counted). */
+ * wider than 32 columns run as per-token calls instead (counted). */
 qsa_status qsa_sparse_prefill_fp8(const void* q, const void* k_cache, const void* v_cache,
                                   const float* k_scale, const float* v_scale, int32_t page_size,
                                   const int32_t* indices, const int32_t* topk_len, void* out,

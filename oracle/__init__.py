@@ -23,10 +23,12 @@ Functions and the passages they follow:
   ownership bitmask ("DSA prefill ... triton_sparse_mla", Modifications: each
   row's selection is sorted by itself, a slot joins the list through the first
   row holding it and carries one bit per owning row; Accuracy Tests: the dedup
-  contract -- listed once, bits = OR of owners, -1 dropped).
+  contract -- every slot appears one time, its bits are the union of the rows
+  that picked it, and padding is removed).
 * ``union.union_attention`` -- attention of each token of a group over the
-  union list restricted to its own ownership bit (same page: the bitmask
-  restores each token's own softmax support, identical to per-token).
+  union list restricted to its own ownership bit (same page: masking by the
+  ownership bit leaves every token exactly its own slots, so union and
+  per-token results agree).
 * ``paged.sparse_prefill_paged`` -- the same attention when each row's slots
   are logical positions of its request, read through a page table with
   ragged request metadata ("DSA prefill ... triton_sparse_mla", Robustness:

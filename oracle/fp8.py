@@ -3,8 +3,8 @@
 TEST INFRASTRUCTURE ONLY (see the package docstring).
 
 Pages: "DSA prefill ... triton_sparse_mla" (Robustness: the Triton kernel refuses a packed FP8
-pool; Accuracy Tests: flashinfer consumes the FP8 pool with its scales directly, this kernel
-takes the dequantised bf16 rows).  The plain reading of "dequantised": the value of cache byte x
+pool; Accuracy Tests: flashinfer reads the FP8 cache together with its scales, while the
+Triton kernel is handed rows already dequantised to bf16).  The plain reading of "dequantised": the value of cache byte x
 at slot s, KV head h is e4m3(x) * scale[s // page_size, h], and attention is the plain
 definition (attention.sparse_prefill) on those values.
 

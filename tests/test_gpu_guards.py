@@ -3,8 +3,8 @@
     canary bytes inside a larger allocation, and each entry point must leave the canaries intact
     while its payload still matches the oracle;
   * 64-bit addressing -- a batch whose O offsets pass 2^31 elements ("DSA prefill ...
-    triton_sparse_mla", Robustness: token offsets are 64-bit so a large batch at 64 or 128 heads
-    cannot wrap into another token's rows);
+    triton_sparse_mla", Robustness: offsets into the token rows are computed in 64 bits, so a big
+    batch with 64 or 128 heads never aliases a neighbouring token's output);
   * the union tail the pages single out: T = 1023 rows at G = 4."""
 import numpy as np
 import pytest

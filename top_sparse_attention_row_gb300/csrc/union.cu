@@ -4,7 +4,8 @@
 // index set.  Each row's selection is sorted by itself and its entries are looked up (a
 // lower_bound search) in the other rows' sorted lists; a slot enters the group's list through
 // the first row holding it and carries one ownership bit per row that selected it.  Accuracy
-// Tests on the same page give the contract: listed once, bits = OR of owners, -1 dropped.
+// Tests on the same page give the contract: every slot appears one time, its bits are the union
+// of the rows that picked it, and padding is removed.
 //
 // Two kernels produce the same lists, bits and lengths:
 //  * union_bitmap_kernel (the hot path): slot numbers are small integers, so each row's valid
