@@ -80,7 +80,7 @@ typedef struct qsa_geometry {
 
 /* Per-path call counters (host side, process wide), in the spirit of the pages' invocation
  * counts ("DSA prefill ... triton_sparse_mla", Speed Tests: every run counts invocations of
- * the kernel so a silent no-op cannot pass for a win). */
+ * the kernel, so that a path which quietly did nothing could not look like a speed-up). */
 typedef struct qsa_counters {
   uint64_t calls_per_token;    /* calls served by the per-token path */
   uint64_t calls_union;        /* calls served by the union path */

@@ -180,7 +180,7 @@ def make_group12(seed: int = 2, n_rows: int = 8192, context: int = 131072,
 
 def make_rows(n_rows: int, seed: int = 9) -> Workload:
     """Query-count sweep point: ``n_rows`` rows at the end of an 8192-token context (the rest a
-    prefix), group 6, topk 2051, so every row streams the full budget ("[QSA] Tune sm120 sparse
+    prefix), group 6, topk 2051, so each row gathers all 2051 of its slots ("[QSA] Tune sm120 sparse
     prefill geometry", Query-count sweep)."""
     return make_chunk(n_rows, 8192, 6, 1, 2051, seed + n_rows, f"rows{n_rows}_8k")
 
