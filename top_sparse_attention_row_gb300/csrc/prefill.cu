@@ -15,7 +15,8 @@
 //    query columns of the item (heads, or G x heads in union mode) are N, padded to 16 --
 //    instead of padding the head dimension up to the MMA M.
 //      S^T[128 x N]  = K_tile[128 x 256] . Q^T            (A: K-major SW128, B: K-major SW128)
-//      O^T[256 x N] += V_tile^T[256 x 128] . P^T[128 x N]  (A: MN-major SW128, B: K-major SW128)
+//      O^T[256 x N] += V_tile^T[256 x 128] . P^T[128 x N]  (A: MN-major SW128, B: MN-major SW32 /
+//                                                           SW64 for N = 16 / 32, else K-major SW128)
 //    Accumulators live in tensor memory: L + 1 S buffers (L = MMA lookahead: 1 per-token, 2
 //    union) and the two 128-row halves of O^T.
 //  * K/V rows are gathered into a ring of 32 KiB stages (128 slots x 128 dims, 128-byte
